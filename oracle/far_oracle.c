@@ -1,0 +1,334 @@
+/*
+ * CPU oracle for fused residual-add + RMSNorm under the mixed-precision
+ * rounding contract.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the
+ * CUDA path is checked against.  Only the tests, the smoke check and the CPU
+ * baseline leg of the bench may load it; the library itself never does, and
+ * it shares no code with the CUDA sources.
+ *
+ * What it computes, per row t of a [tokens, hidden] row-major matrix, follows
+ * the case study "Aligning fused RMSNorm rounding across vLLM backends":
+ *   section "Finding the rounding boundary" (the stage table) and
+ *   section "Implementation and tradeoffs":
+ *
+ *   s_i   = fl32(x_i + r_i)                  add in binary32, kept unrounded
+ *                                            (no-residual variant: s_i = x_i)
+ *   residual_out_i = RNE_act(s_i)            rounded only when stored
+ *   S     = RN32( sum_i fl32(s_i * s_i) )    squares in binary32; the sum is the
+ *                                            correctly rounded binary32 value of
+ *                                            the exact sum of those squares
+ *   var   = fl32(S / hidden)                 mean of the squares
+ *   rstd  = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   a_i   = fl32(s_i * rstd)                 normalised from the binary32 sum
+ *   n_i   = RNE_wd(a_i)                      cast to the weight dtype first ...
+ *   out_i = RNE_od(fl32(n_i * w_i))          ... then multiplied by the weight
+ *
+ * The dtype policy follows the LyCORIS page "Precision", section "Dtype
+ * policy": fp16, bf16 and fp32 may be combined freely except fp16 with bf16,
+ * which is rejected; the output dtype od is the promotion of the operands'
+ * dtypes (fp32 if either is fp32).
+ *
+ * Readings taken where the pages leave a step open:
+ *  - The sum of squares: the pages fix binary32 accumulation but let the
+ *    reduction order vary ("Testing the contract").  The oracle takes the one
+ *    order-free binary32 value, the correct rounding of the exact sum of the
+ *    binary32 squares, computed with an exact fixed-point accumulator.
+ *  - rstd is 1/sqrt with IEEE square root and IEEE division (eps inside the
+ *    root, as the "Mixed-Precision Kernels" page's layer-norm sketch places it).
+ *  - Rounding is to nearest, ties to even, everywhere; no flush to zero;
+ *    overflow of a 16-bit format gives infinity; NaN propagates.
+ *
+ * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math (binary32
+ * arithmetic must not be fused or reassociated).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+
+/* ------------------------------------------------------------------ */
+/* binary32 bits                                                       */
+/* ------------------------------------------------------------------ */
+
+static uint32_t bits_of(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float float_of(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/*
+ * Round a binary32 value to the nearest value of a narrower binary format
+ * (p significand bits including the leading one, normal exponents emin..emax,
+ * subnormals below), ties to even, overflow to infinity.  Every value of
+ * fp16 and bf16 is also a binary32 value, so the result is returned as one.
+ */
+static float round_to_format(float v, int p, int emin, int emax) {
+    if (isnan(v)) return v;
+    if (isinf(v) || v == 0.0f) return v;
+    uint32_t b = bits_of(v);
+    int negative = (int)(b >> 31);
+    int field = (int)((b >> 23) & 0xffu);
+    uint64_t m;   /* integer significand */
+    int e;        /* value = m * 2^e     */
+    if (field == 0) { m = b & 0x7fffffu; e = -149; }
+    else { m = (b & 0x7fffffu) | 0x800000u; e = field - 150; }
+    int lead = 63 - __builtin_clzll(m) + e;         /* exponent of the leading bit */
+    int q = (lead > emin ? lead : emin) - (p - 1);  /* exponent of the target's last place */
+    int drop = q - e;                                /* low bits that do not fit */
+    if (drop > 0) {
+        if (drop > 40) {
+            m = 0;                                   /* below half the smallest subnormal */
+        } else {
+            uint64_t keep = m >> drop;
+            uint64_t rest = m & ((1ull << drop) - 1);
+            uint64_t half = 1ull << (drop - 1);
+            if (rest > half || (rest == half && (keep & 1u))) keep += 1;
+            m = keep;
+        }
+        e = q;
+    }
+    double mag = ldexp((double)m, e);
+    if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;
+    float r = (float)mag;   /* exact: mag is a value of the target format, or infinity */
+    return negative ? -r : r;
+}
+
+static float round_f16(float v) { return round_to_format(v, 11, -14, 15); }
+static float round_bf16(float v) { return round_to_format(v, 8, -126, 127); }
+
+static float round_to(int dtype, float v) {
+    if (dtype == OR_F16) return round_f16(v);
+    if (dtype == OR_BF16) return round_bf16(v);
+    return v;
+}
+
+/* bits of a binary32 value that is exactly an fp16 value (or inf / NaN) */
+static uint16_t encode_f16(float v) {
+    uint32_t b = bits_of(v);
+    uint16_t sign = (uint16_t)((b >> 16) & 0x8000u);
+    if (isnan(v)) return (uint16_t)(sign | 0x7e00u);
+    if (isinf(v)) return (uint16_t)(sign | 0x7c00u);
+    if (v == 0.0f) return sign;
+    int e = (int)((b >> 23) & 0xffu) - 127;   /* fp16 values are normal binary32 values */
+    uint32_t m = (b & 0x7fffffu) | 0x800000u;
+    if (e >= -14) return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)((m >> 13) & 0x3ffu));
+    return (uint16_t)(sign | (uint16_t)(m >> (-e - 1)));  /* subnormal: v / 2^-24 */
+}
+
+static float decode_f16(uint16_t h) {
+    int negative = h >> 15;
+    int field = (h >> 10) & 0x1f;
+    int man = h & 0x3ff;
+    float v;
+    if (field == 31) v = man ? NAN : INFINITY;
+    else if (field == 0) v = ldexpf((float)man, -24);
+    else v = ldexpf((float)(1024 + man), field - 25);
+    return negative ? -v : v;
+}
+
+/* bits of a binary32 value that is exactly a bf16 value (or inf / NaN) */
+static uint16_t encode_bf16(float v) {
+    uint32_t b = bits_of(v);
+    if (isnan(v)) return (uint16_t)(((b >> 16) & 0x8000u) | 0x7fc0u);
+    return (uint16_t)(b >> 16);
+}
+
+static float decode_bf16(uint16_t h) { return float_of((uint32_t)h << 16); }
+
+static float load(const void* base, int dtype, int64_t i) {
+    if (dtype == OR_F16) return decode_f16(((const uint16_t*)base)[i]);
+    if (dtype == OR_BF16) return decode_bf16(((const uint16_t*)base)[i]);
+    return ((const float*)base)[i];
+}
+
+/* store a value that is already a value of `dtype` */
+static void store(void* base, int dtype, int64_t i, float v) {
+    if (dtype == OR_F16) ((uint16_t*)base)[i] = encode_f16(v);
+    else if (dtype == OR_BF16) ((uint16_t*)base)[i] = encode_bf16(v);
+    else ((float*)base)[i] = v;
+}
+
+/* ------------------------------------------------------------------ */
+/* exact sum of binary32 values                                        */
+/* ------------------------------------------------------------------ */
+
+/*
+ * Fixed-point accumulator: bit k of the integer has weight 2^(k-149), the
+ * last place of the smallest binary32 subnormal, so every finite binary32
+ * value is an integer here.  The largest finite value needs bit 277; ten
+ * 32-bit limbs (320 bits) leave room for more than 2^40 terms.
+ */
+#define ACC_LIMBS 10
+
+typedef struct {
+    uint32_t limb[ACC_LIMBS];
+    int has_nan, has_pinf, has_ninf;
+} exact_acc;
+
+static void acc_init(exact_acc* a) { memset(a, 0, sizeof *a); }
+
+/* add a non-negative binary32 value (the squares are never negative) */
+static void acc_add(exact_acc* a, float v) {
+    if (isnan(v)) { a->has_nan = 1; return; }
+    if (isinf(v)) { if (v > 0) a->has_pinf = 1; else a->has_ninf = 1; return; }
+    uint32_t b = bits_of(v) & 0x7fffffffu;
+    int field = (int)(b >> 23);
+    uint64_t m = b & 0x7fffffu;
+    int pos = 0;                             /* value = m * 2^(pos - 149) */
+    if (field != 0) { m |= 0x800000u; pos = field - 1; }
+    int k = pos / 32;
+    uint64_t chunk = m << (pos % 32);        /* at most 55 bits */
+    uint64_t carry = 0;
+    for (int j = k; j < ACC_LIMBS; ++j) {
+        uint64_t add = (j == k) ? (chunk & 0xffffffffu) : (j == k + 1) ? (chunk >> 32) : 0;
+        if (j > k + 1 && carry == 0) break;
+        uint64_t t = (uint64_t)a->limb[j] + add + carry;
+        a->limb[j] = (uint32_t)t;
+        carry = t >> 32;
+    }
+}
+
+static int acc_bit(const exact_acc* a, int k) { return (int)((a->limb[k / 32] >> (k % 32)) & 1u); }
+
+/* the accumulated exact sum, rounded to nearest binary32 (ties to even) */
+static float acc_round(const exact_acc* a) {
+    if (a->has_nan || (a->has_pinf && a->has_ninf)) return NAN;
+    if (a->has_pinf) return INFINITY;
+    if (a->has_ninf) return -INFINITY;
+    int top = -1;
+    for (int k = ACC_LIMBS * 32 - 1; k >= 0; --k)
+        if (acc_bit(a, k)) { top = k; break; }
+    if (top < 0) return 0.0f;
+    if (top < 24) {                           /* fewer than 24 bits: exact */
+        uint64_t n = 0;
+        for (int k = top; k >= 0; --k) n = (n << 1) | (uint64_t)acc_bit(a, k);
+        return (float)ldexp((double)n, -149);
+    }
+    uint64_t keep = 0;                        /* the 24 leading bits */
+    for (int k = top; k > top - 24; --k) keep = (keep << 1) | (uint64_t)acc_bit(a, k);
+    int guard = acc_bit(a, top - 24);
+    int sticky = 0;
+    for (int k = top - 25; k >= 0 && !sticky; --k) sticky = acc_bit(a, k);
+    if (guard && (sticky || (keep & 1u))) keep += 1;
+    double mag = ldexp((double)keep, top - 23 - 149);  /* exact in binary64 */
+    return (float)mag;  /* exact, or infinity when the rounded sum reaches 2^128 */
+}
+
+/* ------------------------------------------------------------------ */
+/* dtype policy                                                        */
+/* ------------------------------------------------------------------ */
+
+static int valid_dtype(int d) { return d == OR_F32 || d == OR_F16 || d == OR_BF16; }
+
+/* output dtype = promotion of act and wd; -1 for fp16 with bf16 or an unknown code */
+int oracle_output_dtype(int act, int wd) {
+    if (!valid_dtype(act) || !valid_dtype(wd)) return -1;
+    if ((act == OR_F16 && wd == OR_BF16) || (act == OR_BF16 && wd == OR_F16)) return -1;
+    if (act == OR_F32 || wd == OR_F32) return OR_F32;
+    return act;
+}
+
+/* ------------------------------------------------------------------ */
+/* the row                                                             */
+/* ------------------------------------------------------------------ */
+
+/* rstd of one row of binary32 sums s[0..hidden); also returns S and var */
+static float row_rstd(const float* s, int64_t hidden, float eps, float* S_out, float* var_out) {
+    exact_acc acc;
+    acc_init(&acc);
+    for (int64_t i = 0; i < hidden; ++i) {
+        float sq = s[i] * s[i];
+        acc_add(&acc, sq);
+    }
+    float S = acc_round(&acc);
+    float var = S / (float)hidden;
+    float tv = var + eps;
+    float root = sqrtf(tv);
+    float rstd = 1.0f / root;
+    if (S_out) *S_out = S;
+    if (var_out) *var_out = var;
+    return rstd;
+}
+
+static int run(const void* x, const void* residual, const void* weight, float eps,
+               void* out, void* residual_out, int64_t tokens, int64_t hidden,
+               int act, int wd, int has_residual) {
+    int od = oracle_output_dtype(act, wd);
+    if (od < 0) return -1;
+    if (tokens < 0 || hidden <= 0) return -2;
+    size_t sa = act == OR_F32 ? 4 : 2, so = od == OR_F32 ? 4 : 2;
+    float* s = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!s) return -3;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const char* xr = (const char*)x + (size_t)t * (size_t)hidden * sa;
+        const char* rr = has_residual ? (const char*)residual + (size_t)t * (size_t)hidden * sa : NULL;
+        char* orow = (char*)out + (size_t)t * (size_t)hidden * so;
+        char* rorow = has_residual ? (char*)residual_out + (size_t)t * (size_t)hidden * sa : NULL;
+        for (int64_t i = 0; i < hidden; ++i) {
+            float xf = load(xr, act, i);             /* widening is exact */
+            if (has_residual) {
+                float rf = load(rr, act, i);
+                s[i] = xf + rf;                      /* binary32 add, kept unrounded */
+                store(rorow, act, i, round_to(act, s[i]));
+            } else {
+                s[i] = xf;
+            }
+        }
+        float rstd = row_rstd(s, hidden, eps, NULL, NULL);
+        for (int64_t i = 0; i < hidden; ++i) {
+            float a = s[i] * rstd;                   /* from the binary32 sum */
+            float n = round_to(wd, a);               /* weight dtype first */
+            float prod = n * load(weight, wd, i);    /* then the weight */
+            store(orow, od, i, round_to(od, prod));
+        }
+    }
+    free(s);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* exported entry points (host pointers; same argument order as the    */
+/* library's, with the two dtypes passed separately)                   */
+/* ------------------------------------------------------------------ */
+
+int oracle_fused_add_rmsnorm(const void* x, const void* residual, const void* weight, float eps,
+                             void* out, void* residual_out, int64_t tokens, int64_t hidden,
+                             int act, int wd) {
+    return run(x, residual, weight, eps, out, residual_out, tokens, hidden, act, wd, 1);
+}
+
+int oracle_rmsnorm(const void* x, const void* weight, float eps, void* out,
+                   int64_t tokens, int64_t hidden, int act, int wd) {
+    return run(x, NULL, weight, eps, out, NULL, tokens, hidden, act, wd, 0);
+}
+
+/* per-row intermediates of the fused op: S, var and rstd (for pins) */
+int oracle_row_stats(const void* x, const void* residual, float eps, int64_t tokens, int64_t hidden,
+                     int act, float* S, float* var, float* rstd) {
+    size_t sa = act == OR_F32 ? 4 : 2;
+    float* s = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!s) return -3;
+    for (int64_t t = 0; t < tokens; ++t) {
+        const char* xr = (const char*)x + (size_t)t * (size_t)hidden * sa;
+        const char* rr = residual ? (const char*)residual + (size_t)t * (size_t)hidden * sa : NULL;
+        for (int64_t i = 0; i < hidden; ++i)
+            s[i] = rr ? load(xr, act, i) + load(rr, act, i) : load(xr, act, i);
+        rstd[t] = row_rstd(s, hidden, eps, &S[t], &var[t]);
+    }
+    free(s);
+    return 0;
+}
+
+/* correctly rounded binary32 sum of n non-negative binary32 values */
+float oracle_exact_sum(const float* v, int64_t n) {
+    exact_acc acc;
+    acc_init(&acc);
+    for (int64_t i = 0; i < n; ++i) acc_add(&acc, v[i]);
+    return acc_round(&acc);
+}
+
+/* format conversions, exposed so they can be pinned on their own */
+uint16_t oracle_f32_to_f16(float v) { return encode_f16(round_f16(v)); }
+uint16_t oracle_f32_to_bf16(float v) { return encode_bf16(round_bf16(v)); }
+float oracle_f16_to_f32(uint16_t h) { return decode_f16(h); }
+float oracle_bf16_to_f32(uint16_t h) { return decode_bf16(h); }

@@ -1,0 +1,110 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each mutant is a textual edit of a copy of the oracle's C source, compiled on
+the CPU into a temporary library; the pins of ``oracle_pins`` then run
+against it.  A mutant that no pin rejects means the pins cannot tell that
+mistake from the contract.  The first three are the defects the case study
+"Aligning fused RMSNorm rounding across vLLM backends" discusses (early
+rounding of the sum, and the two wrong orders of the weighted-output cast);
+the rest are the slips a plain implementation could make.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+SRC = open(oracle.SOURCE).read()
+
+MUTANTS = {
+    # the early-rounding defect: variance and normalisation from the rounded sum
+    "early_rounding": [("s[i] = xf + rf;", "s[i] = round_to(act, xf + rf);")],
+    # cast to the activation dtype instead of the weight dtype
+    "cast_to_act": [("float n = round_to(wd, a);", "float n = round_to(act, a);")],
+    # multiply by the weight before casting
+    "multiply_then_cast": [("float n = round_to(wd, a);", "float n = a;")],
+    "divisor_h_minus_1": [("float var = S / (float)hidden;",
+                           "float var = S / (float)(hidden > 1 ? hidden - 1 : 1);")],
+    "eps_dropped": [("float tv = var + eps;", "float tv = var;")],
+    "eps_outside_root": [("float tv = var + eps;", "float tv = var;"),
+                         ("float rstd = 1.0f / root;", "float rstd = 1.0f / root + eps;")],
+    "abs_not_square": [("float sq = s[i] * s[i];", "float sq = fabsf(s[i]);")],
+    "weight_index_shift": [("float prod = n * load(weight, wd, i);",
+                            "float prod = n * load(weight, wd, (i + 1) % hidden);")],
+    "residual_unrounded_store": [("store(rorow, act, i, round_to(act, s[i]));",
+                                  "store(rorow, act, i, s[i]);")],
+    "residual_reads_x_twice": [("float rf = load(rr, act, i);", "float rf = load(xr, act, i);")],
+    "negated_output": [("float a = s[i] * rstd;", "float a = -s[i] * rstd;")],
+    "ties_away_from_zero": [("if (rest > half || (rest == half && (keep & 1u))) keep += 1;",
+                             "if (rest >= half) keep += 1;")],
+    "sum_truncated": [("if (guard && (sticky || (keep & 1u))) keep += 1;", "")],
+    "sum_sequential_binary32": [("float S = acc_round(&acc);",
+                                 "float S = 0.0f; for (int64_t i = 0; i < hidden; ++i) S += s[i] * s[i];")],
+    "rstd_single_rounding": [("float root = sqrtf(tv);\n    float rstd = 1.0f / root;",
+                              "float root = sqrtf(tv);\n    float rstd = (float)(1.0 / sqrt((double)tv));")],
+    "out_row_stride_of_act": [("char* orow = (char*)out + (size_t)t * (size_t)hidden * so;",
+                               "char* orow = (char*)out + (size_t)t * (size_t)hidden * sa;")],
+    "no_residual_doubles_x": [("                s[i] = xf;\n", "                s[i] = xf + xf;\n")],
+    "f16_subnormal_encoding": [("return (uint16_t)(sign | (uint16_t)(m >> (-e - 1)));",
+                                "return (uint16_t)(sign | (uint16_t)(m >> (-e)));")],
+    # (">" instead of ">=" here would be an equivalent mutant: a value rounded to
+    # exactly 2^16 encodes as the fp16 infinity anyway, and no |a| reaches it)
+    "overflow_exponent_off_by_one": [("if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;",
+                                      "if (mag >= ldexp(1.0, emax)) mag = INFINITY;")],
+}
+
+
+@pytest.fixture(scope="module")
+def cases():
+    return P.pin_cases()
+
+
+def _mutant_lib(tmp_path, name, edits):
+    src = SRC
+    for old, new in edits:
+        assert src.count(old) == 1, f"mutant {name}: edit site not unique/found: {old!r}"
+        src = src.replace(old, new)
+    path = tmp_path / f"{name}.c"
+    path.write_text(src)
+    return oracle.bind(oracle.compile_oracle(str(path), str(tmp_path / f"lib{name}.so")))
+
+
+def _failed_pins(L, cases):
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            if pin in (P.pin_policy, P.pin_closed_forms):
+                pin(L)
+            else:
+                pin(L, cases)
+        except AssertionError:
+            failed.append(pin.__name__)
+        except (RuntimeError, ValueError):
+            failed.append(pin.__name__ + "(error)")
+    return failed
+
+
+def _extra_pin_checks(L):
+    """Converter pins on boundary values (the exhaustive sweep lives in its own test)."""
+    import test_oracle_converters as C
+    failed = []
+    for check in (C.check_page_format_facts, C.check_converter_boundaries):
+        try:
+            check(L)
+        except AssertionError:
+            failed.append(check.__name__)
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(tmp_path, cases, name):
+    L = _mutant_lib(tmp_path, name, MUTANTS[name])
+    failed = _failed_pins(L, cases) + _extra_pin_checks(L)
+    assert failed, f"no pin rejects the planted mistake {name!r}"
+
+
+def test_unmutated_copy_passes(tmp_path, cases):
+    L = _mutant_lib(tmp_path, "identity", [])
+    assert _failed_pins(L, cases) == []
+    assert _extra_pin_checks(L) == []
