@@ -1,0 +1,386 @@
+"""Bench: fused residual-add + RMSNorm (and its no-residual variant) on GB300.
+
+One step = one pass of the whole hot path over one batch of the fp16
+65536 x 8192 workload (the largest one-GPU workload; per-row log-uniform scales
+in [0.1, 10]): fused_add_rmsnorm(x, r, w) -> (out, residual_out), then
+rmsnorm(x, w) -> out2 on the same x.  Inputs are resident in HBM when the
+timed region starts; every tensor (1 GiB each) is far larger than the 129 MB
+L2, so no flush is needed between steps.
+
+Metric: achieved HBM GB/s from the algorithmic bytes (x, r, out, residual_out
+once each plus w once for the fused op; x, out2 plus w for the variant),
+tokens/s beside it.  Also reported: the end-to-end rate through the host-buffer
+entry points (copies inside the timed region), the dominant kernel's roofline
+from its own CUDA-event-timed launches, SM clocks sampled during the timed
+region, and the CPU oracle timed on the host cores as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl far|reference]
+Under torchrun each rank runs its own replica (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "achieved HBM GB/s and tokens/s of fused add+RMSNorm at 1 GB300 (% of HBM peak)"
+WORKLOAD = "c5"
+CSRC = os.path.join(ROOT, "mixed_precision_residual_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+DSIZE = {torch.float16: 2, torch.bfloat16: 2, torch.float32: 4}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["far", "reference"], default="far")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="time only the first N rows of the workload (profiling captures)")
+    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def step_bytes(tokens, hidden, act, wd, od):
+    """Algorithmic bytes of one step: (fused, variant)."""
+    sa, sw, so = DSIZE[act], DSIZE[wd], DSIZE[od]
+    fused = tokens * hidden * (2 * sa + sa + so) + hidden * sw
+    norm = tokens * hidden * (sa + so) + hidden * sw
+    return fused, norm
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def traffic_from_profile(workload: str):
+    """DRAM bytes per fused launch from a committed ncu summary, if the kernel sources still match."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed region
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sms, maxes, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sms.append(float(row[1]))
+                maxes.append(float(row[2]))
+                power.append(float(row[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, row[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sms) if sms else None, "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(sms),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+def cpu_baseline(d, seconds: float):
+    """The oracle, as it stands, on the first rows of the batch (fused + variant), host threads."""
+    import oracle
+
+    threads = oracle.default_threads()
+    H = d["hidden"]
+    act, wd = d["act"], d["wd"]
+    od = "f32" if "f32" in (act, wd) else act
+    rows_done, t0 = 0, time.perf_counter()
+    chunk = max(threads * 4, 64)
+    while time.perf_counter() - t0 < seconds and rows_done < d["tokens"]:
+        sl = slice(rows_done, min(d["tokens"], rows_done + chunk))
+        x, r = d["x"][sl], d["r"][sl]
+        oracle.fused_add_rmsnorm(x, r, d["w"], d["eps"], act, wd, threads=threads)
+        oracle.rmsnorm(x, d["w"], d["eps"], act, wd, threads=threads)
+        rows_done = sl.stop
+    el = time.perf_counter() - t0
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    fb, nb = step_bytes(rows_done, H, tdt[act], tdt[wd], tdt[od])
+    return {"value": round((fb + nb) / el / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "seconds": round(el, 2), "tokens_per_s": round(rows_done / el, 1),
+            "sample": f"first {rows_done} of {d['tokens']} rows of the {d['workload']} batch, fused add+RMSNorm "
+                      f"then the no-residual variant, oracle on {threads} host threads"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed on the host cores, each step a bounded row sample."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import far_gen
+    import oracle
+
+    w = far_gen.WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    probe = far_gen.make_inputs(w, rows=threads * 2)
+    t0 = time.perf_counter()
+    oracle.fused_add_rmsnorm(probe["x"], probe["r"], probe["w"], w.eps, w.act, w.wd, threads=threads)
+    oracle.rmsnorm(probe["x"], probe["w"], w.eps, w.act, w.wd, threads=threads)
+    per_row = (time.perf_counter() - t0) / (threads * 2)
+    budget = 120.0  # seconds for all steps
+    rows = int(max(threads, min(w.tokens, budget / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+    d = far_gen.make_inputs(w, rows=rows)
+    for _ in range(args.warmup):
+        oracle.fused_add_rmsnorm(d["x"], d["r"], d["w"], w.eps, w.act, w.wd, threads=threads)
+        oracle.rmsnorm(d["x"], d["w"], w.eps, w.act, w.wd, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.fused_add_rmsnorm(d["x"], d["r"], d["w"], w.eps, w.act, w.wd, threads=threads)
+        oracle.rmsnorm(d["x"], d["w"], w.eps, w.act, w.wd, threads=threads)
+    el = time.perf_counter() - t0
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    od = "f32" if "f32" in (w.act, w.wd) else w.act
+    fb, nb = step_bytes(rows, w.hidden, tdt[w.act], tdt[w.wd], tdt[od])
+    value = (fb + nb) * args.steps / el / 1e9
+    sample = (f"{rows} of {w.tokens} rows of the {w.name} batch per step (fused add+RMSNorm then the "
+              f"no-residual variant), oracle on {threads} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.act,
+            "data": "synthetic (seeded Philox4x32-10 generator)",
+            "config": {"workload": f"{w.name}: {w.note}", "tokens": w.tokens, "hidden": w.hidden,
+                       "act_dtype": w.act, "weight_dtype": w.wd, "eps": w.eps, "rows_per_step": rows},
+            "tokens_per_s": round(rows * args.steps / el, 1),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import far_gen
+    import mixed_precision_residual_gb300 as far
+
+    w = far_gen.WORKLOADS[args.workload]
+    d = far_gen.make_inputs(w, seed=rank, rows=args.tokens or None)  # each rank its own batch (replica)
+    dev = torch.device("cuda", local)
+    x, r, wt = d["x"].to(dev), d["r"].to(dev), d["w"].to(dev)
+    od = far.output_dtype(x.dtype, wt.dtype)
+    out = torch.empty(x.shape, dtype=od, device=dev)
+    res = torch.empty_like(x)
+    out2 = torch.empty(x.shape, dtype=od, device=dev)
+    T, H = x.shape
+    eps = d["eps"]
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    code = far.dtypes(x.dtype, wt.dtype)
+    L = far.lib
+    xp, rp, wp, op, rop, o2p = (t.data_ptr() for t in (x, r, wt, out, res, out2))
+
+    def step():
+        s1 = L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh)
+        s2 = L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh)
+        if s1 or s2:
+            raise RuntimeError(f"launch failed: {s1} {s2}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert far.device_status() == 0
+
+    ev_f0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_f1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev_start.record(stream)
+    for k in range(args.steps):
+        ev_f0[k].record(stream)
+        if L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh):
+            raise RuntimeError("fused launch failed")
+        ev_f1[k].record(stream)
+        if L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh):
+            raise RuntimeError("rmsnorm launch failed")
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    status = far.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    total_ms = ev_start.elapsed_time(ev_end)
+    fused_ms = sum(a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)) / args.steps
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od)
+    value = (fb + nb) * world / (ms_per_step * 1e-3) / 1e9
+    tokens_per_s = T * world / (ms_per_step * 1e-3)
+
+    # end to end through the host-buffer entry points: copies inside the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        xh, rh, wh = d["x"].pin_memory(), d["r"].pin_memory(), d["w"].pin_memory()
+        oh = torch.empty(x.shape, dtype=od, pin_memory=True)
+        roh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+        o2h = torch.empty(x.shape, dtype=od, pin_memory=True)
+        chunk = 4096
+        ws = torch.empty(far.host_workspace_bytes(chunk, H, x.dtype, wt.dtype, True), dtype=torch.uint8, device=dev)
+        wsb = ws.numel()
+        def e2e_step():
+            s1 = L.fused_add_rmsnorm_host(xh.data_ptr(), rh.data_ptr(), wh.data_ptr(), eps, oh.data_ptr(),
+                                          roh.data_ptr(), T, H, code, ws.data_ptr(), wsb, sh)
+            s2 = L.rmsnorm_host(xh.data_ptr(), wh.data_ptr(), eps, o2h.data_ptr(), T, H, code, ws.data_ptr(), wsb, sh)
+            if s1 or s2:
+                raise RuntimeError(f"host-buffer launch failed: {s1} {s2}")
+        e2e_step()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        sa, sw, so = DSIZE[x.dtype], DSIZE[wt.dtype], DSIZE[od]
+        h2d = T * H * sa * 2 + H * sw + T * H * sa + H * sw
+        d2h = T * H * so + T * H * sa + T * H * so
+        e2e = {"value": round((fb + nb) * world / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
+               "tokens_per_s": round(T * world / (e2e_ms * 1e-3), 1),
+               "path": "fused_add_rmsnorm_host + rmsnorm_host (pinned host buffers, 4096-row chunks, "
+                       "two internal streams)"}
+        assert far.device_status() == 0
+
+    peak, peak_kind = measured_peaks()
+    achieved = fb / (fused_ms * 1e-3) / 1e9
+    traffic = traffic_from_profile(args.workload)
+    plan = far.describe_launch(T, H, x.dtype, wt.dtype, True)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16" if x.dtype == torch.float16 else str(x.dtype),
+        "data": "synthetic (seeded Philox4x32-10 generator, per-row log-uniform scales)",
+        "config": {"workload": f"{w.name}: {w.note}", "tokens": T, "hidden": H,
+                   "act_dtype": w.act, "weight_dtype": w.wd, "out_dtype": w.act if od == x.dtype else "f32",
+                   "eps": eps, "step": "fused_add_rmsnorm then rmsnorm on the same x",
+                   "l2": "no flush: every tensor (1 GiB) is larger than the 129 MB L2",
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "gpu_launches": 2 * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "staged_kernel (fused add+RMSNorm)", "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": fb, "avg_launch_ms": round(fused_ms, 5),
+                     "launch_plan": plan},
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,150 @@
+/*
+ * far.h -- C ABI of the GB300 fused residual-add + RMSNorm library.
+ *
+ * The operation is the one the case study "Aligning fused RMSNorm rounding
+ * across vLLM backends" pins down (sections "Finding the rounding boundary"
+ * and "Implementation and tradeoffs"), per row t of a [tokens, hidden]
+ * row-major matrix:
+ *
+ *   s_i            = fl32(x_i + r_i)          binary32 add, never rounded before use
+ *   residual_out_i = RNE_act(s_i)             rounded only when stored
+ *   var            = fl32(S / hidden),        S = the binary32 sum of fl32(s_i * s_i)
+ *   rstd           = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   out_i          = RNE_od(fl32(RNE_wd(fl32(s_i * rstd)) * w_i))
+ *                                             cast to the weight dtype, then multiply
+ *
+ * The dtype policy is the one of the LyCORIS page "Precision", section
+ * "Dtype policy": activations (x, residual, residual_out: dtype `act`) and the
+ * weight (dtype `wd`) may each be fp16, bf16 or fp32, except fp16 together with
+ * bf16, which is a caller error; out has the promoted dtype od (fp32 if either
+ * is fp32, else the common 16-bit type).  Accumulation is binary32 throughout.
+ *
+ * Every entry point validates its arguments on the host first and returns a
+ * status without touching memory when they are wrong.  0 means the work was
+ * enqueued on `stream`; device faults surface at the caller's next
+ * synchronisation (CUDA convention).  There is no CPU fallback: a pointer the
+ * GPU cannot reach is a CUDA error, not a slow path.
+ *
+ * Memory: all tensors are caller-owned, contiguous and row-major (row stride =
+ * hidden elements).  The device entry points allocate nothing and keep no
+ * per-call state; they only enqueue on the stream they are given.
+ *
+ * Aliasing: an output may be the very same buffer as an input of the same
+ * element size (in-place use: out == x, residual_out == residual, ...).  Any
+ * other overlap between an output and any buffer is FAR_ERR_ALIAS.
+ */
+#ifndef FAR_H
+#define FAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+typedef enum { FAR_F32 = 0, FAR_F16 = 1, FAR_BF16 = 2 } far_dtype;
+
+/* the single `dtype` argument packs the activation and weight dtypes */
+#define FAR_DTYPES(act, w) ((int)(act) | ((int)(w) << 4))
+
+/* status codes */
+#define FAR_OK 0
+#define FAR_ERR_DTYPE_MIX 1  /* fp16 with bf16: a caller error under the dtype policy */
+#define FAR_ERR_DTYPE 2      /* an unknown dtype code */
+#define FAR_ERR_NULL 3       /* a required pointer is NULL (tokens > 0) */
+#define FAR_ERR_SHAPE 4      /* hidden <= 0 or > 2^24, tokens < 0, or byte sizes overflow */
+#define FAR_ERR_ALIAS 5      /* an output overlaps another buffer other than exactly */
+#define FAR_ERR_EPS 6        /* eps is negative or not finite */
+#define FAR_ERR_CUDA 7       /* a CUDA call failed; far_status_string gives its text */
+#define FAR_ERR_TIMEOUT 8    /* a bounded wait inside a kernel ran out (far_device_status) */
+#define FAR_ERR_WORKSPACE 9  /* the host-buffer entry points got too small a workspace */
+
+/*
+ * Fused residual add + RMSNorm.
+ *   x, residual     [tokens, hidden] act, device memory (read)
+ *   weight          [hidden] wd, device memory (read)
+ *   eps             added to the mean square inside the root (binary32)
+ *   out             [tokens, hidden] od, device memory (written)
+ *   residual_out    [tokens, hidden] act, device memory (written): RNE_act(x + r)
+ *   tokens, hidden  tokens >= 0 (0 is a no-op), 1 <= hidden <= 2^24
+ *   dtype           FAR_DTYPES(act, wd)
+ *   stream          cudaStream_t to enqueue on; NULL is the legacy default stream
+ * Returns FAR_OK or a status above.
+ */
+int fused_add_rmsnorm(const void* x, const void* residual, const void* weight, float eps,
+                      void* out, void* residual_out, int64_t tokens, int64_t hidden,
+                      int dtype, void* stream);
+
+/*
+ * RMSNorm without a residual: the same contract with s_i = x_i (exact
+ * widening) and no residual_out.  Arguments as for fused_add_rmsnorm.
+ */
+int rmsnorm(const void* x, const void* weight, float eps, void* out,
+            int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+/* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
+int far_output_dtype(int dtype);
+
+/* a static, human-readable text for a status (FAR_ERR_CUDA: the last CUDA error on this thread) */
+const char* far_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports and clears the device-side error word of
+ * the current device: FAR_ERR_TIMEOUT when a kernel gave up a bounded wait
+ * since the last call (its outputs are then incomplete), FAR_ERR_CUDA when the
+ * synchronisation itself failed, FAR_OK otherwise.
+ */
+int far_device_status(void* stream);
+
+/*
+ * End-to-end variants on HOST buffers: x, residual, weight, out and
+ * residual_out are host pointers (pinned memory for asynchronous copies;
+ * pageable memory works but the copies then block the calling thread).  The
+ * call streams row chunks through `workspace` (caller-owned device memory of
+ * `workspace_bytes`): host-to-device copy, kernel, device-to-host copy, with
+ * two internal streams so that copies in both directions overlap the kernels.
+ * Everything is ordered after the work already on `stream`, and work later
+ * enqueued on `stream` is ordered after all of it.  Returns FAR_OK once
+ * enqueued; the host outputs are valid after `stream` is synchronised.  Calls
+ * on one device are serialised by a lock (they share the internal streams).
+ */
+int64_t far_host_workspace_bytes(int64_t chunk_tokens, int64_t hidden, int dtype, int has_residual);
+
+int fused_add_rmsnorm_host(const void* x, const void* residual, const void* weight, float eps,
+                           void* out, void* residual_out, int64_t tokens, int64_t hidden,
+                           int dtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+int rmsnorm_host(const void* x, const void* weight, float eps, void* out, int64_t tokens,
+                 int64_t hidden, int dtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * Failure-detection self test: launches one tiny kernel that waits on a
+ * barrier nothing ever completes, with the same bounded wait the kernels use,
+ * limited to `timeout_us` microseconds (1 .. 10^7).  The wait runs out, the
+ * kernel records FAR_ERR_TIMEOUT in the device error word and returns, so a
+ * following far_device_status(stream) reports it and the context stays usable.
+ */
+int far_selftest_wait_timeout(uint32_t timeout_us, void* stream);
+
+/*
+ * Tuning hooks (the library's own choice is used when they are not called).
+ *
+ * far_set_launch_override: process-wide override of the launch plan, for
+ * measurements: kind -1 automatic, 0 staged kernel, 1 generic kernel; nch (16-byte
+ * chunks per thread: 1, 2, 4, 8), groups (rows in flight per CTA) and stages
+ * (shared-memory ring slots, 2..32) override the automatic choice when non-zero
+ * and feasible.  Returns FAR_ERR_SHAPE for out-of-range values.
+ *
+ * far_describe_launch: the plan the library would use for a call with
+ * 16-byte-aligned, non-overlapping buffers of this shape on the current device:
+ * out6 = {kind, nch, warps per row, groups, stages, grid}.
+ */
+int far_set_launch_override(int kind, int nch, int groups, int stages);
+int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAR_H */

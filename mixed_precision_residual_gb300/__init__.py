@@ -1,0 +1,181 @@
+"""GB300 fused residual-add + RMSNorm under the mixed-precision rounding contract.
+
+A thin ctypes binding of the C ABI in ``include/far.h`` (library
+``_build/libfar.so``, built for sm_103a by ``build.py``).  The functions keep
+the C names and only marshal arguments: every step of the computation runs in
+the library's CUDA kernels.  PyTorch provides device memory and streams.
+
+    out, residual_out = fused_add_rmsnorm(x, residual, weight, eps)
+    out = rmsnorm(x, weight, eps)
+
+There is no fallback: importing this package fails loudly when the library
+has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libfar.so")
+
+F32, F16, BF16 = 0, 1, 2
+STATUS = {0: "FAR_OK", 1: "FAR_ERR_DTYPE_MIX", 2: "FAR_ERR_DTYPE", 3: "FAR_ERR_NULL", 4: "FAR_ERR_SHAPE",
+          5: "FAR_ERR_ALIAS", 6: "FAR_ERR_EPS", 7: "FAR_ERR_CUDA", 8: "FAR_ERR_TIMEOUT",
+          9: "FAR_ERR_WORKSPACE"}
+FAR_OK, FAR_ERR_TIMEOUT = 0, 8
+TORCH_TO_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+CODE_TO_TORCH = {v: k for k, v in TORCH_TO_CODE.items()}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                      "(python -c 'import __graft_entry__ as g; g.build()')")
+
+lib = ctypes.CDLL(LIB_PATH)
+_vp, _f32, _i64, _int, _u32 = ctypes.c_void_p, ctypes.c_float, ctypes.c_int64, ctypes.c_int, ctypes.c_uint32
+lib.fused_add_rmsnorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _vp]
+lib.fused_add_rmsnorm.restype = _int
+lib.rmsnorm.argtypes = [_vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
+lib.rmsnorm.restype = _int
+lib.far_output_dtype.argtypes = [_int]
+lib.far_output_dtype.restype = _int
+lib.far_status_string.argtypes = [_int]
+lib.far_status_string.restype = ctypes.c_char_p
+lib.far_device_status.argtypes = [_vp]
+lib.far_device_status.restype = _int
+lib.far_host_workspace_bytes.argtypes = [_i64, _i64, _int, _int]
+lib.far_host_workspace_bytes.restype = _i64
+lib.fused_add_rmsnorm_host.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _vp, _i64, _vp]
+lib.fused_add_rmsnorm_host.restype = _int
+lib.rmsnorm_host.argtypes = [_vp, _vp, _f32, _vp, _i64, _i64, _int, _vp, _i64, _vp]
+lib.rmsnorm_host.restype = _int
+lib.far_selftest_wait_timeout.argtypes = [_u32, _vp]
+lib.far_selftest_wait_timeout.restype = _int
+lib.far_set_launch_override.argtypes = [_int, _int, _int, _int]
+lib.far_set_launch_override.restype = _int
+lib.far_describe_launch.argtypes = [_i64, _i64, _int, _int, _vp]
+lib.far_describe_launch.restype = _int
+
+
+class FarError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {lib.far_status_string(status).decode()}")
+
+
+def _check(status: int) -> None:
+    if status != FAR_OK:
+        raise FarError(status)
+
+
+def dtypes(act: torch.dtype, wd: torch.dtype) -> int:
+    """The packed dtype argument FAR_DTYPES(act, wd)."""
+    return TORCH_TO_CODE[act] | (TORCH_TO_CODE[wd] << 4)
+
+
+def output_dtype(act: torch.dtype, wd: torch.dtype) -> torch.dtype:
+    code = lib.far_output_dtype(dtypes(act, wd))
+    if code < 0:
+        raise FarError(-code)
+    return CODE_TO_TORCH[code]
+
+
+def _stream_handle(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _rows(x: torch.Tensor) -> tuple[int, int]:
+    hidden = x.shape[-1]
+    return (x.numel() // hidden if hidden else 0), hidden
+
+
+def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor, eps: float,
+                      out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None,
+                      stream=None):
+    """out, residual_out = RMSNorm(x + residual) * weight under the rounding contract.
+
+    x, residual: [..., hidden] contiguous CUDA tensors of one dtype; weight:
+    [hidden].  Outputs are allocated when not given (out in the promoted dtype);
+    pass out=x / residual_out=residual for in-place use.
+    """
+    if not (x.is_contiguous() and residual.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("x, residual and weight must be contiguous")
+    code = dtypes(x.dtype, weight.dtype)
+    if residual.dtype != x.dtype:
+        raise ValueError("x and residual must share a dtype")
+    if out is None:
+        out = torch.empty(x.shape, dtype=output_dtype(x.dtype, weight.dtype), device=x.device)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    tokens, hidden = _rows(x)
+    if weight.numel() != hidden or residual.shape != x.shape or out.shape != x.shape or residual_out.shape != x.shape:
+        raise ValueError("shape mismatch")
+    _check(lib.fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(out), _ptr(residual_out),
+                                 tokens, hidden, code, _stream_handle(stream)))
+    return out, residual_out
+
+
+def rmsnorm(x: torch.Tensor, weight: torch.Tensor, eps: float, out: torch.Tensor | None = None, stream=None):
+    """out = RMSNorm(x) * weight under the rounding contract (no residual)."""
+    if not (x.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("x and weight must be contiguous")
+    code = dtypes(x.dtype, weight.dtype)
+    if out is None:
+        out = torch.empty(x.shape, dtype=output_dtype(x.dtype, weight.dtype), device=x.device)
+    tokens, hidden = _rows(x)
+    if weight.numel() != hidden or out.shape != x.shape:
+        raise ValueError("shape mismatch")
+    _check(lib.rmsnorm(_ptr(x), _ptr(weight), eps, _ptr(out), tokens, hidden, code, _stream_handle(stream)))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word's status."""
+    return lib.far_device_status(_stream_handle(stream))
+
+
+def host_workspace_bytes(chunk_tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype,
+                         residual: bool = True) -> int:
+    n = lib.far_host_workspace_bytes(chunk_tokens, hidden, dtypes(act, wd), int(residual))
+    if n < 0:
+        raise FarError(-n)
+    return n
+
+
+def fused_add_rmsnorm_host(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor, eps: float,
+                           out: torch.Tensor, residual_out: torch.Tensor, workspace: torch.Tensor,
+                           stream=None) -> None:
+    """End-to-end call on host (CPU, ideally pinned) tensors through a device workspace."""
+    tokens, hidden = _rows(x)
+    _check(lib.fused_add_rmsnorm_host(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(out), _ptr(residual_out),
+                                      tokens, hidden, dtypes(x.dtype, weight.dtype), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+def rmsnorm_host(x: torch.Tensor, weight: torch.Tensor, eps: float, out: torch.Tensor, workspace: torch.Tensor,
+                 stream=None) -> None:
+    tokens, hidden = _rows(x)
+    _check(lib.rmsnorm_host(_ptr(x), _ptr(weight), eps, _ptr(out), tokens, hidden,
+                            dtypes(x.dtype, weight.dtype), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream)))
+
+
+def selftest_wait_timeout(timeout_us: int = 20000, stream=None) -> None:
+    _check(lib.far_selftest_wait_timeout(timeout_us, _stream_handle(stream)))
+
+
+def set_launch_override(kind: int = -1, nch: int = 0, groups: int = 0, stages: int = 0) -> None:
+    _check(lib.far_set_launch_override(kind, nch, groups, stages))
+
+
+def describe_launch(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool = True) -> dict:
+    buf = (ctypes.c_int * 6)()
+    _check(lib.far_describe_launch(tokens, hidden, dtypes(act, wd), int(residual), ctypes.addressof(buf)))
+    return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid"), list(buf)))

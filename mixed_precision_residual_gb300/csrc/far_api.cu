@@ -1,0 +1,525 @@
+// C ABI of the fused residual-add + RMSNorm library (declared in include/far.h):
+// host-side validation, the launch plan, the device error word, the
+// host-buffer (end-to-end) pipeline and the bounded-wait self test.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "far.h"
+#include "far_device.cuh"
+#include "far_params.h"
+
+namespace far {
+
+// Device error word: bit FAR_ERR_TIMEOUT is set by a kernel that gave up a
+// bounded wait.  Read and cleared by far_device_status.
+__device__ unsigned int g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxHidden = int64_t(1) << 24;  // (float)hidden must be exact
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  unsigned int* status = nullptr;  // device address of g_status on this device
+  // host-buffer pipeline: two internal streams and the events that fork/join them
+  bool pipe_ready = false;
+  cudaStream_t pipe[2] = {nullptr, nullptr};
+  cudaEvent_t fork = nullptr, wready = nullptr, join[2] = {nullptr, nullptr};
+  std::mutex pipe_mu;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+thread_local char g_cuda_msg[256] = "CUDA error";
+
+int cuda_fail(cudaError_t e) {
+  snprintf(g_cuda_msg, sizeof g_cuda_msg, "CUDA error %d: %s", (int)e, cudaGetErrorString(e));
+  return FAR_ERR_CUDA;
+}
+
+int current_device(DeviceState*& st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+  st = &g_dev[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!st->ready) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    void* addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    st->sms = sms;
+    st->status = static_cast<unsigned int*>(addr);
+    st->ready = true;
+  }
+  return FAR_OK;
+}
+
+// tuning override of the staged plan (0 = automatic), process-wide
+std::atomic<int> g_force_nch{0}, g_force_groups{0}, g_force_stages{0}, g_force_kind{-1};
+
+int decode(int dtype, int& act, int& wd, int& od) {
+  if (dtype < 0 || (dtype >> 8) != 0) return FAR_ERR_DTYPE;
+  act = dtype & 0xf;
+  wd = (dtype >> 4) & 0xf;
+  auto known = [](int d) { return d == FAR_F32 || d == FAR_F16 || d == FAR_BF16; };
+  if (!known(act) || !known(wd)) return FAR_ERR_DTYPE;
+  if ((act == FAR_F16 && wd == FAR_BF16) || (act == FAR_BF16 && wd == FAR_F16)) return FAR_ERR_DTYPE_MIX;
+  od = promote(act, wd);
+  return FAR_OK;
+}
+
+int dsize(int dt) { return dt == FAR_F32 ? 4 : 2; }
+
+bool overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  uint64_t pa = (uint64_t)(uintptr_t)a, pb = (uint64_t)(uintptr_t)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+// an output may coincide exactly with an input of the same size; nothing else may overlap it
+bool bad_overlap(const void* o, uint64_t no, const void* in, uint64_t nin) {
+  if (!overlap(o, no, in, nin)) return false;
+  return !(o == in && no == nin);
+}
+
+struct Call {
+  const void* x;
+  const void* r;
+  const void* w;
+  float eps;
+  void* out;
+  void* res_out;
+  int64_t tokens, hidden;
+  int act, wd, od;
+  bool residual;
+};
+
+int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
+             int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c) {
+  int st = decode(dtype, c.act, c.wd, c.od);
+  if (st != FAR_OK) return st;
+  if (hidden <= 0 || hidden > kMaxHidden || tokens < 0) return FAR_ERR_SHAPE;
+  // byte sizes must fit in int64 (and in the kernels' 64-bit offsets)
+  if (tokens > (INT64_MAX / 8) / hidden) return FAR_ERR_SHAPE;
+  if (!(eps >= 0.0f) || eps == INFINITY) return FAR_ERR_EPS;
+  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual};
+  if (tokens == 0) return FAR_OK;
+  if (!x || !w || !out || (residual && (!r || !res_out))) return FAR_ERR_NULL;
+  const uint64_t na = (uint64_t)tokens * hidden * dsize(c.act);
+  const uint64_t no = (uint64_t)tokens * hidden * dsize(c.od);
+  const uint64_t nw = (uint64_t)hidden * dsize(c.wd);
+  if (bad_overlap(out, no, x, na) || overlap(out, no, w, nw)) return FAR_ERR_ALIAS;
+  if (residual) {
+    if (bad_overlap(out, no, r, na) || overlap(out, no, res_out, na)) return FAR_ERR_ALIAS;
+    if (bad_overlap(res_out, na, x, na) || bad_overlap(res_out, na, r, na) || overlap(res_out, na, w, nw))
+      return FAR_ERR_ALIAS;
+  }
+  return FAR_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// the launch plan for a validated call
+int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) {
+  memset(&L, 0, sizeof L);
+  Params& p = L.p;
+  p.x = c.x;
+  p.r = c.r;
+  p.w = c.w;
+  p.out = c.out;
+  p.res_out = c.res_out;
+  p.tokens = c.tokens;
+  p.hidden = (int32_t)c.hidden;
+  p.hidden_f = (float)c.hidden;
+  p.eps = c.eps;
+  p.status = dev.status;
+  p.timeout_ns = kWaitTimeoutNs;
+  L.stream = stream;
+
+  const int sa = dsize(c.act), sw = dsize(c.wd);
+  const int64_t row_bytes = c.hidden * sa;
+  bool staged = g_force_kind.load() != kGeneric && row_bytes % 16 == 0 && aligned16(c.x) &&
+                aligned16(c.w) && aligned16(c.out) && (!c.residual || (aligned16(c.r) && aligned16(c.res_out)));
+  int nch = 0, G = 0, groups = 0, stages = 0;
+  uint32_t stage_bytes = 0, w_bytes = (uint32_t)((c.hidden * sw + 15) / 16 * 16);
+  size_t smem = 0;
+  if (staged) {
+    const int64_t C = row_bytes / 16;
+    const int V = 16 / sa;
+    // about 32 elements per thread: 4 chunks of 16-bit data, 8 of binary32
+    nch = (V == 8) ? 4 : 8;
+    if (C <= 32LL * nch) {  // one warp covers the row: no more chunks per thread than needed
+      nch = 1;
+      while (32LL * nch < C) nch *= 2;
+    }
+    G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+    if (G > kMaxConsumerWarps && nch < 8) {
+      nch = 8;
+      G = (int)((C + 255) / 256);
+    }
+    if (g_force_nch.load() > 0) {
+      nch = g_force_nch.load();
+      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+    }
+    staged = G <= kMaxConsumerWarps;
+    if (staged) {
+      groups = kMaxConsumerWarps / G;
+      const int64_t per_sm = (c.tokens + dev.sms - 1) / dev.sms;  // rows per SM if spread evenly
+      if (groups > per_sm) groups = (int)(per_sm > 0 ? per_sm : 1);
+      if (g_force_groups.load() > 0) groups = g_force_groups.load() * G <= kMaxConsumerWarps ? g_force_groups.load() : groups;
+      stage_bytes = (uint32_t)(((row_bytes + 127) / 128 * 128) * (c.residual ? 2 : 1));
+      // as many ring slots as fit (at most 32): more slots, more bytes in flight per SM
+      stages = 32;
+      while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes) > (size_t)kMaxDynamicSmem)
+        --stages;
+      const int forced = g_force_stages.load();
+      if (forced >= 2 && forced <= stages) stages = forced;
+      if (stages < 2) {
+        staged = false;
+      } else {
+        if (groups > stages) groups = stages;
+        smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes);
+      }
+    }
+  }
+  if (staged) {
+    L.kind = kStaged;
+    L.nch = nch;
+    p.chunks = (int32_t)(row_bytes / 16);
+    p.warps_per_row = G;
+    p.groups = groups;
+    p.stages = stages;
+    p.row_bytes = (uint32_t)row_bytes;
+    p.w_smem_bytes = w_bytes;
+    p.stage_bytes = stage_bytes;
+    int64_t grid = (c.tokens + groups - 1) / groups;
+    if (grid > dev.sms) grid = dev.sms;
+    L.grid = dim3((unsigned)grid);
+    L.block = dim3((unsigned)((1 + groups * G) * 32));
+    L.smem = smem;
+  } else {
+    L.kind = kGeneric;
+    int64_t grid = c.tokens < (int64_t)dev.sms * 8 ? c.tokens : (int64_t)dev.sms * 8;
+    L.grid = dim3((unsigned)grid);
+    L.block = dim3(kGenericThreads);
+    L.smem = 0;
+  }
+  return FAR_OK;
+}
+
+int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
+  if (c.tokens == 0) return FAR_OK;
+  Launch L;
+  int st = plan(c, dev, stream, L);
+  if (st != FAR_OK) return st;
+  cudaError_t e;
+  switch (c.act) {
+    case FAR_F16: e = launch_act_f16(c.wd, c.residual, L); break;
+    case FAR_BF16: e = launch_act_bf16(c.wd, c.residual, L); break;
+    default: e = launch_act_f32(c.wd, c.residual, L); break;
+  }
+  return e == cudaSuccess ? FAR_OK : cuda_fail(e);
+}
+
+int run(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
+        int64_t hidden, int dtype, bool residual, void* stream) {
+  Call c;
+  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  if (st != FAR_OK || tokens == 0) return st;
+  DeviceState* dev = nullptr;
+  st = current_device(dev);
+  if (st != FAR_OK) return st;
+  return launch(c, *dev, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// host-buffer pipeline
+// ---------------------------------------------------------------------------
+
+int64_t align256(int64_t n) { return (n + 255) / 256 * 256; }
+
+struct HostLayout {
+  int64_t w_bytes, x_bytes, o_bytes;  // per chunk of `rows` rows
+  int64_t total;
+};
+
+HostLayout host_layout(int64_t rows, int64_t hidden, int act, int wd, int od, bool residual) {
+  HostLayout h;
+  h.w_bytes = align256(hidden * dsize(wd));
+  h.x_bytes = align256(rows * hidden * dsize(act));
+  h.o_bytes = align256(rows * hidden * dsize(od));
+  // per slot: x, (residual, residual_out), out
+  int64_t slot = h.x_bytes * (residual ? 3 : 1) + h.o_bytes;
+  h.total = h.w_bytes + 2 * slot;
+  return h;
+}
+
+int ensure_pipe(DeviceState& d) {
+  if (d.pipe_ready) return FAR_OK;
+  for (int i = 0; i < 2; ++i) {
+    cudaError_t e = cudaStreamCreateWithFlags(&d.pipe[i], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaEventCreateWithFlags(&d.join[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  cudaError_t e = cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaEventCreateWithFlags(&d.wready, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_fail(e);
+  d.pipe_ready = true;
+  return FAR_OK;
+}
+
+int run_host(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
+             int64_t hidden, int dtype, bool residual, void* workspace, int64_t ws_bytes, void* stream) {
+  Call c;
+  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  if (st != FAR_OK || tokens == 0) return st;
+  if (!workspace) return FAR_ERR_NULL;
+  if (!aligned16(workspace)) return FAR_ERR_WORKSPACE;
+  // the largest chunk of rows whose two slots fit the workspace (the layout grows with rows)
+  if (host_layout(1, hidden, c.act, c.wd, c.od, residual).total > ws_bytes) return FAR_ERR_WORKSPACE;
+  int64_t lo = 1, hi = tokens;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo + 1) / 2;
+    if (host_layout(mid, hidden, c.act, c.wd, c.od, residual).total <= ws_bytes) lo = mid;
+    else hi = mid - 1;
+  }
+  const int64_t rows = lo;
+  DeviceState* dev = nullptr;
+  st = current_device(dev);
+  if (st != FAR_OK) return st;
+  std::lock_guard<std::mutex> lk(dev->pipe_mu);
+  st = ensure_pipe(*dev);
+  if (st != FAR_OK) return st;
+
+  const HostLayout lay = host_layout(rows, hidden, c.act, c.wd, c.od, residual);
+  char* base = static_cast<char*>(workspace);
+  char* w_dev = base;
+  char* slot_base[2] = {base + lay.w_bytes, base + lay.w_bytes + (lay.total - lay.w_bytes) / 2};
+  const int64_t sa = dsize(c.act), so = dsize(c.od);
+  cudaStream_t caller = static_cast<cudaStream_t>(stream);
+
+  cudaError_t e = cudaEventRecord(dev->fork, caller);
+  for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(dev->pipe[i], dev->fork, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(w_dev, w, hidden * dsize(c.wd), cudaMemcpyHostToDevice, dev->pipe[0]);
+  if (e == cudaSuccess) e = cudaEventRecord(dev->wready, dev->pipe[0]);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(dev->pipe[1], dev->wready, 0);
+  if (e != cudaSuccess) return cuda_fail(e);
+
+  int64_t chunk = 0;
+  for (int64_t t0 = 0; t0 < tokens; t0 += rows, ++chunk) {
+    const int64_t n = (tokens - t0 < rows) ? tokens - t0 : rows;
+    const int s = (int)(chunk & 1);
+    cudaStream_t ps = dev->pipe[s];
+    char* xd = slot_base[s];
+    char* od = xd + lay.x_bytes;
+    char* rd = od + lay.o_bytes;
+    char* rod = rd + lay.x_bytes;
+    const int64_t in_off = t0 * hidden * sa, out_off = t0 * hidden * so;
+    e = cudaMemcpyAsync(xd, static_cast<const char*>(x) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
+    if (e == cudaSuccess && residual)
+      e = cudaMemcpyAsync(rd, static_cast<const char*>(r) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
+    if (e != cudaSuccess) return cuda_fail(e);
+    Call cc = c;
+    cc.x = xd;
+    cc.r = residual ? rd : nullptr;
+    cc.w = w_dev;
+    cc.out = od;
+    cc.res_out = residual ? rod : nullptr;
+    cc.tokens = n;
+    st = launch(cc, *dev, ps);
+    if (st != FAR_OK) return st;
+    e = cudaMemcpyAsync(static_cast<char*>(out) + out_off, od, n * hidden * so, cudaMemcpyDeviceToHost, ps);
+    if (e == cudaSuccess && residual)
+      e = cudaMemcpyAsync(static_cast<char*>(res_out) + in_off, rod, n * hidden * sa, cudaMemcpyDeviceToHost, ps);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  for (int i = 0; i < 2; ++i) {
+    e = cudaEventRecord(dev->join[i], dev->pipe[i]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(caller, dev->join[i], 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return FAR_OK;
+}
+
+// ---------------------------------------------------------------------------
+// bounded-wait self test
+// ---------------------------------------------------------------------------
+
+__global__ void wait_selftest_kernel(unsigned int* status, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the wait runs out and records the time-out
+  if (threadIdx.x == 0) mbar_wait(smem_addr(&bar), 0u, timeout_ns, status);
+}
+
+std::mutex g_attr_mu;
+std::set<std::pair<const void*, int>> g_attr_done;
+
+}  // namespace
+
+cudaError_t ensure_smem_attribute(const void* func, size_t bytes) {
+  (void)bytes;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_attr_mu);
+  if (g_attr_done.count({func, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+  if (e == cudaSuccess) g_attr_done.insert({func, dev});
+  return e;
+}
+
+cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace far
+
+using namespace far;
+
+extern "C" {
+
+int fused_add_rmsnorm(const void* x, const void* residual, const void* weight, float eps, void* out,
+                      void* residual_out, int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  return run(x, residual, weight, eps, out, residual_out, tokens, hidden, dtype, true, stream);
+}
+
+int rmsnorm(const void* x, const void* weight, float eps, void* out, int64_t tokens, int64_t hidden, int dtype,
+            void* stream) {
+  return run(x, nullptr, weight, eps, out, nullptr, tokens, hidden, dtype, false, stream);
+}
+
+int far_output_dtype(int dtype) {
+  int act, wd, od;
+  int st = decode(dtype, act, wd, od);
+  return st == FAR_OK ? od : -st;
+}
+
+const char* far_status_string(int status) {
+  switch (status) {
+    case FAR_OK: return "ok";
+    case FAR_ERR_DTYPE_MIX: return "fp16 mixed with bf16 is rejected by the dtype policy";
+    case FAR_ERR_DTYPE: return "unknown dtype code";
+    case FAR_ERR_NULL: return "a required pointer is NULL";
+    case FAR_ERR_SHAPE: return "invalid shape (hidden must be 1..2^24, tokens >= 0)";
+    case FAR_ERR_ALIAS: return "an output overlaps another buffer (only exact in-place aliasing is allowed)";
+    case FAR_ERR_EPS: return "eps must be finite and non-negative";
+    case FAR_ERR_CUDA: return g_cuda_msg;
+    case FAR_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out; its outputs are incomplete";
+    case FAR_ERR_WORKSPACE: return "workspace too small or misaligned for one row";
+    default: return "unknown status";
+  }
+}
+
+int far_device_status(void* stream) {
+  DeviceState* dev = nullptr;
+  int st = current_device(dev);
+  if (st != FAR_OK) return st;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int word = 0;
+  e = cudaMemcpy(&word, dev->status, sizeof word, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (word != 0) {
+    e = cudaMemset(dev->status, 0, sizeof word);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return (word & (1u << FAR_ERR_TIMEOUT)) ? FAR_ERR_TIMEOUT : FAR_OK;
+}
+
+int64_t far_host_workspace_bytes(int64_t chunk_tokens, int64_t hidden, int dtype, int has_residual) {
+  int act, wd, od;
+  int st = decode(dtype, act, wd, od);
+  if (st != FAR_OK) return -st;
+  if (chunk_tokens <= 0 || hidden <= 0 || hidden > kMaxHidden) return -FAR_ERR_SHAPE;
+  return host_layout(chunk_tokens, hidden, act, wd, od, has_residual != 0).total;
+}
+
+int fused_add_rmsnorm_host(const void* x, const void* residual, const void* weight, float eps, void* out,
+                           void* residual_out, int64_t tokens, int64_t hidden, int dtype, void* workspace,
+                           int64_t workspace_bytes, void* stream) {
+  return run_host(x, residual, weight, eps, out, residual_out, tokens, hidden, dtype, true, workspace,
+                  workspace_bytes, stream);
+}
+
+int rmsnorm_host(const void* x, const void* weight, float eps, void* out, int64_t tokens, int64_t hidden,
+                 int dtype, void* workspace, int64_t workspace_bytes, void* stream) {
+  return run_host(x, nullptr, weight, eps, out, nullptr, tokens, hidden, dtype, false, workspace,
+                  workspace_bytes, stream);
+}
+
+int far_selftest_wait_timeout(uint32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000u) return FAR_ERR_SHAPE;
+  DeviceState* dev = nullptr;
+  int st = current_device(dev);
+  if (st != FAR_OK) return st;
+  cudaError_t e = launch_wait_selftest(dev->status, (uint64_t)timeout_us * 1000ull, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FAR_OK : cuda_fail(e);
+}
+
+int far_set_launch_override(int kind, int nch, int groups, int stages) {
+  if (kind < -1 || kind > 1 || (nch != 0 && nch != 1 && nch != 2 && nch != 4 && nch != 8) || groups < 0 ||
+      groups > kMaxConsumerWarps || stages < 0 || stages > 32)
+    return FAR_ERR_SHAPE;
+  g_force_kind = kind;
+  g_force_nch = nch;
+  g_force_groups = groups;
+  g_force_stages = stages;
+  return FAR_OK;
+}
+
+int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6) {
+  // kind, nch, warps_per_row, groups, stages, grid -- for a call with 16-byte-aligned buffers
+  Call c;
+  // distinct, aligned, non-overlapping stand-in addresses: only the plan is computed
+  const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
+  const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;
+  const void* x = base;
+  const void* r = base + span;
+  const void* w = base + 2 * span;
+  void* o = const_cast<char*>(base + 3 * span);
+  void* ro = const_cast<char*>(base + 4 * span);
+  int st = validate(x, has_residual ? r : nullptr, w, 1e-6f, o, has_residual ? ro : nullptr, tokens, hidden,
+                    dtype, has_residual != 0, c);
+  if (st != FAR_OK) return st;
+  if (tokens == 0) return FAR_ERR_SHAPE;
+  DeviceState* dev = nullptr;
+  st = current_device(dev);
+  if (st != FAR_OK) return st;
+  Launch L;
+  st = plan(c, *dev, nullptr, L);
+  if (st != FAR_OK) return st;
+  out6[0] = L.kind;
+  out6[1] = L.nch;
+  out6[2] = L.p.warps_per_row;
+  out6[3] = L.p.groups;
+  out6[4] = L.p.stages;
+  out6[5] = (int)L.grid.x;
+  return FAR_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,279 @@
+// Kernels for fused residual-add + RMSNorm and its no-residual variant.
+//
+// staged_kernel -- the hot path.  Persistent (one CTA per SM), warp-specialised:
+//   warp 0, lane 0 (producer) bulk-copies each row of x and of the residual into
+//   a ring of shared-memory slots (cp.async.bulk, mbarrier completion, plain
+//   copies into the CTA's own shared memory);
+//   `groups` groups of G consumer warps each take a row from the ring: every
+//   thread widens its 16-byte chunks, forms s = fl32(x + r) and keeps s in
+//   registers, accumulates the squares, releases the slot, reduces across the
+//   warp (shuffles) and the group (shared memory + mbarrier), then normalises
+//   from the registers and streams residual_out and out to HBM.
+//   So every input byte is read from HBM once and the binary32 sum is never
+//   re-read; every output byte is written once.
+//
+// generic_kernel -- any alignment and any hidden size: one CTA per row
+//   (grid-stride), scalar accesses, the row re-read in the second pass (from
+//   L1/L2).  Same arithmetic, same results.
+//
+// The rounding steps are the ones the case study "Aligning fused RMSNorm
+// rounding across vLLM backends" fixes (stage table of "Finding the rounding
+// boundary"): s kept in binary32, residual rounded only on store, variance and
+// normalisation from s, the normalised value cast to the weight dtype before
+// the weight multiply.
+#pragma once
+
+#include "far_device.cuh"
+
+namespace far {
+
+template <int ACT, int WD, bool RES, int NCH>
+__global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) {
+  constexpr int SA = dtype_size<ACT>::value;
+  constexpr int SW = dtype_size<WD>::value;
+  constexpr int OD = promote(ACT, WD);
+  constexpr int SO = dtype_size<OD>::value;
+  constexpr int V = 16 / SA;   // elements per 16-byte activation chunk
+  constexpr int WB = V * SW;   // weight bytes per chunk: 8, 16 or 32
+  constexpr int OB = V * SO;   // output bytes per chunk: 16 or 32
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
+  // layout: full[stages] | empty[stages] | reduce[groups][2] | partials[groups][2][G] | w | ring
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+  float2* partials = reinterpret_cast<float2*>(smem + (size_t)(2 * stages + 2 * groups) * 8);
+  const size_t head = ((size_t)(2 * stages + 2 * groups) * 8 + (size_t)groups * 2 * G * 8 + 127) / 128 * 128;
+  unsigned char* wsm = smem + head;
+  unsigned char* ring = wsm + (p.w_smem_bytes + 127) / 128 * 128;
+  const uint32_t r_off = (p.row_bytes + 127u) & ~127u;  // residual row inside a slot
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(smem_addr(&bars[i]), 1);           // full: the producer's arrive + bytes
+      mbar_init(smem_addr(&bars[stages + i]), G);  // empty: one arrive per consumer warp
+    }
+    for (int i = 0; i < 2 * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
+    fence_barrier_init();
+  }
+  {  // the weight row, once per CTA (16-byte aligned; hidden * SW is even)
+    const int nbytes = p.hidden * SW;
+    const int n16 = nbytes >> 4;
+    const uint4* src = reinterpret_cast<const uint4*>(p.w);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(wsm)[i] = src[i];
+    const uint16_t* src2 = reinterpret_cast<const uint16_t*>(p.w);
+    for (int i = (n16 << 3) + threadIdx.x; i < (nbytes >> 1); i += blockDim.x)
+      reinterpret_cast<uint16_t*>(wsm)[i] = src2[i];
+  }
+  __syncthreads();
+
+  const int64_t b = blockIdx.x, nb = gridDim.x;
+  const int64_t n_local = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t tx = RES ? 2u * p.row_bytes : p.row_bytes;
+      int64_t k = 0;
+      for (; k < n_local; ++k) {
+        const int slot = (int)(k % stages);
+        if (k >= stages &&
+            !mbar_wait(smem_addr(&bars[stages + slot]), (uint32_t)((k / stages) - 1) & 1u, p.timeout_ns,
+                       p.status))
+          break;
+        const int64_t row = b + k * nb;
+        const uint32_t full = smem_addr(&bars[slot]);
+        const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
+        mbar_arrive_expect_tx(full, tx);
+        bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full, pol);
+        if constexpr (RES)
+          bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full, pol);
+      }
+      // the copies of the last (at most `stages`) rows must have landed before the CTA may exit
+      for (int64_t j = (k > stages ? k - stages : 0); j < k; ++j)
+        mbar_wait(smem_addr(&bars[j % stages]), (uint32_t)(j / stages) & 1u, p.timeout_ns, p.status);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int cw = warp - 1;
+  const int g = cw / G, wg = cw - g * G;
+  const int C = p.chunks;
+  int64_t it = 0;  // this group's row count, for the reduction buffers
+  for (int64_t k = g; k < n_local; k += groups, ++it) {
+    const int slot = (int)(k % stages);
+    if (!mbar_wait(smem_addr(&bars[slot]), (uint32_t)(k / stages) & 1u, p.timeout_ns, p.status)) return;
+    const unsigned char* xs = ring + (size_t)slot * p.stage_bytes;
+
+    // pass 1 (from shared memory): s = fl32(x + r) into registers, squares into the accumulator
+    float s[NCH][V];
+    DW acc0{0.f, 0.f}, acc1{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = (j * G + wg) * 32 + lane;
+      if (c < C) {
+        uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
+        float xf[V];
+        widen<ACT, V>(reinterpret_cast<const uint32_t*>(&xv), xf);
+        if constexpr (RES) {
+          uint4 rv = *reinterpret_cast<const uint4*>(xs + r_off + (size_t)c * 16);
+          float rf[V];
+          widen<ACT, V>(reinterpret_cast<const uint32_t*>(&rv), rf);
+#pragma unroll
+          for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(xf[e], rf[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) s[j][e] = xf[e];
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const float q = __fmul_rn(s[j][e], s[j][e]);
+          if (e & 1) dw_add(acc1, q); else dw_add(acc0, q);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) s[j][e] = 0.f;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&bars[stages + slot]));  // the slot may be refilled
+
+    DW acc = dw_warp_allreduce(dw_combine(acc0, acc1));
+    if (G > 1) {
+      const int buf = (int)(it & 1);
+      float2* part = partials + (size_t)(g * 2 + buf) * G;
+      const uint32_t rbar = smem_addr(&bars[2 * stages + g * 2 + buf]);
+      if (lane == 0) {
+        part[wg] = make_float2(acc.hi, acc.lo);
+        mbar_arrive(rbar);
+      }
+      if (!mbar_wait(rbar, (uint32_t)(it >> 1) & 1u, p.timeout_ns, p.status)) return;
+      DW tot{part[0].x, part[0].y};
+      for (int i = 1; i < G; ++i) tot = dw_combine(tot, DW{part[i].x, part[i].y});
+      acc = tot;
+    }
+    const float rstd = row_rstd(dw_value(acc), p.hidden_f, p.eps);
+
+    // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w)
+    const int64_t row = b + k * nb;
+    char* orow = static_cast<char*>(p.out) + row * (int64_t)p.hidden * SO;
+    char* rrow = RES ? static_cast<char*>(p.res_out) + row * (int64_t)p.row_bytes : nullptr;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int c = (j * G + wg) * 32 + lane;
+      if (c < C) {
+        uint32_t ww[WB / 4];
+        load_bytes<WB>(wsm + (size_t)c * WB, ww);
+        float wf[V];
+        widen<WD, V>(ww, wf);
+        float o[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] = __fmul_rn(s[j][e], rstd);
+        round_through<WD, V>(o);  // cast to the weight dtype first
+#pragma unroll
+        for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
+        uint32_t ow[OB / 4];
+        narrow<OD, V>(o, ow);
+        store_bytes_stream<OB>(orow + (size_t)c * OB, ow);
+        if constexpr (RES) {
+          uint32_t rw[4];
+          narrow<ACT, V>(s[j], rw);
+          store_bytes_stream<16>(rrow + (size_t)c * 16, rw);
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// generic path: any alignment, any hidden size
+// ---------------------------------------------------------------------------
+
+template <int DT> __device__ __forceinline__ float load_elem(const void* base, int64_t i) {
+  if constexpr (DT == FAR_F16) return __half2float(static_cast<const __half*>(base)[i]);
+  else if constexpr (DT == FAR_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+  else return static_cast<const float*>(base)[i];
+}
+
+// store a binary32 value rounded to nearest even in dtype DT
+template <int DT> __device__ __forceinline__ void store_elem(void* base, int64_t i, float v) {
+  if constexpr (DT == FAR_F16) static_cast<__half*>(base)[i] = __float2half_rn(v);
+  else if constexpr (DT == FAR_BF16) static_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  else static_cast<float*>(base)[i] = v;
+}
+
+template <int DT> __device__ __forceinline__ float round_one(float v) {
+  if constexpr (DT == FAR_F16) return __half2float(__float2half_rn(v));
+  else if constexpr (DT == FAR_BF16) return __bfloat162float(__float2bfloat16_rn(v));
+  else return v;
+}
+
+template <int ACT, int WD, bool RES>
+__global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p) {
+  constexpr int SA = dtype_size<ACT>::value;
+  constexpr int OD = promote(ACT, WD);
+  constexpr int SO = dtype_size<OD>::value;
+  constexpr int NW = kGenericThreads / 32;
+  __shared__ float2 part[NW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t H = p.hidden;
+  for (int64_t row = blockIdx.x; row < p.tokens; row += gridDim.x) {
+    const char* xr = static_cast<const char*>(p.x) + row * H * SA;
+    const char* rr = RES ? static_cast<const char*>(p.r) + row * H * SA : nullptr;
+    DW acc{0.f, 0.f};
+    for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+      float s = load_elem<ACT>(xr, i);
+      if constexpr (RES) s = __fadd_rn(s, load_elem<ACT>(rr, i));
+      dw_add(acc, __fmul_rn(s, s));
+    }
+    acc = dw_warp_allreduce(acc);
+    if (lane == 0) part[warp] = make_float2(acc.hi, acc.lo);
+    __syncthreads();
+    DW tot{part[0].x, part[0].y};
+    for (int i = 1; i < NW; ++i) tot = dw_combine(tot, DW{part[i].x, part[i].y});
+    __syncthreads();  // `part` is reused by the next row
+    const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
+    char* orow = static_cast<char*>(p.out) + row * H * SO;
+    char* rrow = RES ? static_cast<char*>(p.res_out) + row * H * SA : nullptr;
+    for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+      float s = load_elem<ACT>(xr, i);  // each element is read and written by the same thread
+      if constexpr (RES) {
+        s = __fadd_rn(s, load_elem<ACT>(rr, i));
+        store_elem<ACT>(rrow, i, s);
+      }
+      const float n = round_one<WD>(__fmul_rn(s, rstd));
+      store_elem<OD>(orow, i, __fmul_rn(n, load_elem<WD>(p.w, i)));
+    }
+  }
+}
+
+cudaError_t ensure_smem_attribute(const void* func, size_t bytes);
+
+template <int ACT, int WD, bool RES>
+cudaError_t launch_typed(const Launch& L) {
+  void (*k)(Params) = nullptr;
+  if (L.kind == kGeneric) {
+    k = generic_kernel<ACT, WD, RES>;
+  } else {
+    switch (L.nch) {
+      case 1: k = staged_kernel<ACT, WD, RES, 1>; break;
+      case 2: k = staged_kernel<ACT, WD, RES, 2>; break;
+      case 4: k = staged_kernel<ACT, WD, RES, 4>; break;
+      case 8: k = staged_kernel<ACT, WD, RES, 8>; break;
+      default: return cudaErrorInvalidValue;
+    }
+    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);
+    if (e != cudaSuccess) return e;
+  }
+  k<<<L.grid, L.block, L.smem, L.stream>>>(L.p);
+  return cudaGetLastError();
+}
+
+template <int ACT, int WD>
+cudaError_t launch_res(bool residual, const Launch& L) {
+  return residual ? launch_typed<ACT, WD, true>(L) : launch_typed<ACT, WD, false>(L);
+}
+
+}  // namespace far

@@ -1,0 +1,66 @@
+// Kernel parameters and the per-activation-dtype launchers shared between the
+// C-ABI translation unit and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace far {
+
+// shapes of the staged kernel: a CTA = 1 producer warp + groups x warps_per_row consumer warps
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+constexpr int kMaxDynamicSmem = 227 * 1024;
+constexpr int kGenericThreads = 256;
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+
+struct Params {
+  const void* x;
+  const void* r;         // residual (unused by the no-residual variant)
+  const void* w;         // weight [hidden]
+  void* out;             // [tokens, hidden] od
+  void* res_out;         // [tokens, hidden] act (unused by the no-residual variant)
+  int64_t tokens;
+  int32_t hidden;
+  float hidden_f;        // (float)hidden, exact for hidden <= 2^24
+  float eps;
+  int32_t chunks;        // 16-byte chunks per activation row (staged kernel)
+  int32_t warps_per_row; // G (staged kernel)
+  int32_t groups;        // rows processed concurrently per CTA (staged kernel)
+  int32_t stages;        // shared-memory ring slots (staged kernel)
+  uint32_t row_bytes;    // hidden * sizeof(act)
+  uint32_t w_smem_bytes; // hidden * sizeof(wd), rounded up to 16
+  uint32_t stage_bytes;  // bytes of one ring slot (x row, then residual row), 128-aligned
+  unsigned int* status;  // device error word
+  uint64_t timeout_ns;
+};
+
+enum Kind { kStaged = 0, kGeneric = 1 };
+
+struct Launch {
+  Params p;
+  int kind;
+  int nch;  // 16-byte chunks per thread (staged kernel): 1, 2, 4 or 8
+  dim3 grid, block;
+  size_t smem;
+  cudaStream_t stream;
+};
+
+// shared-memory bytes the staged kernel needs for a plan
+inline size_t staged_smem_bytes(int stages, int groups, int warps_per_row, uint32_t w_smem_bytes,
+                                uint32_t stage_bytes) {
+  size_t bars = (size_t)(2 * stages + 2 * groups) * 8;
+  size_t red = (size_t)groups * 2 * warps_per_row * 8;
+  size_t head = (bars + red + 127) / 128 * 128;
+  return head + (w_smem_bytes + 127) / 128 * 128 + (size_t)stages * stage_bytes;
+}
+
+// one launcher per activation dtype (each in its own translation unit)
+cudaError_t launch_act_f16(int wd, bool residual, const Launch& L);
+cudaError_t launch_act_bf16(int wd, bool residual, const Launch& L);
+cudaError_t launch_act_f32(int wd, bool residual, const Launch& L);
+
+// the bounded-wait self test (far_api.cu)
+cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);
+
+}  // namespace far

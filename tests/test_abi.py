@@ -1,0 +1,126 @@
+"""The C-ABI library: it loads, exports every symbol include/*.h declares, and
+its host-side validation returns the documented statuses.  No compute runs
+here: every call below is rejected (or is a no-op) before any CUDA call."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def far():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixed_precision_residual_gb300 as far
+
+    return far
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)  # drop comments
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M):
+            if m.group(1) not in ("defined",):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("fused_add_rmsnorm", "rmsnorm", "far_output_dtype", "far_status_string",
+                     "far_device_status", "fused_add_rmsnorm_host", "rmsnorm_host"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(far):
+    lib = ctypes.CDLL(far.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+D = {"f32": 0, "f16": 1, "bf16": 2}
+
+
+def code(a, w):
+    return D[a] | (D[w] << 4)
+
+
+def test_output_dtype_policy(far):
+    L = far.lib
+    assert L.far_output_dtype(code("f16", "bf16")) == -1  # -FAR_ERR_DTYPE_MIX
+    assert L.far_output_dtype(code("bf16", "f16")) == -1
+    assert L.far_output_dtype(code("bf16", "bf16")) == D["bf16"]
+    assert L.far_output_dtype(code("f16", "f16")) == D["f16"]
+    for a in ("f16", "bf16", "f32"):
+        assert L.far_output_dtype(code(a, "f32")) == D["f32"]
+        assert L.far_output_dtype(code("f32", a)) == D["f32"]
+    assert L.far_output_dtype(3) == -2 and L.far_output_dtype(0x100) == -2 and L.far_output_dtype(-1) == -2
+
+
+FAKE = 1 << 40  # never dereferenced: every call below fails validation first
+
+
+def call(far, x=FAKE, r=FAKE + (1 << 30), w=FAKE + (2 << 30), eps=1e-6, out=FAKE + (3 << 30),
+         ro=FAKE + (4 << 30), tokens=4, hidden=64, dtype=None):
+    dtype = code("bf16", "bf16") if dtype is None else dtype
+    return far.lib.fused_add_rmsnorm(x, r, w, eps, out, ro, tokens, hidden, dtype, None)
+
+
+def test_validation_statuses(far):
+    assert call(far, dtype=code("f16", "bf16")) == 1   # FAR_ERR_DTYPE_MIX
+    assert call(far, dtype=code("bf16", "f16")) == 1
+    assert call(far, dtype=7) == 2                      # FAR_ERR_DTYPE
+    assert call(far, x=None) == 3                       # FAR_ERR_NULL
+    assert call(far, w=None) == 3
+    assert call(far, ro=None) == 3
+    assert call(far, hidden=0) == 4                     # FAR_ERR_SHAPE
+    assert call(far, hidden=(1 << 24) + 1) == 4
+    assert call(far, tokens=-1) == 4
+    assert call(far, tokens=1 << 62, hidden=1 << 20) == 4
+    assert call(far, eps=-1e-6) == 6                    # FAR_ERR_EPS
+    assert call(far, eps=float("nan")) == 6
+    assert call(far, eps=float("inf")) == 6
+    # aliasing: exact in-place is allowed, partial overlap is not
+    assert call(far, out=FAKE + 2) == 5                 # out overlaps x partially
+    assert call(far, ro=FAKE + (1 << 30) + 64) == 5     # residual_out overlaps residual partially
+    assert call(far, out=FAKE + (4 << 30)) == 5         # out == residual_out
+    assert call(far, out=FAKE + (2 << 30)) == 5         # out overlaps the weight
+    assert call(far, dtype=code("bf16", "f32"), out=FAKE) == 5  # fp32 out cannot alias a bf16 x
+    # no-residual variant
+    assert far.lib.rmsnorm(FAKE, FAKE + (2 << 30), 1e-6, FAKE + 2, 4, 64, code("f16", "f16"), None) == 5
+    assert far.lib.rmsnorm(FAKE, None, 1e-6, FAKE + (3 << 30), 4, 64, code("f16", "f16"), None) == 3
+    assert far.lib.rmsnorm(FAKE, FAKE + (2 << 30), 1e-6, FAKE + (3 << 30), 4, 64, code("f16", "bf16"), None) == 1
+
+
+def test_zero_tokens_is_a_noop(far):
+    assert call(far, tokens=0, x=None, r=None, w=None, out=None, ro=None) == 0
+    assert far.lib.rmsnorm(None, None, 1e-6, None, 0, 128, code("f32", "f32"), None) == 0
+
+
+def test_host_workspace_size(far):
+    n1 = far.lib.far_host_workspace_bytes(1, 4096, code("bf16", "f32"), 1)
+    n8 = far.lib.far_host_workspace_bytes(8, 4096, code("bf16", "f32"), 1)
+    # weight + two slots of (x, residual, residual_out in bf16, out in fp32)
+    assert n8 == 4096 * 4 + 2 * 8 * 4096 * (2 + 2 + 2 + 4)
+    assert n1 < n8
+    assert far.lib.far_host_workspace_bytes(8, 4096, code("f16", "bf16"), 1) == -1
+    assert far.lib.far_host_workspace_bytes(0, 4096, code("f16", "f16"), 1) == -4
+
+
+def test_status_strings(far):
+    for s in range(10):
+        assert far.lib.far_status_string(s)
+    assert b"bf16" in far.lib.far_status_string(1)
+
+
+def test_binding_rejects_mixed_halves_before_the_call(far):
+    with pytest.raises(far.FarError):
+        far.output_dtype(torch.float16, torch.bfloat16)

@@ -1,0 +1,65 @@
+"""The large workloads at full size, in the launch configuration the bench times.
+
+The fp16 65536 x 8192 workload is compared with the oracle on sampled rows
+(first, last and spread rows) and its residual_out on every element (a
+property that holds at any size: RNE_act(fl32(x + r)), rebuilt with torch's
+binary32 add and RNE cast); the bf16 16384 x 5120 workload is compared with
+the oracle on every row, for both variants.
+"""
+import numpy as np
+import pytest
+import torch
+
+import far_gen
+import oracle
+from gpu_helpers import gate
+from oracle_pins import bits_equal
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def far():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixed_precision_residual_gb300 as far
+
+    far.set_launch_override()
+    return far
+
+
+def _run(far, d):
+    x, r, w = d["x"].cuda(), d["r"].cuda(), d["w"].cuda()
+    out, res = far.fused_add_rmsnorm(x, r, w, d["eps"])
+    nout = far.rmsnorm(x, w, d["eps"])
+    assert far.device_status() == 0
+    return out.cpu(), res.cpu(), nout.cpu()
+
+
+def test_bf16_16384x5120_every_row(far):
+    d = far_gen.make_inputs("c4")
+    out, res, nout = _run(far, d)
+    ref_out, ref_res = oracle.fused_add_rmsnorm(d["x"], d["r"], d["w"], d["eps"], "bf16", "bf16")
+    gate(out, ref_out, res, ref_res, "c4 fused")
+    gate(nout, oracle.rmsnorm(d["x"], d["w"], d["eps"], "bf16", "bf16"), where="c4 rmsnorm")
+
+
+def test_f16_65536x8192_sampled_rows(far):
+    d = far_gen.make_inputs("c5")
+    out, res, nout = _run(far, d)
+    # residual_out everywhere, by its defining property (binary32 add, one RNE cast)
+    for t0 in range(0, d["tokens"], 8192):
+        sl = slice(t0, t0 + 8192)
+        ref = (d["x"][sl].float() + d["r"][sl].float()).half()
+        assert bits_equal(res[sl], ref), f"residual_out rows {t0}.."
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([np.arange(0, 64), np.arange(d["tokens"] - 64, d["tokens"]),
+                                     rng.choice(d["tokens"], 1920, replace=False)]))
+    idx = torch.from_numpy(rows)
+    x, r = d["x"][idx].contiguous(), d["r"][idx].contiguous()
+    ref_out, ref_res = oracle.fused_add_rmsnorm(x, r, d["w"], d["eps"], "f16", "f16")
+    gate(out[idx], ref_out, res[idx], ref_res, "c5 fused (sampled rows)")
+    gate(nout[idx], oracle.rmsnorm(x, d["w"], d["eps"], "f16", "f16"), where="c5 rmsnorm (sampled rows)")

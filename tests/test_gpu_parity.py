@@ -1,0 +1,188 @@
+"""CUDA path against the CPU oracle, element by element, through the C ABI.
+
+Sizes here are ones the oracle finishes in seconds but that still span many
+rows per CTA, several CTAs per SM sweep and ragged tails; the full workload
+sizes are in test_gpu_full.py.
+"""
+import itertools
+
+import pytest
+import torch
+
+import far_gen
+from gpu_helpers import check_both, far_fused, far_norm, gate, oracle_fused, oracle_norm
+from oracle_pins import bits_equal, golden
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "f32"), ("f32", "f32"), ("f32", "bf16"),
+         ("f32", "f16")]
+
+
+@pytest.fixture(scope="module")
+def far():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixed_precision_residual_gb300 as far
+
+    far.set_launch_override()  # automatic plans
+    return far
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+def test_workloads(far, name):
+    d = far_gen.make_inputs(name)
+    check_both(far, d, name)
+
+
+@pytest.mark.parametrize("name", ["c4", "c5"])
+def test_workload_rows(far, name):
+    """The large workloads' first rows (the full sizes run in test_gpu_full)."""
+    d = far_gen.make_inputs(name, rows=700)
+    check_both(far, d, name)
+
+
+def _matrix():
+    g = golden("contract.json")["test_matrix"]
+    return list(itertools.product(g["dtypes"], g["tokens"], g["hidden"]))
+
+
+@pytest.mark.parametrize("act,tokens,hidden", _matrix())
+def test_case_study_matrix(far, act, tokens, hidden):
+    d = far_gen.custom_inputs(act, act, tokens, hidden, seed=tokens + hidden)
+    check_both(far, d, f"{act} {tokens}x{hidden}")
+
+
+@pytest.mark.parametrize("act,wd", PAIRS)
+@pytest.mark.parametrize("hidden", [1, 7, 8, 33, 1000, 2048, 4095, 4096, 4097, 5120, 8192, 12288])
+def test_dtype_pairs_and_hidden_sizes(far, act, wd, hidden):
+    tokens = 40 if hidden <= 8192 else 12
+    d = far_gen.custom_inputs(act, wd, tokens, hidden, seed=hidden, scale_lo=1e-3, scale_hi=30.0)
+    check_both(far, d, f"{act}/{wd} H={hidden}")
+
+
+@pytest.mark.parametrize("hidden", [16384, 24576, 32768, 65536, 100003])
+def test_large_hidden(far, hidden):
+    d = far_gen.custom_inputs("bf16", "bf16", 5, hidden, seed=3)
+    check_both(far, d, f"H={hidden}")
+    d = far_gen.custom_inputs("f16", "f32", 3, hidden, seed=4)
+    check_both(far, d, f"f16/f32 H={hidden}")
+
+
+@pytest.mark.parametrize("tokens", [1, 2, 151, 152, 153, 305, 1217])
+def test_token_counts(far, tokens):
+    d = far_gen.custom_inputs("f16", "f16", tokens, 5120, seed=tokens)
+    check_both(far, d, f"T={tokens}")
+
+
+def test_zero_tokens(far):
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    out, res = far.fused_add_rmsnorm(x, x.clone(), w, 1e-6)
+    assert out.shape == (0, 256)
+    assert far.rmsnorm(x, w, 1e-6).shape == (0, 256)
+
+
+@pytest.mark.parametrize("offset", [1, 3])
+def test_misaligned_pointers(far, offset):
+    """Buffers off a 16-byte boundary take the generic path: same results."""
+    for act, wd in [("bf16", "bf16"), ("f16", "f32"), ("f32", "f32")]:
+        d = far_gen.custom_inputs(act, wd, 50, 2048, seed=offset)
+        check_both(far, d, f"misaligned {act}/{wd}", offset=offset)
+
+
+def test_in_place(far):
+    for act, wd in [("bf16", "bf16"), ("f16", "f16"), ("f32", "f32")]:
+        d = far_gen.custom_inputs(act, wd, 300, 4096, seed=11)
+        check_both(far, d, f"in-place {act}", inplace=True)
+
+
+def test_every_plan_gives_the_same_bits(far):
+    """Chunks per thread, rows in flight, ring depth and the generic kernel all change
+    the reduction order; the double-word accumulator makes the results identical."""
+    d = far_gen.custom_inputs("f16", "f16", 400, 8192, seed=5)
+    ref_out, ref_res = oracle_fused(d)
+    ref_norm = oracle_norm(d)
+    plans = [(-1, 0, 0, 0), (1, 0, 0, 0), (0, 4, 1, 2), (0, 4, 2, 3), (0, 8, 1, 0), (0, 8, 4, 0), (0, 2, 0, 0)]
+    results = []
+    try:
+        for kind, nch, groups, stages in plans:
+            far.set_launch_override(kind, nch, groups, stages)
+            out, res = far_fused(far, d)
+            nout = far_norm(far, d)
+            gate(out, ref_out, res, ref_res, f"plan {kind, nch, groups, stages}")
+            gate(nout, ref_norm, where=f"plan {kind, nch, groups, stages} rmsnorm")
+            results.append((out, nout))
+    finally:
+        far.set_launch_override()
+    for out, nout in results[1:]:
+        assert bits_equal(out, results[0][0]) and bits_equal(nout, results[0][1])
+
+
+def test_special_values(far):
+    """inf / NaN / huge / subnormal inputs: NaN spreads through its row only."""
+    for act in ("f16", "bf16", "f32"):
+        d = far_gen.custom_inputs(act, act, 16, 1024, seed=9)
+        x, r = d["x"].clone(), d["r"].clone()
+        x[0, 5] = float("nan")
+        x[1, 7] = float("inf")
+        r[2, 9] = float("-inf")
+        x[3] = 0.0
+        r[3] = 0.0
+        big = {"f16": 60000.0, "bf16": 3.0e38, "f32": 3.0e38}[act]
+        x[4, :4] = big
+        r[4, :4] = big
+        tiny = {"f16": 6e-8, "bf16": 1e-39, "f32": 1e-44}[act]
+        x[5] = tiny
+        r[5] = -tiny / 2
+        x[6, 100] = -0.0
+        r[6, 100] = -0.0
+        d = dict(d, x=x, r=r)
+        check_both(far, d, f"special {act}")
+
+
+def test_eps_variants(far):
+    for eps in (0.0, 1e-12, 1e-5, 0.5):
+        d = dict(far_gen.custom_inputs("bf16", "f32", 64, 3072, seed=2, scale_lo=1e-4, scale_hi=1e-1), eps=eps)
+        check_both(far, d, f"eps={eps}")
+
+
+def test_host_buffer_entry_points(far):
+    """The end-to-end entry points (host buffers, chunked through a small workspace)
+    give the same bits as the device entry points."""
+    for act, wd in [("f16", "f16"), ("bf16", "f32")]:
+        d = far_gen.custom_inputs(act, wd, 1000, 4096, seed=21)
+        od = far.output_dtype(d["x"].dtype, d["w"].dtype)
+        ws = torch.empty(far.host_workspace_bytes(96, 4096, d["x"].dtype, d["w"].dtype), dtype=torch.uint8,
+                         device="cuda")
+        ref_out, ref_res = oracle_fused(d)
+        for pinned in (True, False):
+            x, r, w = (t.pin_memory() if pinned else t.clone() for t in (d["x"], d["r"], d["w"]))
+            out = torch.empty(d["x"].shape, dtype=od, pin_memory=pinned)
+            res = torch.empty(d["x"].shape, dtype=d["x"].dtype, pin_memory=pinned)
+            far.fused_add_rmsnorm_host(x, r, w, d["eps"], out, res, ws)
+            torch.cuda.current_stream().synchronize()
+            gate(out, ref_out, res, ref_res, f"host {act}/{wd} pinned={pinned}")
+            nout = torch.empty(d["x"].shape, dtype=od, pin_memory=pinned)
+            far.rmsnorm_host(x, w, d["eps"], nout, ws)
+            torch.cuda.current_stream().synchronize()
+            gate(nout, oracle_norm(d), where=f"host rmsnorm {act}/{wd}")
+    with pytest.raises(far.FarError):
+        tiny = torch.empty(64, dtype=torch.uint8, device="cuda")
+        far.fused_add_rmsnorm_host(x, r, w, d["eps"], out, res, tiny)
+
+
+def test_errors_through_the_abi_on_device(far):
+    x = torch.zeros((8, 256), dtype=torch.float16, device="cuda")
+    w = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(far.FarError) as e:
+        far.fused_add_rmsnorm(x, x.clone(), w, 1e-6)
+    assert e.value.status == 1
+    w16 = torch.ones(256, dtype=torch.float16, device="cuda")
+    buf = torch.zeros(8 * 256 + 8, dtype=torch.float16, device="cuda")
+    with pytest.raises(far.FarError) as e:  # out overlapping x at an offset
+        far.fused_add_rmsnorm(buf[:2048].view(8, 256), x, w16, 1e-6, out=buf[8:].view(8, 256))
+    assert e.value.status == 5
