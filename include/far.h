@@ -139,9 +139,14 @@ int far_selftest_wait_timeout(uint32_t timeout_us, void* stream);
  * far_describe_launch: the plan the library would use for a call with
  * 16-byte-aligned, non-overlapping buffers of this shape on the current device:
  * out6 = {kind, nch, warps per row, groups, stages, grid}.
+ *
+ * far_plan_for_sms: the same plan for a device with `sms` SMs, computed on the
+ * host alone (no CUDA call): out8 = {kind, nch, warps per row, groups, stages,
+ * grid, threads per CTA, dynamic shared-memory bytes}.
  */
 int far_set_launch_override(int kind, int nch, int groups, int stages);
 int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6);
+int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int sms, int* out8);
 
 #ifdef __cplusplus
 }

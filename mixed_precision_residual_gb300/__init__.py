@@ -57,6 +57,8 @@ lib.far_set_launch_override.argtypes = [_int, _int, _int, _int]
 lib.far_set_launch_override.restype = _int
 lib.far_describe_launch.argtypes = [_i64, _i64, _int, _int, _vp]
 lib.far_describe_launch.restype = _int
+lib.far_plan_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _vp]
+lib.far_plan_for_sms.restype = _int
 
 
 class FarError(RuntimeError):
@@ -179,3 +181,10 @@ def describe_launch(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype,
     buf = (ctypes.c_int * 6)()
     _check(lib.far_describe_launch(tokens, hidden, dtypes(act, wd), int(residual), ctypes.addressof(buf)))
     return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid"), list(buf)))
+
+
+def plan_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool, sms: int) -> dict:
+    """The launch plan for a device with `sms` SMs (host logic only, no GPU needed)."""
+    buf = (ctypes.c_int * 8)()
+    _check(lib.far_plan_for_sms(tokens, hidden, dtypes(act, wd), int(residual), sms, ctypes.addressof(buf)))
+    return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))

@@ -133,8 +133,8 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// the launch plan for a validated call
-int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) {
+// the launch plan for a validated call on a device with `sms` SMs (pure host logic)
+int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Launch& L) {
   memset(&L, 0, sizeof L);
   Params& p = L.p;
   p.x = c.x;
@@ -146,7 +146,7 @@ int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) 
   p.hidden = (int32_t)c.hidden;
   p.hidden_f = (float)c.hidden;
   p.eps = c.eps;
-  p.status = dev.status;
+  p.status = status;
   p.timeout_ns = kWaitTimeoutNs;
   L.stream = stream;
 
@@ -158,40 +158,62 @@ int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) 
   uint32_t stage_bytes = 0, w_bytes = (uint32_t)((c.hidden * sw + 15) / 16 * 16);
   size_t smem = 0;
   if (staged) {
+    // Launch table (measured on GB300 over nch x groups x slots, L2 flushed between launches):
+    //  - 8 chunks a thread (64 values of s for 16-bit data) keeps the per-row work
+    //    (reductions, IEEE divide and square root, waits) small against the per-element work;
+    //  - the fused op on long rows (more than 3 warps a row) runs best with a single group
+    //    of up to 16 warps on one row at a time and 4 ring slots;
+    //  - otherwise as many groups as 12 warps allow, one ring slot per group for the fused
+    //    op (two inputs in flight) and two for the variant (one input).
     const int64_t C = row_bytes / 16;
-    const int V = 16 / sa;
-    // about 32 elements per thread: 4 chunks of 16-bit data, 8 of binary32
-    nch = (V == 8) ? 4 : 8;
-    if (C <= 32LL * nch) {  // one warp covers the row: no more chunks per thread than needed
+    int slots_per_group = c.residual ? 1 : 2;
+    nch = 8;
+    G = (int)((C + 255) / 256);
+    if (C <= 128) {  // one warp covers the row with fewer chunks a thread
       nch = 1;
       while (32LL * nch < C) nch *= 2;
+      G = 1;
     }
-    G = (int)((C + 32LL * nch - 1) / (32LL * nch));
-    if (G > kMaxConsumerWarps && nch < 8) {
-      nch = 8;
-      G = (int)((C + 255) / 256);
+    bool one_group = false;
+    if (c.residual && G > 3) {
+      nch = 1;
+      while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
+      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+      one_group = true;
     }
     if (g_force_nch.load() > 0) {
       nch = g_force_nch.load();
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+      one_group = false;
     }
-    staged = G <= kMaxConsumerWarps;
+    staged = G <= max_consumer_warps(nch);
     if (staged) {
-      groups = kMaxConsumerWarps / G;
-      const int64_t per_sm = (c.tokens + dev.sms - 1) / dev.sms;  // rows per SM if spread evenly
+      const int64_t per_sm = (c.tokens + sms - 1) / sms;  // rows per SM if spread evenly
+      groups = one_group ? 1 : max_consumer_warps(nch) / G;
       if (groups > per_sm) groups = (int)(per_sm > 0 ? per_sm : 1);
-      if (g_force_groups.load() > 0) groups = g_force_groups.load() * G <= kMaxConsumerWarps ? g_force_groups.load() : groups;
+      if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch))
+        groups = g_force_groups.load();
       stage_bytes = (uint32_t)(((row_bytes + 127) / 128 * 128) * (c.residual ? 2 : 1));
-      // as many ring slots as fit (at most 32): more slots, more bytes in flight per SM
-      stages = 32;
+      int want = one_group ? 4 : groups * slots_per_group;
+      if (want < 2) want = 2;
+      // as many ring slots as wanted and as fit in shared memory
+      stages = want > 32 ? 32 : want;
       while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes) > (size_t)kMaxDynamicSmem)
         --stages;
       const int forced = g_force_stages.load();
-      if (forced >= 2 && forced <= stages) stages = forced;
+      if (forced >= 2) {
+        stages = forced;
+        while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes) > (size_t)kMaxDynamicSmem)
+          --stages;
+      }
+      if (groups > stages) groups = stages;
+      // Each ring slot must belong to one group (stages a multiple of groups):
+      // then every wait on a slot's barriers is for the phase right after the
+      // one its waiter saw complete, which is all a parity wait can tell apart.
+      stages -= stages % groups;
       if (stages < 2) {
         staged = false;
       } else {
-        if (groups > stages) groups = stages;
         smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes);
       }
     }
@@ -199,6 +221,7 @@ int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) 
   if (staged) {
     L.kind = kStaged;
     L.nch = nch;
+    L.exact = (row_bytes / 16) == (int64_t)nch * G * 32;
     p.chunks = (int32_t)(row_bytes / 16);
     p.warps_per_row = G;
     p.groups = groups;
@@ -207,13 +230,13 @@ int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) 
     p.w_smem_bytes = w_bytes;
     p.stage_bytes = stage_bytes;
     int64_t grid = (c.tokens + groups - 1) / groups;
-    if (grid > dev.sms) grid = dev.sms;
+    if (grid > sms) grid = sms;
     L.grid = dim3((unsigned)grid);
     L.block = dim3((unsigned)((1 + groups * G) * 32));
     L.smem = smem;
   } else {
     L.kind = kGeneric;
-    int64_t grid = c.tokens < (int64_t)dev.sms * 8 ? c.tokens : (int64_t)dev.sms * 8;
+    int64_t grid = c.tokens < (int64_t)sms * 8 ? c.tokens : (int64_t)sms * 8;
     L.grid = dim3((unsigned)grid);
     L.block = dim3(kGenericThreads);
     L.smem = 0;
@@ -224,7 +247,7 @@ int plan(const Call& c, const DeviceState& dev, cudaStream_t stream, Launch& L) 
 int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   if (c.tokens == 0) return FAR_OK;
   Launch L;
-  int st = plan(c, dev, stream, L);
+  int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
   cudaError_t e;
   switch (c.act) {
@@ -448,7 +471,8 @@ int far_device_status(void* stream) {
     e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e);
   }
-  return (word & (1u << FAR_ERR_TIMEOUT)) ? FAR_ERR_TIMEOUT : FAR_OK;
+  if (word & (1u << FAR_ERR_TIMEOUT)) return FAR_ERR_TIMEOUT;
+  return word ? FAR_ERR_SHAPE : FAR_OK;  // a kernel refused an inconsistent launch plan
 }
 
 int64_t far_host_workspace_bytes(int64_t chunk_tokens, int64_t hidden, int dtype, int has_residual) {
@@ -492,8 +516,9 @@ int far_set_launch_override(int kind, int nch, int groups, int stages) {
   return FAR_OK;
 }
 
-int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6) {
-  // kind, nch, warps_per_row, groups, stages, grid -- for a call with 16-byte-aligned buffers
+int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int sms, int* out8) {
+  // kind, nch, warps per row, groups, stages, grid, threads per CTA, dynamic shared bytes
+  if (sms < 1 || !out8) return FAR_ERR_SHAPE;
   Call c;
   // distinct, aligned, non-overlapping stand-in addresses: only the plan is computed
   const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
@@ -507,18 +532,28 @@ int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_resid
                     dtype, has_residual != 0, c);
   if (st != FAR_OK) return st;
   if (tokens == 0) return FAR_ERR_SHAPE;
-  DeviceState* dev = nullptr;
-  st = current_device(dev);
-  if (st != FAR_OK) return st;
   Launch L;
-  st = plan(c, *dev, nullptr, L);
+  st = plan(c, sms, nullptr, nullptr, L);
   if (st != FAR_OK) return st;
-  out6[0] = L.kind;
-  out6[1] = L.nch;
-  out6[2] = L.p.warps_per_row;
-  out6[3] = L.p.groups;
-  out6[4] = L.p.stages;
-  out6[5] = (int)L.grid.x;
+  out8[0] = L.kind;
+  out8[1] = L.nch;
+  out8[2] = L.p.warps_per_row;
+  out8[3] = L.p.groups;
+  out8[4] = L.p.stages;
+  out8[5] = (int)L.grid.x;
+  out8[6] = (int)L.block.x;
+  out8[7] = (int)L.smem;
+  return FAR_OK;
+}
+
+int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6) {
+  DeviceState* dev = nullptr;
+  int st = current_device(dev);
+  if (st != FAR_OK) return st;
+  int o8[8];
+  st = far_plan_for_sms(tokens, hidden, dtype, has_residual, dev->sms, o8);
+  if (st != FAR_OK) return st;
+  for (int i = 0; i < 6; ++i) out6[i] = o8[i];
   return FAR_OK;
 }
 

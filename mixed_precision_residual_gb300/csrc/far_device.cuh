@@ -89,6 +89,39 @@ __device__ __forceinline__ void round_through(float* f) {
   }
 }
 
+// two packed 16-bit products, each rounded once to nearest even (IEEE binary16 /
+// bfloat16 multiply, subnormals kept).  For 16-bit n and w the binary32 product
+// n * w is exact, so this equals RNE_DT(fl32(n * w)) with one instruction per pair.
+template <int DT> __device__ __forceinline__ uint32_t mul2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t mul2<FAR_F16>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+template <> __device__ __forceinline__ uint32_t mul2<FAR_BF16>(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// fl32(x + r) for the two 16-bit x values packed in xw and binary32 r0, r1:
+// the mixed-precision add widens x exactly and rounds the sum once.
+template <int DT> __device__ __forceinline__ float2 add2_mixed(uint32_t xw, float r0, float r1);
+template <> __device__ __forceinline__ float2 add2_mixed<FAR_F16>(uint32_t xw, float r0, float r1) {
+  float s0, s1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %3;\n\tadd.rn.f32.f16 %1, hi, %4;\n\t}"
+      : "=f"(s0), "=f"(s1) : "r"(xw), "f"(r0), "f"(r1));
+  return make_float2(s0, s1);
+}
+template <> __device__ __forceinline__ float2 add2_mixed<FAR_BF16>(uint32_t xw, float r0, float r1) {
+  float s0, s1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %3;\n\tadd.rn.f32.bf16 %1, hi, %4;\n\t}"
+      : "=f"(s0), "=f"(s1) : "r"(xw), "f"(r0), "f"(r1));
+  return make_float2(s0, s1);
+}
+
 // vector memory access of N bytes (N = 8, 16 or 32), N-aligned
 template <int N> __device__ __forceinline__ void load_bytes(const void* p, uint32_t* w) {
   if constexpr (N == 8) {
@@ -120,45 +153,55 @@ template <int N> __device__ __forceinline__ void store_bytes_stream(void* p, con
 // the row's sum of squares: a binary32 double-word (hi + lo) accumulator
 // ---------------------------------------------------------------------------
 //
-// The contract fixes binary32 accumulation but not the order.  Adding each
-// square with an error-free transformation (Knuth's TwoSum, TAOCP vol. 2,
-// 4.2.2) and carrying the rounding errors in `lo` keeps hi + lo within about
-// 2^-44 (relative) of the exact sum, so the final hi + lo rounded to binary32
-// is the correctly rounded sum -- the one order-free binary32 value -- except
-// in the astronomically rare rows whose exact sum lies within that distance of
-// a binary32 rounding boundary.  Every operation is a binary32 add with an
-// explicit rounding intrinsic, so nothing is contracted into an FMA.
+// The contract fixes binary32 accumulation but not the order.  Each square is
+// added with an error-free transformation and the exact rounding errors are
+// carried in `lo`; hi + lo then stays within about 2^-44 (relative) of the
+// exact sum, so hi + lo rounded once to binary32 is the correctly rounded sum
+// -- the one order-free binary32 value -- except in astronomically rare rows
+// whose exact sum lies within that distance of a binary32 rounding boundary.
+// All terms are non-negative, so ordering the pair with max/min makes Dekker's
+// Fast2Sum exact (|a| >= |b|); the NaN-propagating max/min keep a NaN square
+// from being dropped.  Every add carries an explicit rounding intrinsic, so
+// nothing is contracted into an FMA.
 
 struct DW {
   float hi, lo;
 };
 
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  float bv = __fsub_rn(s, a);
-  float av = __fsub_rn(s, bv);
-  e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+__device__ __forceinline__ float min_nan(float a, float b) {
+  float d;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// s + e == a + b exactly, for non-negative a, b (or inf / NaN, which stand in s)
+__device__ __forceinline__ void fast_two_sum_ordered(float a, float b, float& s, float& e) {
+  const float big = max_nan(a, b), small = min_nan(a, b);
+  s = __fadd_rn(big, small);
+  e = __fsub_rn(small, __fsub_rn(s, big));
 }
 
 // acc += p for a non-negative binary32 p
 __device__ __forceinline__ void dw_add(DW& acc, float p) {
   float s, e;
-  two_sum(acc.hi, p, s, e);
+  fast_two_sum_ordered(acc.hi, p, s, e);
   acc.hi = s;
   acc.lo = __fadd_rn(acc.lo, e);
 }
 
-// a + b, renormalised; commutative bit for bit, so butterfly partners agree.
-// An infinite or NaN sum stands as it is (its error terms are NaN and must not
-// leak into it: a row with an infinite square has S = inf, not NaN).
+// a + b; commutative bit for bit, so butterfly partners agree.  hi carries the
+// rounded sum of the his, lo every exact error so far (an infinite or NaN hi
+// makes lo NaN, and dw_value then lets hi stand).
 __device__ __forceinline__ DW dw_combine(DW a, DW b) {
   float s, e;
-  two_sum(a.hi, b.hi, s, e);
-  if (!isfinite(s)) return DW{s, 0.f};
-  e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
-  float hi = __fadd_rn(s, e);
-  float lo = __fsub_rn(e, __fsub_rn(hi, s));
-  return DW{hi, lo};
+  fast_two_sum_ordered(a.hi, b.hi, s, e);
+  return DW{s, __fadd_rn(__fadd_rn(a.lo, b.lo), e)};
 }
 
 // the binary32 sum: hi + lo rounded once; an infinite or NaN hi stands
@@ -166,12 +209,13 @@ __device__ __forceinline__ float dw_value(DW a) {
   return isfinite(a.hi) ? __fadd_rn(a.hi, a.lo) : a.hi;
 }
 
+__device__ __forceinline__ DW dw_shfl_xor(DW a, int off) {
+  return DW{__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
+}
+
 __device__ __forceinline__ DW dw_warp_allreduce(DW a) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    DW o{__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
-    a = dw_combine(a, o);
-  }
+  for (int off = 16; off > 0; off >>= 1) a = dw_combine(a, dw_shfl_xor(a, off));
   return a;
 }
 
@@ -208,14 +252,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// One bounded attempt: the thread may be suspended until the phase completes or
+// kSuspendHintNs passes, so a waiting warp sleeps instead of spinning on issue slots.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return done != 0;
 }
@@ -235,7 +283,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   const uint64_t t0 = global_timer_ns();
   for (;;) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < 8; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > timeout_ns) {
       atomicOr(status, 1u << FAR_ERR_TIMEOUT);

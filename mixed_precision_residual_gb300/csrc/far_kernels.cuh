@@ -27,8 +27,8 @@
 
 namespace far {
 
-template <int ACT, int WD, bool RES, int NCH>
-__global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) {
+template <int ACT, int WD, bool RES, int NCH, bool EXACT>
+__global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Params p) {
   constexpr int SA = dtype_size<ACT>::value;
   constexpr int SW = dtype_size<WD>::value;
   constexpr int OD = promote(ACT, WD);
@@ -48,6 +48,29 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
   const uint32_t r_off = (p.row_bytes + 127u) & ~127u;  // residual row inside a slot
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The ring's phase bookkeeping needs every slot owned by one group (stages a
+  // multiple of groups) and a warp count that matches the plan; refuse anything
+  // else before any barrier or copy exists (the host never launches it).
+  if (stages < 2 || groups < 1 || stages % groups != 0 || (int)blockDim.x != (1 + groups * G) * 32) {
+    if (threadIdx.x == 0) atomicOr(p.status, 1u << FAR_ERR_SHAPE);
+    return;
+  }
+  const int64_t b = blockIdx.x, nb = gridDim.x;
+  const int64_t n_local = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
+  const uint32_t tx = RES ? 2u * p.row_bytes : p.row_bytes;
+  const int64_t first = n_local < stages ? n_local : stages;  // rows issued before the weight load
+
+  // producer: one bulk copy of row k's x (and residual) into ring slot k % stages
+  auto issue = [&](int64_t k, int slot, uint64_t pol) {
+    const int64_t row = b + k * nb;
+    const uint32_t full = smem_addr(&bars[slot]);
+    const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
+    mbar_arrive_expect_tx(full, tx);
+    bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full, pol);
+    if constexpr (RES)
+      bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full, pol);
+  };
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < stages; ++i) {
       mbar_init(smem_addr(&bars[i]), 1);           // full: the producer's arrive + bytes
@@ -55,6 +78,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
     }
     for (int i = 0; i < 2 * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
     fence_barrier_init();
+    // the first `stages` rows need no free slot: start them now, under the weight load
+    const uint64_t pol = l2_evict_first_policy();
+    for (int64_t k = 0; k < first; ++k) issue(k, (int)k, pol);
   }
   {  // the weight row, once per CTA (16-byte aligned; hidden * SW is even)
     const int nbytes = p.hidden * SW;
@@ -67,28 +93,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
   }
   __syncthreads();
 
-  const int64_t b = blockIdx.x, nb = gridDim.x;
-  const int64_t n_local = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
-
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
-      const uint32_t tx = RES ? 2u * p.row_bytes : p.row_bytes;
-      int64_t k = 0;
+      int64_t k = first;
+      int slot = (int)(first % stages);
+      uint32_t phase = (uint32_t)(first / stages) & 1u;  // (k / stages) & 1
       for (; k < n_local; ++k) {
-        const int slot = (int)(k % stages);
-        if (k >= stages &&
-            !mbar_wait(smem_addr(&bars[stages + slot]), (uint32_t)((k / stages) - 1) & 1u, p.timeout_ns,
-                       p.status))
-          break;
-        const int64_t row = b + k * nb;
-        const uint32_t full = smem_addr(&bars[slot]);
-        const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
-        mbar_arrive_expect_tx(full, tx);
-        bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full, pol);
-        if constexpr (RES)
-          bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full, pol);
+        // slot k % stages was last used by row k - stages: wait until its consumers released it
+        if (!mbar_wait(smem_addr(&bars[stages + slot]), phase ^ 1u, p.timeout_ns, p.status)) break;
+        issue(k, slot, pol);
+        if (++slot == stages) {
+          slot = 0;
+          phase ^= 1u;
+        }
       }
       // the copies of the last (at most `stages`) rows must have landed before the CTA may exit
       for (int64_t j = (k > stages ? k - stages : 0); j < k; ++j)
@@ -101,37 +120,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
   const int cw = warp - 1;
   const int g = cw / G, wg = cw - g * G;
   const int C = p.chunks;
-  int64_t it = 0;  // this group's row count, for the reduction buffers
+  int G8 = 1;  // G rounded up to a power of two (<= 16): the lanes of the cross-warp butterfly
+  while (G8 < G) G8 <<= 1;
+  int slot = g;          // k % stages (g < groups <= stages)
+  uint32_t phase = 0;    // (k / stages) & 1
+  uint32_t it = 0;       // this group's row count, for the reduction buffers
   for (int64_t k = g; k < n_local; k += groups, ++it) {
-    const int slot = (int)(k % stages);
-    if (!mbar_wait(smem_addr(&bars[slot]), (uint32_t)(k / stages) & 1u, p.timeout_ns, p.status)) return;
+    if (!mbar_wait(smem_addr(&bars[slot]), phase, p.timeout_ns, p.status)) return;
     const unsigned char* xs = ring + (size_t)slot * p.stage_bytes;
 
     // pass 1 (from shared memory): s = fl32(x + r) into registers, squares into the accumulator
     float s[NCH][V];
-    DW acc0{0.f, 0.f}, acc1{0.f, 0.f};
+    DW acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // four independent chains
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
-      if (c < C) {
-        uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
-        float xf[V];
-        widen<ACT, V>(reinterpret_cast<const uint32_t*>(&xv), xf);
+      if (EXACT || c < C) {
+        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
+        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
         if constexpr (RES) {
-          uint4 rv = *reinterpret_cast<const uint4*>(xs + r_off + (size_t)c * 16);
+          const uint4 rv = *reinterpret_cast<const uint4*>(xs + r_off + (size_t)c * 16);
           float rf[V];
           widen<ACT, V>(reinterpret_cast<const uint32_t*>(&rv), rf);
+          if constexpr (ACT == FAR_F32) {
 #pragma unroll
-          for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(xf[e], rf[e]);
+            for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(__uint_as_float(xw[e]), rf[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < V / 2; ++e) {
+              const float2 t = add2_mixed<ACT>(xw[e], rf[2 * e], rf[2 * e + 1]);
+              s[j][2 * e] = t.x;
+              s[j][2 * e + 1] = t.y;
+            }
+          }
         } else {
-#pragma unroll
-          for (int e = 0; e < V; ++e) s[j][e] = xf[e];
+          widen<ACT, V>(xw, s[j]);
         }
 #pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const float q = __fmul_rn(s[j][e], s[j][e]);
-          if (e & 1) dw_add(acc1, q); else dw_add(acc0, q);
-        }
+        for (int e = 0; e < V; ++e) dw_add(acc[e & 3], __fmul_rn(s[j][e], s[j][e]));
       } else {
 #pragma unroll
         for (int e = 0; e < V; ++e) s[j][e] = 0.f;
@@ -139,22 +165,31 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_addr(&bars[stages + slot]));  // the slot may be refilled
+    slot += groups;
+    if (slot >= stages) {
+      slot -= stages;
+      phase ^= 1u;
+    }
 
-    DW acc = dw_warp_allreduce(dw_combine(acc0, acc1));
+    DW tot = dw_warp_allreduce(dw_combine(dw_combine(acc[0], acc[1]), dw_combine(acc[2], acc[3])));
     if (G > 1) {
-      const int buf = (int)(it & 1);
+      // every warp of the group publishes its sum, then combines all G of them
+      // with the same fixed butterfly over lanes 0..G8-1, so all agree bit for bit
+      const int buf = (int)(it & 1u);
       float2* part = partials + (size_t)(g * 2 + buf) * G;
       const uint32_t rbar = smem_addr(&bars[2 * stages + g * 2 + buf]);
       if (lane == 0) {
-        part[wg] = make_float2(acc.hi, acc.lo);
+        part[wg] = make_float2(tot.hi, tot.lo);
         mbar_arrive(rbar);
       }
-      if (!mbar_wait(rbar, (uint32_t)(it >> 1) & 1u, p.timeout_ns, p.status)) return;
-      DW tot{part[0].x, part[0].y};
-      for (int i = 1; i < G; ++i) tot = dw_combine(tot, DW{part[i].x, part[i].y});
-      acc = tot;
+      if (!mbar_wait(rbar, (it >> 1) & 1u, p.timeout_ns, p.status)) return;
+      const int src = lane & (G8 - 1);
+      const float2 mine = src < G ? part[src] : make_float2(0.f, 0.f);
+      DW t{mine.x, mine.y};
+      for (int off = G8 >> 1; off > 0; off >>= 1) t = dw_combine(t, dw_shfl_xor(t, off));
+      tot = t;
     }
-    const float rstd = row_rstd(dw_value(acc), p.hidden_f, p.eps);
+    const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
 
     // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w)
     const int64_t row = b + k * nb;
@@ -163,19 +198,27 @@ __global__ void __launch_bounds__(kMaxThreads, 1) staged_kernel(const Params p) 
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
-      if (c < C) {
+      if (EXACT || c < C) {
         uint32_t ww[WB / 4];
         load_bytes<WB>(wsm + (size_t)c * WB, ww);
-        float wf[V];
-        widen<WD, V>(ww, wf);
-        float o[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) o[e] = __fmul_rn(s[j][e], rstd);
-        round_through<WD, V>(o);  // cast to the weight dtype first
-#pragma unroll
-        for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
         uint32_t ow[OB / 4];
-        narrow<OD, V>(o, ow);
+        if constexpr (WD == OD && WD != FAR_F32) {
+          // 16-bit weight and output (then act == wd): cast to the weight dtype,
+          // then one packed multiply rounds the exact product once
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e)
+            ow[e] = mul2<WD>(narrow2<WD>(__fmul_rn(s[j][2 * e], rstd), __fmul_rn(s[j][2 * e + 1], rstd)), ww[e]);
+        } else {
+          float wf[V];
+          widen<WD, V>(ww, wf);
+          float o[V];
+#pragma unroll
+          for (int e = 0; e < V; ++e) o[e] = __fmul_rn(s[j][e], rstd);
+          round_through<WD, V>(o);  // cast to the weight dtype first
+#pragma unroll
+          for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
+          narrow<OD, V>(o, ow);
+        }
         store_bytes_stream<OB>(orow + (size_t)c * OB, ow);
         if constexpr (RES) {
           uint32_t rw[4];
@@ -257,11 +300,15 @@ cudaError_t launch_typed(const Launch& L) {
   if (L.kind == kGeneric) {
     k = generic_kernel<ACT, WD, RES>;
   } else {
-    switch (L.nch) {
-      case 1: k = staged_kernel<ACT, WD, RES, 1>; break;
-      case 2: k = staged_kernel<ACT, WD, RES, 2>; break;
-      case 4: k = staged_kernel<ACT, WD, RES, 4>; break;
-      case 8: k = staged_kernel<ACT, WD, RES, 8>; break;
+    switch (L.nch * 2 + (L.exact ? 1 : 0)) {
+      case 2: k = staged_kernel<ACT, WD, RES, 1, false>; break;
+      case 3: k = staged_kernel<ACT, WD, RES, 1, true>; break;
+      case 4: k = staged_kernel<ACT, WD, RES, 2, false>; break;
+      case 5: k = staged_kernel<ACT, WD, RES, 2, true>; break;
+      case 8: k = staged_kernel<ACT, WD, RES, 4, false>; break;
+      case 9: k = staged_kernel<ACT, WD, RES, 4, true>; break;
+      case 16: k = staged_kernel<ACT, WD, RES, 8, false>; break;
+      case 17: k = staged_kernel<ACT, WD, RES, 8, true>; break;
       default: return cudaErrorInvalidValue;
     }
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);

@@ -7,9 +7,12 @@
 
 namespace far {
 
-// shapes of the staged kernel: a CTA = 1 producer warp + groups x warps_per_row consumer warps
+// shapes of the staged kernel: a CTA = 1 producer warp + groups x warps_per_row consumer warps.
+// 16 consumer warps leave 96 registers a thread (17 warps: 5 on one SM sub-partition);
+// 8 chunks a thread (64 values of s) need more, so those CTAs stop at 12 (128 registers).
 constexpr int kMaxConsumerWarps = 16;
-constexpr int kMaxThreads = (kMaxConsumerWarps + 1) * 32;
+__host__ __device__ constexpr int max_consumer_warps(int nch) { return nch >= 8 ? 12 : 16; }
+__host__ __device__ constexpr int max_threads(int nch) { return (max_consumer_warps(nch) + 1) * 32; }
 constexpr int kMaxDynamicSmem = 227 * 1024;
 constexpr int kGenericThreads = 256;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
@@ -40,7 +43,8 @@ enum Kind { kStaged = 0, kGeneric = 1 };
 struct Launch {
   Params p;
   int kind;
-  int nch;  // 16-byte chunks per thread (staged kernel): 1, 2, 4 or 8
+  int nch;     // 16-byte chunks per thread (staged kernel): 1, 2, 4 or 8
+  bool exact;  // chunks == nch * warps_per_row * 32: no per-chunk bounds test
   dim3 grid, block;
   size_t smem;
   cudaStream_t stream;

@@ -2,6 +2,7 @@
 its host-side validation returns the documented statuses.  No compute runs
 here: every call below is rejected (or is a no-op) before any CUDA call."""
 import ctypes
+import itertools
 import glob
 import os
 import re
@@ -124,3 +125,37 @@ def test_status_strings(far):
 def test_binding_rejects_mixed_halves_before_the_call(far):
     with pytest.raises(far.FarError):
         far.output_dtype(torch.float16, torch.bfloat16)
+
+
+def test_launch_plans_are_consistent(far):
+    """The host planner, over shapes, dtype pairs, SM counts and every override the
+    tests and the bench use: each ring slot belongs to one group (stages a multiple of
+    groups), the CTA fits the register and shared-memory budgets, the grid covers
+    the rows, and a row is covered by its group's warps."""
+    T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
+    overrides = [(-1, 0, 0, 0), (0, 4, 1, 2), (0, 4, 2, 3), (0, 8, 1, 0), (0, 8, 4, 0), (0, 2, 0, 0),
+                 (0, 4, 2, 0), (0, 8, 3, 0), (0, 4, 2, 4), (0, 8, 2, 4), (0, 1, 0, 0), (0, 4, 16, 5)]
+    try:
+        for kind, nch, groups, stages in overrides:
+            far.set_launch_override(kind, nch, groups, stages)
+            for (act, wd), hidden, tokens, res, sms in itertools.product(
+                    [(T16, T16), (B16, B16), (B16, F32), (F32, F32), (F32, B16)],
+                    [1, 8, 64, 1000, 2048, 4096, 5120, 8192, 12288, 16384, 24576, 32768],
+                    [1, 8, 151, 152, 4096, 65536], (True, False), (152, 148, 1)):
+                p = far.plan_for_sms(tokens, hidden, act, wd, res, sms)
+                if p["kind"] == 1:  # generic kernel
+                    assert p["threads"] == 256 and p["smem"] == 0 and 1 <= p["grid"] <= min(tokens, 8 * sms)
+                    continue
+                sa = 4 if act == F32 else 2
+                chunks = hidden * sa // 16
+                G, g, st = p["warps_per_row"], p["groups"], p["stages"]
+                assert p["nch"] in (1, 2, 4, 8)
+                assert st >= 2 and st % g == 0, p
+                assert g * G <= (12 if p["nch"] == 8 else 16), p
+                assert p["threads"] == (1 + g * G) * 32
+                assert p["smem"] <= 227 * 1024
+                # the group's warps cover the row, and one warp fewer would not
+                assert (G - 1) * 32 * p["nch"] < chunks <= G * 32 * p["nch"], p
+                assert 1 <= p["grid"] <= min(sms, -(-tokens // g))
+    finally:
+        far.set_launch_override()

@@ -186,3 +186,17 @@ def test_errors_through_the_abi_on_device(far):
     with pytest.raises(far.FarError) as e:  # out overlapping x at an offset
         far.fused_add_rmsnorm(buf[:2048].view(8, 256), x, w16, 1e-6, out=buf[8:].view(8, 256))
     assert e.value.status == 5
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+def test_subnormal_products(far, act):
+    """Weights so small that n * w lands among the 16-bit subnormals (and rounds to
+    zero at the bottom): the packed 16-bit multiply must keep subnormals and round
+    them to nearest even exactly like the oracle."""
+    d = far_gen.custom_inputs(act, act, 64, 4096, seed=17)
+    tiny = {"f16": 2.0 ** -20, "bf16": 2.0 ** -130}[act]
+    g = torch.Generator().manual_seed(5)
+    w = (torch.rand(4096, generator=g, dtype=torch.float64) * 8 - 4) * tiny
+    w[::7] = torch.linspace(-1, 1, len(w[::7]), dtype=torch.float64) * tiny * 2 ** -8
+    d = dict(d, w=w.to(d["w"].dtype))
+    check_both(far, d, f"subnormal products {act}")
