@@ -74,9 +74,13 @@ def step_bytes(tokens, hidden, act, wd, od):
     return fused, norm
 
 
+KERNEL_SOURCES = ("far_kernels.cuh", "far_device.cuh", "far_params.h")
+
+
 def source_hash() -> str:
+    """Hash of the sources that define the staged kernel (the captured counters' validity)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
