@@ -59,6 +59,7 @@ typedef enum { FAR_F32 = 0, FAR_F16 = 1, FAR_BF16 = 2 } far_dtype;
 #define FAR_ERR_CUDA 7       /* a CUDA call failed; far_status_string gives its text */
 #define FAR_ERR_TIMEOUT 8    /* a bounded wait inside a kernel ran out (far_device_status) */
 #define FAR_ERR_WORKSPACE 9  /* the host-buffer entry points got too small a workspace */
+#define FAR_ERR_SCRATCH 10   /* a row does not fit the allocation-free entry point's fixed scratch */
 
 /*
  * Fused residual add + RMSNorm.
@@ -117,6 +118,37 @@ int fused_add_rmsnorm_host(const void* x, const void* residual, const void* weig
 
 int rmsnorm_host(const void* x, const void* weight, float eps, void* out, int64_t tokens,
                  int64_t hidden, int dtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * fused_add_rmsnorm_host on host buffers WITHOUT any allocation: no workspace
+ * argument, no cudaMalloc or cudaFree, no stream or event creation.  (The pages
+ * describe no such entry point: it is an addition of this library.)
+ *
+ * For callers that cannot allocate device memory themselves: code embedded in a
+ * host program that owns all device memory through its own pool and forbids
+ * other allocations, or code bound by a rule of no device allocation after
+ * start-up.  They pass host buffers only, with the same meaning, layout and
+ * checks as fused_add_rmsnorm_host.
+ *
+ * The device staging area is one fixed array inside the library,
+ * FAR_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, held by every GPU that has
+ * loaded it until the process exits.  Rows are streamed through it in chunks
+ * on `stream` alone (copy in, kernel, copy out).  FAR_ERR_SCRATCH when a single
+ * row of x, residual, out and residual_out plus the weight does not fit it
+ * (a row of about 1.6 million elements when every dtype is 16-bit, 0.8 million
+ * when every dtype is fp32).  Every byte the kernel reads from
+ * the array is copied in by the same call, so nothing in it needs clearing;
+ * the array keeps the last call's contents.  All calls share the one array:
+ * calls that overlap on the GPU (on different streams, or from several host
+ * threads) race on it and must be serialised by the caller.  The first call on
+ * a device looks up the array's device address (once per device) and should
+ * come before any stream capture on that device.
+ */
+#define FAR_NOALLOC_SCRATCH_BYTES (16ll << 20)
+
+int fused_add_rmsnorm_host_noalloc(const void* x, const void* residual, const void* weight, float eps,
+                                   void* out, void* residual_out, int64_t tokens, int64_t hidden, int dtype,
+                                   void* stream);
 
 /*
  * Failure-detection self test: launches one tiny kernel that waits on a

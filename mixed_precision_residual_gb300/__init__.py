@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_PKG, "_build", "libfar.so")
 F32, F16, BF16 = 0, 1, 2
 STATUS = {0: "FAR_OK", 1: "FAR_ERR_DTYPE_MIX", 2: "FAR_ERR_DTYPE", 3: "FAR_ERR_NULL", 4: "FAR_ERR_SHAPE",
           5: "FAR_ERR_ALIAS", 6: "FAR_ERR_EPS", 7: "FAR_ERR_CUDA", 8: "FAR_ERR_TIMEOUT",
-          9: "FAR_ERR_WORKSPACE"}
+          9: "FAR_ERR_WORKSPACE", 10: "FAR_ERR_SCRATCH"}
 FAR_OK, FAR_ERR_TIMEOUT = 0, 8
 TORCH_TO_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
 CODE_TO_TORCH = {v: k for k, v in TORCH_TO_CODE.items()}
@@ -51,6 +51,8 @@ lib.fused_add_rmsnorm_host.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64
 lib.fused_add_rmsnorm_host.restype = _int
 lib.rmsnorm_host.argtypes = [_vp, _vp, _f32, _vp, _i64, _i64, _int, _vp, _i64, _vp]
 lib.rmsnorm_host.restype = _int
+lib.fused_add_rmsnorm_host_noalloc.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _vp]
+lib.fused_add_rmsnorm_host_noalloc.restype = _int
 lib.far_selftest_wait_timeout.argtypes = [_u32, _vp]
 lib.far_selftest_wait_timeout.restype = _int
 lib.far_set_launch_override.argtypes = [_int, _int, _int, _int]

@@ -413,6 +413,23 @@ cudaError_t ensure_smem_attribute(const void* func, size_t bytes) {
   return e;
 }
 
+int check_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
+               int64_t hidden, int dtype, bool residual, int* act, int* wd, int* od) {
+  Call c;
+  const int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  if (st == FAR_OK) {
+    *act = c.act;
+    *wd = c.wd;
+    *od = c.od;
+  }
+  return st;
+}
+
+int enqueue_device_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
+                        int64_t tokens, int64_t hidden, int dtype, bool residual, cudaStream_t stream) {
+  return run(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, stream);
+}
+
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
   return cudaGetLastError();
@@ -452,6 +469,8 @@ const char* far_status_string(int status) {
     case FAR_ERR_CUDA: return g_cuda_msg;
     case FAR_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out; its outputs are incomplete";
     case FAR_ERR_WORKSPACE: return "workspace too small or misaligned for one row";
+    case FAR_ERR_SCRATCH:
+      return "one row (plus the weight) does not fit the fixed device scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }

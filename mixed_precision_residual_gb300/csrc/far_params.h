@@ -64,6 +64,12 @@ cudaError_t launch_act_f16(int wd, bool residual, const Launch& L);
 cudaError_t launch_act_bf16(int wd, bool residual, const Launch& L);
 cudaError_t launch_act_f32(int wd, bool residual, const Launch& L);
 
+// the argument checks and the device-buffer launch behind the public entry points (far_api.cu)
+int check_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
+               int64_t hidden, int dtype, bool residual, int* act, int* wd, int* od);
+int enqueue_device_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
+                        int64_t tokens, int64_t hidden, int dtype, bool residual, cudaStream_t stream);
+
 // the bounded-wait self test (far_api.cu)
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);
 
