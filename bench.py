@@ -66,6 +66,20 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job rate: the units all ranks processed in one step over the slowest rank's step time."""
+    return units_per_rank * world / (ms_per_step * 1e-3)
+
+
 def step_bytes(tokens, hidden, act, wd, od):
     """Algorithmic bytes of one step: (fused, variant)."""
     sa, sw, so = DSIZE[act], DSIZE[wd], DSIZE[od]
@@ -299,16 +313,12 @@ def main():
     status = far.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    total_ms = ev_start.elapsed_time(ev_end)
+    total_ms = max_over_ranks(ev_start.elapsed_time(ev_end), dist, dev)
     fused_ms = sum(a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)) / args.steps
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
     fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od)
-    value = (fb + nb) * world / (ms_per_step * 1e-3) / 1e9
-    tokens_per_s = T * world / (ms_per_step * 1e-3)
+    value = job_rate(fb + nb, world, ms_per_step) / 1e9
+    tokens_per_s = job_rate(T, world, ms_per_step)
 
     # end to end through the host-buffer entry points: copies inside the timed region
     e2e = None
@@ -336,17 +346,13 @@ def main():
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
         sa, sw, so = DSIZE[x.dtype], DSIZE[wt.dtype], DSIZE[od]
         h2d = T * H * sa * 2 + H * sw + T * H * sa + H * sw
         d2h = T * H * so + T * H * sa + T * H * so
-        e2e = {"value": round((fb + nb) * world / (e2e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+        e2e = {"value": round(job_rate(fb + nb, world, e2e_ms) / 1e9, 3), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
-               "tokens_per_s": round(T * world / (e2e_ms * 1e-3), 1),
+               "tokens_per_s": round(job_rate(T, world, e2e_ms), 1),
                "path": "fused_add_rmsnorm_host + rmsnorm_host (pinned host buffers, 4096-row chunks, "
                        "two internal streams)"}
         assert far.device_status() == 0
