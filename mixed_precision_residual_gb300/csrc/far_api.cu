@@ -159,13 +159,16 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   size_t smem = 0;
   if (staged) {
     // Launch table (measured on GB300 over nch x groups x slots, L2 flushed between launches):
-    //  - 8 chunks a thread (64 values of s for 16-bit data) keeps the per-row work
-    //    (reductions, IEEE divide and square root, waits) small against the per-element work;
-    //  - the fused op on long rows (more than 3 warps a row) runs best with a single group
-    //    of up to 16 warps on one row at a time and 4 ring slots;
-    //  - otherwise as many groups as 12 warps allow, one ring slot per group for the fused
-    //    op (two inputs in flight) and two for the variant (one input).
+    //  - 8 chunks a thread (64 values for 16-bit data) keeps the per-row work (reductions,
+    //    IEEE divide and square root, waits) small against the per-element work;
+    //  - long rows (4 or more warps a row at 8 chunks) want few bytes in flight: the fused op
+    //    runs one group of up to 16 warps with 4 ring slots, the no-residual variant 4 groups
+    //    with one slot each;
+    //  - shorter rows take as many groups as the warp budget allows, but no more than keeps
+    //    5 (fused) or 8 (variant) rows per group per SM, with one (fused) or two (variant)
+    //    slots per group.
     const int64_t C = row_bytes / 16;
+    const bool packed = packed_rows(c.residual, c.act);
     int slots_per_group = c.residual ? 1 : 2;
     nch = 8;
     G = (int)((C + 255) / 256);
@@ -175,23 +178,34 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       G = 1;
     }
     bool one_group = false;
-    if (c.residual && G > 3) {
-      nch = 1;
-      while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
-      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
-      one_group = true;
+    int group_cap = 1 << 30;
+    const int64_t rows_per_sm = (c.tokens + sms - 1) / sms;
+    if (G >= 4) {
+      if (c.residual) {
+        nch = 1;
+        while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
+        G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+        one_group = true;
+      } else {
+        group_cap = 4;
+        slots_per_group = 1;
+      }
+    } else {
+      const int64_t per_group = c.residual ? 5 : 8;
+      const int64_t cap = rows_per_sm / per_group;
+      group_cap = (int)(cap < 1 ? 1 : cap);
     }
     if (g_force_nch.load() > 0) {
       nch = g_force_nch.load();
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
       one_group = false;
     }
-    staged = G <= max_consumer_warps(nch);
+    staged = G <= max_consumer_warps(nch, packed);
     if (staged) {
-      const int64_t per_sm = (c.tokens + sms - 1) / sms;  // rows per SM if spread evenly
-      groups = one_group ? 1 : max_consumer_warps(nch) / G;
-      if (groups > per_sm) groups = (int)(per_sm > 0 ? per_sm : 1);
-      if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch))
+      groups = one_group ? 1 : max_consumer_warps(nch, packed) / G;
+      if (groups > group_cap) groups = group_cap;
+      if (groups > rows_per_sm) groups = (int)(rows_per_sm > 0 ? rows_per_sm : 1);
+      if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch, packed_rows(c.residual, c.act)))
         groups = g_force_groups.load();
       stage_bytes = (uint32_t)(((row_bytes + 127) / 128 * 128) * (c.residual ? 2 : 1));
       int want = one_group ? 4 : groups * slots_per_group;

@@ -122,6 +122,25 @@ template <> __device__ __forceinline__ float2 add2_mixed<FAR_BF16>(uint32_t xw, 
   return make_float2(s0, s1);
 }
 
+// fl32(x * x) for the two 16-bit x values packed in xw: the mixed-precision fma
+// widens both factors exactly and rounds once; x * x of a 16-bit x is exact in
+// binary32, so this is the binary32 square of s = x.  (Adding -0 keeps +0 for x = 0.)
+template <int DT> __device__ __forceinline__ float2 square2_mixed(uint32_t xw);
+template <> __device__ __forceinline__ float2 square2_mixed<FAR_F16>(uint32_t xw) {
+  float q0, q1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.f16 %0, lo, lo, 0f80000000;\n\tfma.rn.f32.f16 %1, hi, hi, 0f80000000;\n\t}"
+      : "=f"(q0), "=f"(q1) : "r"(xw));
+  return make_float2(q0, q1);
+}
+template <> __device__ __forceinline__ float2 square2_mixed<FAR_BF16>(uint32_t xw) {
+  float q0, q1;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, lo, lo, 0f80000000;\n\tfma.rn.f32.bf16 %1, hi, hi, 0f80000000;\n\t}"
+      : "=f"(q0), "=f"(q1) : "r"(xw));
+  return make_float2(q0, q1);
+}
+
 // vector memory access of N bytes (N = 8, 16 or 32), N-aligned
 template <int N> __device__ __forceinline__ void load_bytes(const void* p, uint32_t* w) {
   if constexpr (N == 8) {

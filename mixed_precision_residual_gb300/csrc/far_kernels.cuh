@@ -28,7 +28,7 @@
 namespace far {
 
 template <int ACT, int WD, bool RES, int NCH, bool EXACT>
-__global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Params p) {
+__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) staged_kernel(const Params p) {
   constexpr int SA = dtype_size<ACT>::value;
   constexpr int SW = dtype_size<WD>::value;
   constexpr int OD = promote(ACT, WD);
@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Param
   constexpr int V = 16 / SA;   // elements per 16-byte activation chunk
   constexpr int WB = V * SW;   // weight bytes per chunk: 8, 16 or 32
   constexpr int OB = V * SO;   // output bytes per chunk: 16 or 32
+  // no residual and 16-bit x: s = x exactly, so x stays packed between the passes
+  constexpr bool PACKED = packed_rows(RES, ACT);
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
@@ -130,12 +132,25 @@ __global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Param
     const unsigned char* xs = ring + (size_t)slot * p.stage_bytes;
 
     // pass 1 (from shared memory): s = fl32(x + r) into registers, squares into the accumulator
-    float s[NCH][V];
+    float s[PACKED ? 1 : NCH][PACKED ? 1 : V];
+    uint32_t xk[PACKED ? NCH : 1][PACKED ? V / 2 : 1];  // the packed x of the no-residual variant
     DW acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // four independent chains
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
-      if (EXACT || c < C) {
+      if constexpr (PACKED) {
+        if (EXACT || c < C) {
+          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
+          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e) {
+            xk[j][e] = xw[e];
+            const float2 q = square2_mixed<ACT>(xw[e]);
+            dw_add(acc[(2 * e) & 3], q.x);
+            dw_add(acc[(2 * e + 1) & 3], q.y);
+          }
+        }
+      } else if (EXACT || c < C) {
         const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
         const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
         if constexpr (RES) {
@@ -199,6 +214,12 @@ __global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Param
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
       if (EXACT || c < C) {
+        float sj[V];  // s for this chunk: kept in registers, or widened from the packed x
+        if constexpr (PACKED) widen<ACT, V>(xk[j], sj);
+        else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) sj[e] = s[j][e];
+        }
         uint32_t ww[WB / 4];
         load_bytes<WB>(wsm + (size_t)c * WB, ww);
         uint32_t ow[OB / 4];
@@ -207,13 +228,13 @@ __global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Param
           // then one packed multiply rounds the exact product once
 #pragma unroll
           for (int e = 0; e < V / 2; ++e)
-            ow[e] = mul2<WD>(narrow2<WD>(__fmul_rn(s[j][2 * e], rstd), __fmul_rn(s[j][2 * e + 1], rstd)), ww[e]);
+            ow[e] = mul2<WD>(narrow2<WD>(__fmul_rn(sj[2 * e], rstd), __fmul_rn(sj[2 * e + 1], rstd)), ww[e]);
         } else {
           float wf[V];
           widen<WD, V>(ww, wf);
           float o[V];
 #pragma unroll
-          for (int e = 0; e < V; ++e) o[e] = __fmul_rn(s[j][e], rstd);
+          for (int e = 0; e < V; ++e) o[e] = __fmul_rn(sj[e], rstd);
           round_through<WD, V>(o);  // cast to the weight dtype first
 #pragma unroll
           for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(max_threads(NCH), 1) staged_kernel(const Param
         store_bytes_stream<OB>(orow + (size_t)c * OB, ow);
         if constexpr (RES) {
           uint32_t rw[4];
-          narrow<ACT, V>(s[j], rw);
+          narrow<ACT, V>(sj, rw);
           store_bytes_stream<16>(rrow + (size_t)c * 16, rw);
         }
       }

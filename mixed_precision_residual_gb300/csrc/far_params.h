@@ -10,9 +10,16 @@ namespace far {
 // shapes of the staged kernel: a CTA = 1 producer warp + groups x warps_per_row consumer warps.
 // 16 consumer warps leave 96 registers a thread (17 warps: 5 on one SM sub-partition);
 // 8 chunks a thread (64 values of s) need more, so those CTAs stop at 12 (128 registers).
+// The no-residual variant on 16-bit data keeps x packed (s = x exactly), half the
+// registers, so it keeps 16 warps at 8 chunks a thread.
 constexpr int kMaxConsumerWarps = 16;
-__host__ __device__ constexpr int max_consumer_warps(int nch) { return nch >= 8 ? 12 : 16; }
-__host__ __device__ constexpr int max_threads(int nch) { return (max_consumer_warps(nch) + 1) * 32; }
+__host__ __device__ constexpr bool packed_rows(bool residual, int act) { return !residual && act != 0; }
+__host__ __device__ constexpr int max_consumer_warps(int nch, bool packed = false) {
+  return (nch >= 8 && !packed) ? 12 : 16;
+}
+__host__ __device__ constexpr int max_threads(int nch, bool packed = false) {
+  return (max_consumer_warps(nch, packed) + 1) * 32;
+}
 constexpr int kMaxDynamicSmem = 227 * 1024;
 constexpr int kGenericThreads = 256;
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
