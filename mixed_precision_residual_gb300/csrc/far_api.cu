@@ -180,7 +180,14 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     bool one_group = false;
     int group_cap = 1 << 30;
     const int64_t rows_per_sm = (c.tokens + sms - 1) / sms;
-    if (G >= 4) {
+    if (rows_per_sm <= 2) {
+      // a batch this small is latency-bound: spread each row over as many warps as it has
+      // chunks (one chunk a thread) instead of minimising the per-row overhead
+      nch = 1;
+      while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
+      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+      one_group = true;
+    } else if (G >= 4) {
       if (c.residual) {
         nch = 1;
         while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
