@@ -166,7 +166,9 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     //    with one slot each;
     //  - shorter rows take as many groups as the warp budget allows, but no more than keeps
     //    5 (fused) or 8 (variant) rows per group per SM, with one (fused) or two (variant)
-    //    slots per group.
+    //    slots per group;
+    //  - with an fp32 output, the groups keep about 128 KB (fused) or 120 KB (variant) of
+    //    rows in progress per SM, one slot each.
     const int64_t C = row_bytes / 16;
     const bool packed = packed_rows(c.residual, c.act);
     int slots_per_group = c.residual ? 1 : 2;
@@ -187,6 +189,14 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
       one_group = true;
+    } else if (c.od == FAR_F32) {
+      // fp32 output (or fp32 activations): rows are long in bytes; keep about 128 KB
+      // (fused) or 120 KB (variant) of rows in progress per SM, one ring slot per group
+      const int64_t row_total = c.hidden * (c.residual ? (3 * sa + dsize(c.od)) : (sa + dsize(c.od)));
+      const int64_t budget = c.residual ? 128 * 1024 : 120 * 1024;
+      const int64_t want = (budget + row_total / 2) / row_total;
+      group_cap = (int)(want < 1 ? 1 : want);
+      slots_per_group = 1;
     } else if (G >= 4) {
       if (c.residual) {
         nch = 1;

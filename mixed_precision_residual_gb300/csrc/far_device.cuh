@@ -155,14 +155,15 @@ template <int N> __device__ __forceinline__ void load_bytes(const void* p, uint3
   }
 }
 
-// streaming store (evict-first in L2: the outputs are not re-read by this kernel)
-template <int N> __device__ __forceinline__ void store_bytes_stream(void* p, const uint32_t* w) {
+// vector store of N bytes (N = 8, 16 or 32), N-aligned; default L2 policy, so a
+// following kernel can still find the tail of the output in L2
+template <int N> __device__ __forceinline__ void store_bytes(void* p, const uint32_t* w) {
   if constexpr (N == 8) {
-    asm volatile("st.global.cs.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1]) : "memory");
+    asm volatile("st.global.v2.b32 [%0], {%1, %2};" ::"l"(p), "r"(w[0]), "r"(w[1]) : "memory");
   } else {
 #pragma unroll
     for (int k = 0; k < N / 16; ++k)
-      asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<char*>(p) + 16 * k),
+      asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(reinterpret_cast<char*>(p) + 16 * k),
                    "r"(w[4 * k]), "r"(w[4 * k + 1]), "r"(w[4 * k + 2]), "r"(w[4 * k + 3])
                    : "memory");
   }
@@ -311,21 +312,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // global -> this CTA's shared memory, completion counted in bytes on `bar`
 // (plain copy into the CTA's own shared memory: no multicast)
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                          uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
-      : "memory");
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 }  // namespace far

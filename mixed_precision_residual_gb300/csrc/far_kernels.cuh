@@ -63,14 +63,13 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
   const int64_t first = n_local < stages ? n_local : stages;  // rows issued before the weight load
 
   // producer: one bulk copy of row k's x (and residual) into ring slot k % stages
-  auto issue = [&](int64_t k, int slot, uint64_t pol) {
+  auto issue = [&](int64_t k, int slot) {
     const int64_t row = b + k * nb;
     const uint32_t full = smem_addr(&bars[slot]);
     const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
     mbar_arrive_expect_tx(full, tx);
-    bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full, pol);
-    if constexpr (RES)
-      bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full, pol);
+    bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full);
+    if constexpr (RES) bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full);
   };
 
   if (threadIdx.x == 0) {
@@ -81,8 +80,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
     for (int i = 0; i < 2 * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
     fence_barrier_init();
     // the first `stages` rows need no free slot: start them now, under the weight load
-    const uint64_t pol = l2_evict_first_policy();
-    for (int64_t k = 0; k < first; ++k) issue(k, (int)k, pol);
+    for (int64_t k = 0; k < first; ++k) issue(k, (int)k);
   }
   {  // the weight row, once per CTA (16-byte aligned; hidden * SW is even)
     const int nbytes = p.hidden * SW;
@@ -98,14 +96,13 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
       int64_t k = first;
       int slot = (int)(first % stages);
       uint32_t phase = (uint32_t)(first / stages) & 1u;  // (k / stages) & 1
       for (; k < n_local; ++k) {
         // slot k % stages was last used by row k - stages: wait until its consumers released it
         if (!mbar_wait(smem_addr(&bars[stages + slot]), phase ^ 1u, p.timeout_ns, p.status)) break;
-        issue(k, slot, pol);
+        issue(k, slot);
         if (++slot == stages) {
           slot = 0;
           phase ^= 1u;
@@ -240,11 +237,11 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
           for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
           narrow<OD, V>(o, ow);
         }
-        store_bytes_stream<OB>(orow + (size_t)c * OB, ow);
+        store_bytes<OB>(orow + (size_t)c * OB, ow);
         if constexpr (RES) {
           uint32_t rw[4];
           narrow<ACT, V>(sj, rw);
-          store_bytes_stream<16>(rrow + (size_t)c * 16, rw);
+          store_bytes<16>(rrow + (size_t)c * 16, rw);
         }
       }
     }
