@@ -84,6 +84,36 @@ int fused_add_rmsnorm(const void* x, const void* residual, const void* weight, f
 int rmsnorm(const void* x, const void* weight, float eps, void* out,
             int64_t tokens, int64_t hidden, int dtype, void* stream);
 
+/*
+ * Strided rows: the same two operations on matrices whose consecutive rows are
+ * *_row_stride ELEMENTS apart (each >= hidden; elements within a row stay
+ * contiguous), e.g. column slices of wider matrices.  Rows whose starts are all
+ * 16-byte aligned take the bulk-copy path; others the generic kernel, with the
+ * same results.  Aliasing: an output may be exactly an input (same pointer,
+ * stride and element size); otherwise no byte may be shared.  Regions with equal
+ * strides are checked exactly (interleaved column slices of one buffer are
+ * fine); regions with different strides must not even share their spanned
+ * ranges.  FAR_ERR_SHAPE for a stride below hidden.
+ */
+int fused_add_rmsnorm_strided(const void* x, int64_t x_row_stride, const void* residual,
+                              int64_t residual_row_stride, const void* weight, float eps, void* out,
+                              int64_t out_row_stride, void* residual_out, int64_t residual_out_row_stride,
+                              int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+int rmsnorm_strided(const void* x, int64_t x_row_stride, const void* weight, float eps, void* out,
+                    int64_t out_row_stride, int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+/*
+ * The argument checks of the strided entry points alone (no CUDA call, no memory
+ * access): the status fused_add_rmsnorm_strided (has_residual = 1) or
+ * rmsnorm_strided (has_residual = 0, residual arguments ignored) would return
+ * before launching anything.
+ */
+int far_validate_strided(const void* x, int64_t x_row_stride, const void* residual, int64_t residual_row_stride,
+                         const void* weight, float eps, const void* out, int64_t out_row_stride,
+                         const void* residual_out, int64_t residual_out_row_stride, int64_t tokens, int64_t hidden,
+                         int dtype, int has_residual);
+
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
 int far_output_dtype(int dtype);
 

@@ -39,6 +39,12 @@ lib.fused_add_rmsnorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _in
 lib.fused_add_rmsnorm.restype = _int
 lib.rmsnorm.argtypes = [_vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
 lib.rmsnorm.restype = _int
+lib.fused_add_rmsnorm_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _f32, _vp, _i64, _vp, _i64, _i64, _i64, _int, _vp]
+lib.fused_add_rmsnorm_strided.restype = _int
+lib.rmsnorm_strided.argtypes = [_vp, _i64, _vp, _f32, _vp, _i64, _i64, _i64, _int, _vp]
+lib.rmsnorm_strided.restype = _int
+lib.far_validate_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _f32, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int]
+lib.far_validate_strided.restype = _int
 lib.far_output_dtype.argtypes = [_int]
 lib.far_output_dtype.restype = _int
 lib.far_status_string.argtypes = [_int]
@@ -100,43 +106,67 @@ def _rows(x: torch.Tensor) -> tuple[int, int]:
     return (x.numel() // hidden if hidden else 0), hidden
 
 
+def _row_stride(t: torch.Tensor) -> int | None:
+    """Row stride in elements of a 2-D tensor with contiguous rows, else None."""
+    if t.dim() == 2 and (t.stride(1) == 1 or t.shape[1] == 1):
+        return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+    return None
+
+
 def fused_add_rmsnorm(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor, eps: float,
                       out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None,
                       stream=None):
     """out, residual_out = RMSNorm(x + residual) * weight under the rounding contract.
 
-    x, residual: [..., hidden] contiguous CUDA tensors of one dtype; weight:
-    [hidden].  Outputs are allocated when not given (out in the promoted dtype);
-    pass out=x / residual_out=residual for in-place use.
+    x, residual: [..., hidden] CUDA tensors of one dtype, contiguous, or 2-D with
+    contiguous rows and any row stride (column slices); weight: [hidden].  Outputs
+    are allocated when not given (out in the promoted dtype); pass out=x /
+    residual_out=residual for in-place use.
     """
-    if not (x.is_contiguous() and residual.is_contiguous() and weight.is_contiguous()):
-        raise ValueError("x, residual and weight must be contiguous")
+    if not weight.is_contiguous():
+        raise ValueError("weight must be contiguous")
     code = dtypes(x.dtype, weight.dtype)
     if residual.dtype != x.dtype:
         raise ValueError("x and residual must share a dtype")
     if out is None:
         out = torch.empty(x.shape, dtype=output_dtype(x.dtype, weight.dtype), device=x.device)
     if residual_out is None:
-        residual_out = torch.empty_like(x)
+        residual_out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     tokens, hidden = _rows(x)
     if weight.numel() != hidden or residual.shape != x.shape or out.shape != x.shape or residual_out.shape != x.shape:
         raise ValueError("shape mismatch")
-    _check(lib.fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(out), _ptr(residual_out),
-                                 tokens, hidden, code, _stream_handle(stream)))
+    ts = (x, residual, out, residual_out)
+    if all(t.is_contiguous() for t in ts):
+        _check(lib.fused_add_rmsnorm(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(out), _ptr(residual_out),
+                                     tokens, hidden, code, _stream_handle(stream)))
+    else:
+        st = [_row_stride(t) for t in ts]
+        if None in st:
+            raise ValueError("non-contiguous tensors must be 2-D with contiguous rows")
+        _check(lib.fused_add_rmsnorm_strided(_ptr(x), st[0], _ptr(residual), st[1], _ptr(weight), eps, _ptr(out),
+                                             st[2], _ptr(residual_out), st[3], tokens, hidden, code,
+                                             _stream_handle(stream)))
     return out, residual_out
 
 
 def rmsnorm(x: torch.Tensor, weight: torch.Tensor, eps: float, out: torch.Tensor | None = None, stream=None):
     """out = RMSNorm(x) * weight under the rounding contract (no residual)."""
-    if not (x.is_contiguous() and weight.is_contiguous()):
-        raise ValueError("x and weight must be contiguous")
+    if not weight.is_contiguous():
+        raise ValueError("weight must be contiguous")
     code = dtypes(x.dtype, weight.dtype)
     if out is None:
         out = torch.empty(x.shape, dtype=output_dtype(x.dtype, weight.dtype), device=x.device)
     tokens, hidden = _rows(x)
     if weight.numel() != hidden or out.shape != x.shape:
         raise ValueError("shape mismatch")
-    _check(lib.rmsnorm(_ptr(x), _ptr(weight), eps, _ptr(out), tokens, hidden, code, _stream_handle(stream)))
+    if x.is_contiguous() and out.is_contiguous():
+        _check(lib.rmsnorm(_ptr(x), _ptr(weight), eps, _ptr(out), tokens, hidden, code, _stream_handle(stream)))
+    else:
+        sx, so = _row_stride(x), _row_stride(out)
+        if sx is None or so is None:
+            raise ValueError("non-contiguous tensors must be 2-D with contiguous rows")
+        _check(lib.rmsnorm_strided(_ptr(x), sx, _ptr(weight), eps, _ptr(out), so, tokens, hidden, code,
+                                   _stream_handle(stream)))
     return out
 
 

@@ -84,17 +84,50 @@ int decode(int dtype, int& act, int& wd, int& od) {
 
 int dsize(int dt) { return dt == FAR_F32 ? 4 : 2; }
 
-bool overlap(const void* a, uint64_t na, const void* b, uint64_t nb) {
-  if (!a || !b || na == 0 || nb == 0) return false;
-  uint64_t pa = (uint64_t)(uintptr_t)a, pb = (uint64_t)(uintptr_t)b;
-  return pa < pb + nb && pb < pa + na;
+// Row strides in elements (each >= hidden); the contiguous entry points pass hidden.
+struct Strides {
+  int64_t x, r, out, res;
+};
+
+// A strided tensor in memory: `rows` rows of `width` bytes, `stride` bytes apart.
+struct Region {
+  uint64_t base;
+  int64_t rows, width, stride;
+};
+
+Region region(const void* p, int64_t rows, int64_t width, int64_t stride) {
+  return Region{(uint64_t)(uintptr_t)p, rows, width, stride};
 }
 
-// an output may coincide exactly with an input of the same size; nothing else may overlap it
-bool bad_overlap(const void* o, uint64_t no, const void* in, uint64_t nin) {
-  if (!overlap(o, no, in, nin)) return false;
-  return !(o == in && no == nin);
+int64_t floor_div(int64_t a, int64_t b) {  // b > 0
+  return a >= 0 ? a / b : -((-a + b - 1) / b);
 }
+
+// Do any bytes of A and B coincide?  Exact for equal strides (rows of two column
+// slices of one matrix interleave without touching); otherwise any overlap of the
+// spanned byte ranges counts.
+bool regions_overlap(const Region& A, const Region& B) {
+  if (A.rows == 0 || B.rows == 0 || A.width == 0 || B.width == 0) return false;
+  const uint64_t a_end = A.base + (uint64_t)((A.rows - 1) * A.stride + A.width);
+  const uint64_t b_end = B.base + (uint64_t)((B.rows - 1) * B.stride + B.width);
+  if (!(A.base < b_end && B.base < a_end)) return false;
+  if (A.stride != B.stride || A.rows == 1 || B.rows == 1) return true;
+  // row i of A and row j of B meet iff -B.width < d + (j - i) * s < A.width, d = B.base - A.base
+  const int64_t s = A.stride;
+  const int64_t d = (int64_t)(B.base - A.base);
+  const int64_t kmin = floor_div(-B.width - d, s) + 1;
+  const int64_t kmax = -floor_div(-(A.width - d), s) - 1;  // ceil((A.width - d) / s) - 1
+  const int64_t lo = kmin > -(B.rows - 1) ? kmin : -(B.rows - 1);
+  const int64_t hi = kmax < (A.rows - 1) ? kmax : (A.rows - 1);
+  return lo <= hi;
+}
+
+bool same_region(const Region& A, const Region& B) {
+  return A.base == B.base && A.rows == B.rows && A.width == B.width && A.stride == B.stride;
+}
+
+// an output may be exactly an input region (in place); no other byte may be shared
+bool bad_overlap(const Region& out, const Region& in) { return regions_overlap(out, in) && !same_region(out, in); }
 
 struct Call {
   const void* x;
@@ -106,27 +139,35 @@ struct Call {
   int64_t tokens, hidden;
   int act, wd, od;
   bool residual;
+  Strides st;  // elements
 };
 
 int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
-             int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c) {
+             int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c, const Strides* strides = nullptr) {
   int st = decode(dtype, c.act, c.wd, c.od);
   if (st != FAR_OK) return st;
   if (hidden <= 0 || hidden > kMaxHidden || tokens < 0) return FAR_ERR_SHAPE;
-  // byte sizes must fit in int64 (and in the kernels' 64-bit offsets)
-  if (tokens > (INT64_MAX / 8) / hidden) return FAR_ERR_SHAPE;
+  const Strides sd = strides ? *strides : Strides{hidden, hidden, hidden, hidden};
+  const int64_t widest = residual ? (sd.x > sd.r ? sd.x : sd.r) : sd.x;
+  const int64_t wider = residual ? (sd.out > sd.res ? sd.out : sd.res) : sd.out;
+  if (sd.x < hidden || sd.out < hidden || (residual && (sd.r < hidden || sd.res < hidden))) return FAR_ERR_SHAPE;
+  // byte offsets must fit in int64 (and in the kernels' 64-bit offsets)
+  const int64_t max_stride = widest > wider ? widest : wider;
+  if (tokens > (INT64_MAX / 8) / max_stride) return FAR_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps == INFINITY) return FAR_ERR_EPS;
-  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual};
+  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual, sd};
   if (tokens == 0) return FAR_OK;
   if (!x || !w || !out || (residual && (!r || !res_out))) return FAR_ERR_NULL;
-  const uint64_t na = (uint64_t)tokens * hidden * dsize(c.act);
-  const uint64_t no = (uint64_t)tokens * hidden * dsize(c.od);
-  const uint64_t nw = (uint64_t)hidden * dsize(c.wd);
-  if (bad_overlap(out, no, x, na) || overlap(out, no, w, nw)) return FAR_ERR_ALIAS;
+  const int64_t sa = dsize(c.act), so = dsize(c.od);
+  const Region X = region(x, tokens, hidden * sa, sd.x * sa);
+  const Region O = region(out, tokens, hidden * so, sd.out * so);
+  const Region W = region(w, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
+  if (bad_overlap(O, X) || regions_overlap(O, W)) return FAR_ERR_ALIAS;
   if (residual) {
-    if (bad_overlap(out, no, r, na) || overlap(out, no, res_out, na)) return FAR_ERR_ALIAS;
-    if (bad_overlap(res_out, na, x, na) || bad_overlap(res_out, na, r, na) || overlap(res_out, na, w, nw))
-      return FAR_ERR_ALIAS;
+    const Region R = region(r, tokens, hidden * sa, sd.r * sa);
+    const Region RO = region(res_out, tokens, hidden * sa, sd.res * sa);
+    if (bad_overlap(O, R) || regions_overlap(O, RO)) return FAR_ERR_ALIAS;
+    if (bad_overlap(RO, X) || bad_overlap(RO, R) || regions_overlap(RO, W)) return FAR_ERR_ALIAS;
   }
   return FAR_OK;
 }
@@ -152,7 +193,15 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
 
   const int sa = dsize(c.act), sw = dsize(c.wd);
   const int64_t row_bytes = c.hidden * sa;
-  bool staged = g_force_kind.load() != kGeneric && row_bytes % 16 == 0 && aligned16(c.x) &&
+  const int so = dsize(c.od);
+  p.x_stride = c.st.x * sa;
+  p.r_stride = c.st.r * sa;
+  p.out_stride = c.st.out * so;
+  p.res_stride = c.st.res * sa;
+  // the bulk-copy path needs every row start on a 16-byte boundary
+  const bool rows_aligned = p.x_stride % 16 == 0 && p.out_stride % 16 == 0 &&
+                            (!c.residual || (p.r_stride % 16 == 0 && p.res_stride % 16 == 0));
+  bool staged = g_force_kind.load() != kGeneric && row_bytes % 16 == 0 && rows_aligned && aligned16(c.x) &&
                 aligned16(c.w) && aligned16(c.out) && (!c.residual || (aligned16(c.r) && aligned16(c.res_out)));
   int nch = 0, G = 0, groups = 0, stages = 0;
   uint32_t stage_bytes = 0, w_bytes = (uint32_t)((c.hidden * sw + 15) / 16 * 16);
@@ -290,9 +339,9 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
 }
 
 int run(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
-        int64_t hidden, int dtype, bool residual, void* stream) {
+        int64_t hidden, int dtype, bool residual, void* stream, const Strides* strides = nullptr) {
   Call c;
-  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c, strides);
   if (st != FAR_OK || tokens == 0) return st;
   DeviceState* dev = nullptr;
   st = current_device(dev);
@@ -397,6 +446,7 @@ int run_host(const void* x, const void* r, const void* w, float eps, void* out, 
     cc.out = od;
     cc.res_out = residual ? rod : nullptr;
     cc.tokens = n;
+    cc.st = Strides{hidden, hidden, hidden, hidden};  // the workspace slots are contiguous
     st = launch(cc, *dev, ps);
     if (st != FAR_OK) return st;
     e = cudaMemcpyAsync(static_cast<char*>(out) + out_off, od, n * hidden * so, cudaMemcpyDeviceToHost, ps);
@@ -480,6 +530,32 @@ int fused_add_rmsnorm(const void* x, const void* residual, const void* weight, f
 int rmsnorm(const void* x, const void* weight, float eps, void* out, int64_t tokens, int64_t hidden, int dtype,
             void* stream) {
   return run(x, nullptr, weight, eps, out, nullptr, tokens, hidden, dtype, false, stream);
+}
+
+int fused_add_rmsnorm_strided(const void* x, int64_t x_row_stride, const void* residual,
+                              int64_t residual_row_stride, const void* weight, float eps, void* out,
+                              int64_t out_row_stride, void* residual_out, int64_t residual_out_row_stride,
+                              int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  const Strides sd{x_row_stride, residual_row_stride, out_row_stride, residual_out_row_stride};
+  return run(x, residual, weight, eps, out, residual_out, tokens, hidden, dtype, true, stream, &sd);
+}
+
+int far_validate_strided(const void* x, int64_t x_row_stride, const void* residual, int64_t residual_row_stride,
+                         const void* weight, float eps, const void* out, int64_t out_row_stride,
+                         const void* residual_out, int64_t residual_out_row_stride, int64_t tokens, int64_t hidden,
+                         int dtype, int has_residual) {
+  const Strides sd{x_row_stride, has_residual ? residual_row_stride : hidden, out_row_stride,
+                   has_residual ? residual_out_row_stride : hidden};
+  Call c;
+  return validate(x, has_residual ? residual : nullptr, weight, eps, const_cast<void*>(out),
+                  has_residual ? const_cast<void*>(residual_out) : nullptr, tokens, hidden, dtype, has_residual != 0, c,
+                  &sd);
+}
+
+int rmsnorm_strided(const void* x, int64_t x_row_stride, const void* weight, float eps, void* out,
+                    int64_t out_row_stride, int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  const Strides sd{x_row_stride, hidden, out_row_stride, hidden};
+  return run(x, nullptr, weight, eps, out, nullptr, tokens, hidden, dtype, false, stream, &sd);
 }
 
 int far_output_dtype(int dtype) {

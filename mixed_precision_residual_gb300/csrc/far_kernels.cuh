@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
     const uint32_t full = smem_addr(&bars[slot]);
     const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
     mbar_arrive_expect_tx(full, tx);
-    bulk_load(dst, static_cast<const char*>(p.x) + row * p.row_bytes, p.row_bytes, full);
-    if constexpr (RES) bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.row_bytes, p.row_bytes, full);
+    bulk_load(dst, static_cast<const char*>(p.x) + row * p.x_stride, p.row_bytes, full);
+    if constexpr (RES) bulk_load(dst + r_off, static_cast<const char*>(p.r) + row * p.r_stride, p.row_bytes, full);
   };
 
   if (threadIdx.x == 0) {
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
 
     // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w)
     const int64_t row = b + k * nb;
-    char* orow = static_cast<char*>(p.out) + row * (int64_t)p.hidden * SO;
-    char* rrow = RES ? static_cast<char*>(p.res_out) + row * (int64_t)p.row_bytes : nullptr;
+    char* orow = static_cast<char*>(p.out) + row * p.out_stride;
+    char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
@@ -273,16 +273,14 @@ template <int DT> __device__ __forceinline__ float round_one(float v) {
 
 template <int ACT, int WD, bool RES>
 __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p) {
-  constexpr int SA = dtype_size<ACT>::value;
   constexpr int OD = promote(ACT, WD);
-  constexpr int SO = dtype_size<OD>::value;
   constexpr int NW = kGenericThreads / 32;
   __shared__ float2 part[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t H = p.hidden;
   for (int64_t row = blockIdx.x; row < p.tokens; row += gridDim.x) {
-    const char* xr = static_cast<const char*>(p.x) + row * H * SA;
-    const char* rr = RES ? static_cast<const char*>(p.r) + row * H * SA : nullptr;
+    const char* xr = static_cast<const char*>(p.x) + row * p.x_stride;
+    const char* rr = RES ? static_cast<const char*>(p.r) + row * p.r_stride : nullptr;
     DW acc{0.f, 0.f};
     for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
       float s = load_elem<ACT>(xr, i);
@@ -296,8 +294,8 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
     for (int i = 1; i < NW; ++i) tot = dw_combine(tot, DW{part[i].x, part[i].y});
     __syncthreads();  // `part` is reused by the next row
     const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
-    char* orow = static_cast<char*>(p.out) + row * H * SO;
-    char* rrow = RES ? static_cast<char*>(p.res_out) + row * H * SA : nullptr;
+    char* orow = static_cast<char*>(p.out) + row * p.out_stride;
+    char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
     for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
       float s = load_elem<ACT>(xr, i);  // each element is read and written by the same thread
       if constexpr (RES) {

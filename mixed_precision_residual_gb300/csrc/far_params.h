@@ -39,6 +39,10 @@ struct Params {
   int32_t groups;        // rows processed concurrently per CTA (staged kernel)
   int32_t stages;        // shared-memory ring slots (staged kernel)
   uint32_t row_bytes;    // hidden * sizeof(act)
+  int64_t x_stride;      // bytes between consecutive rows of x
+  int64_t r_stride;      // ... of the residual
+  int64_t out_stride;    // ... of out
+  int64_t res_stride;    // ... of residual_out
   uint32_t w_smem_bytes; // hidden * sizeof(wd), rounded up to 16
   uint32_t stage_bytes;  // bytes of one ring slot (x row, then residual row), 128-aligned
   unsigned int* status;  // device error word

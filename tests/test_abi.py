@@ -160,3 +160,33 @@ def test_launch_plans_are_consistent(far):
                 assert 1 <= p["grid"] <= min(sms, -(-tokens // g))
     finally:
         far.set_launch_override()
+
+
+def strided(far, x=FAKE, xs=256, r=FAKE + (1 << 30), rs=256, w=FAKE + (2 << 30), out=FAKE + (3 << 30), os_=256,
+            ro=FAKE + (4 << 30), ros=256, tokens=4, hidden=64, dtype=None, res=1):
+    """The strided entry point's argument checks alone (host logic, no CUDA call)."""
+    dtype = code("bf16", "bf16") if dtype is None else dtype
+    return far.lib.far_validate_strided(x, xs, r, rs, w, 1e-6, out, os_, ro, ros, tokens, hidden, dtype, res)
+
+
+def test_strided_validation(far):
+    """Strided aliasing: equal-stride column slices of one buffer may interleave; any
+    shared byte is rejected; an output may be exactly its input (in place)."""
+    B = FAKE + (8 << 30)  # a [4, 256] bf16 buffer holding four [4, 64] column slices
+    ok = dict(x=B, xs=256, out=B + 128, os_=256, ro=B + 256, ros=256, r=B + 384, rs=256)
+    assert strided(far, **ok) == 0                      # interleaved slices share no byte
+    assert strided(far, **dict(ok, out=B + 64)) == 5     # out shares half its columns with x
+    assert strided(far, **dict(ok, out=B + 512)) == 5    # out rows shifted by one row: overlap
+    assert strided(far, **dict(ok, out=B + 2)) == 5      # a partial overlap
+    assert strided(far, **dict(ok, out=B)) == 0          # out exactly x: in place
+    assert strided(far, **dict(ok, ro=B + 384)) == 0     # residual_out exactly the residual: in place
+    assert strided(far, **dict(ok, ro=B + 128)) == 5     # residual_out == out
+    assert strided(far, **dict(ok, os_=320)) == 5        # different strides whose spans overlap
+    assert strided(far, **dict(ok, xs=32)) == 4          # a stride below hidden
+    assert strided(far, **dict(ok, ros=63)) == 4
+    assert strided(far, **dict(ok, x=None)) == 3
+    # rows far apart in memory (stride much larger than the row) never touch
+    assert strided(far, x=B, xs=4096, out=B + 1024, os_=4096, ro=B + 2048, ros=4096, r=B + 3072, rs=4096) == 0
+    # the no-residual variant ignores the residual arguments
+    assert strided(far, res=0, r=B, ro=B, **{k: v for k, v in ok.items() if k not in ("r", "ro")}) == 0
+    assert strided(far, res=0, r=None, ro=None, x=B, xs=256, out=B + 100, os_=256) == 5

@@ -200,3 +200,69 @@ def test_subnormal_products(far, act):
     w[::7] = torch.linspace(-1, 1, len(w[::7]), dtype=torch.float64) * tiny * 2 ** -8
     d = dict(d, w=w.to(d["w"].dtype))
     check_both(far, d, f"subnormal products {act}")
+
+
+def _canary_like(shape, dtype):
+    t = torch.empty(shape, dtype=dtype, device="cuda")
+    t.view(torch.int16 if t.element_size() == 2 else torch.int32).fill_(0x3A5A)
+    return t
+
+
+@pytest.mark.parametrize("act,wd,extra", [("bf16", "bf16", 64), ("f16", "f32", 8), ("f32", "f32", 3),
+                                          ("bf16", "bf16", 1)])
+def test_strided_rows(far, act, wd, extra):
+    """x, residual, out and residual_out as column slices of wider matrices (row stride
+    hidden + extra elements); the columns outside the slices must stay untouched.  A
+    stride that breaks 16-byte row alignment (extra = 1 or 3) takes the generic kernel."""
+    T, H = 300, 2048
+    d = far_gen.custom_inputs(act, wd, T, H, seed=extra)
+    S = H + extra
+    xbig = _canary_like((T, S), d["x"].dtype)
+    rbig = _canary_like((T, S), d["x"].dtype)
+    xbig[:, :H] = d["x"].cuda()
+    rbig[:, :H] = d["r"].cuda()
+    od = far.output_dtype(d["x"].dtype, d["w"].dtype)
+    obig = _canary_like((T, S), od)
+    robig = _canary_like((T, S), d["x"].dtype)
+    keep = [t[:, H:].clone() for t in (obig, robig)]
+    out, res = far.fused_add_rmsnorm(xbig[:, :H], rbig[:, :H], d["w"].cuda(), d["eps"],
+                                     out=obig[:, :H], residual_out=robig[:, :H])
+    assert far.device_status() == 0
+    ref_out, ref_res = oracle_fused(d)
+    gate(out.cpu(), ref_out, res.cpu(), ref_res, f"strided {act}/{wd} +{extra}")
+    assert torch.equal(obig[:, H:], keep[0]) and torch.equal(robig[:, H:], keep[1]), "wrote outside the slices"
+    # the no-residual variant on the same slices
+    o2big = _canary_like((T, S), od)
+    nout = far.rmsnorm(xbig[:, :H], d["w"].cuda(), d["eps"], out=o2big[:, :H])
+    assert far.device_status() == 0
+    gate(nout.cpu(), oracle_norm(d), where=f"strided rmsnorm {act}/{wd} +{extra}")
+    assert (o2big[:, H:].view(torch.int16 if o2big.element_size() == 2 else torch.int32) == 0x3A5A).all()
+
+
+def test_interleaved_slices_of_one_buffer(far):
+    """x, out, residual_out and residual as four interleaved column slices of one buffer."""
+    T, H = 200, 1024
+    d = far_gen.custom_inputs("f16", "f16", T, H, seed=31)
+    buf = torch.empty((T, 4 * H), dtype=torch.float16, device="cuda")
+    buf[:, 0:H] = d["x"].cuda()
+    buf[:, 3 * H:4 * H] = d["r"].cuda()
+    out, res = far.fused_add_rmsnorm(buf[:, 0:H], buf[:, 3 * H:], d["w"].cuda(), d["eps"],
+                                     out=buf[:, H:2 * H], residual_out=buf[:, 2 * H:3 * H])
+    assert far.device_status() == 0
+    ref_out, ref_res = oracle_fused(d)
+    gate(out.cpu(), ref_out, res.cpu(), ref_res, "interleaved slices")
+    assert torch.equal(buf[:, 0:H].cpu(), d["x"]) and torch.equal(buf[:, 3 * H:].cpu(), d["r"])
+
+
+def test_strided_in_place(far):
+    T, H = 150, 4096
+    d = far_gen.custom_inputs("bf16", "bf16", T, H, seed=32)
+    xbig = torch.zeros((T, H + 512), dtype=torch.bfloat16, device="cuda")
+    rbig = torch.zeros((T, H + 512), dtype=torch.bfloat16, device="cuda")
+    xbig[:, :H] = d["x"].cuda()
+    rbig[:, :H] = d["r"].cuda()
+    out, res = far.fused_add_rmsnorm(xbig[:, :H], rbig[:, :H], d["w"].cuda(), d["eps"],
+                                     out=xbig[:, :H], residual_out=rbig[:, :H])
+    assert far.device_status() == 0
+    ref_out, ref_res = oracle_fused(d)
+    gate(xbig[:, :H].cpu(), ref_out, rbig[:, :H].cpu(), ref_res, "strided in place")
