@@ -73,6 +73,16 @@ def bind(path: str) -> ctypes.CDLL:
     l.oracle_f16_to_f32.restype = f32
     l.oracle_bf16_to_f32.argtypes = [u16]
     l.oracle_bf16_to_f32.restype = f32
+    l.oracle_fused_add_rmsnorm_quant.argtypes = [vp, vp, vp, f32, vp, vp, vp, i64, i64, i32, i32, i32]
+    l.oracle_fused_add_rmsnorm_quant.restype = i32
+    l.oracle_rmsnorm_quant.argtypes = [vp, vp, f32, vp, vp, i64, i64, i32, i32, i32]
+    l.oracle_rmsnorm_quant.restype = i32
+    l.oracle_f32_to_e4m3.argtypes = [f32]
+    l.oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    l.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    l.oracle_e4m3_to_f32.restype = f32
+    l.oracle_f32_to_int8.argtypes = [f32]
+    l.oracle_f32_to_int8.restype = i32
     return l
 
 
@@ -177,3 +187,53 @@ def row_stats(x: torch.Tensor, residual: torch.Tensor | None, eps: float, act: s
 def exact_sum(values: np.ndarray, L: ctypes.CDLL | None = None) -> np.float32:
     v = np.ascontiguousarray(values, dtype=np.float32)
     return np.float32((L or lib()).oracle_exact_sum(v.ctypes.data, v.size))
+
+
+QTYPE_CODE = {"int8": 1, "fp8": 2}
+Q_TORCH = {"int8": torch.int8, "fp8": torch.uint8}  # fp8 E4M3 codes held as bytes
+
+
+def fused_add_rmsnorm_quant(x, residual, weight, eps, act, wd, qtype, threads=None, L=None):
+    """Oracle of the fused op with a per-token quantised output: (q, scale, residual_out)."""
+    L = L or lib()
+    if output_dtype(act, wd, L) is None:
+        raise ValueError(f"dtype pair ({act}, {wd}) is rejected by the dtype policy")
+    T, H = x.shape
+    x, residual, weight = x.contiguous(), residual.contiguous(), weight.contiguous()
+    q = torch.empty((T, H), dtype=Q_TORCH[qtype])
+    scale = torch.empty(T, dtype=torch.float32)
+    res_out = torch.empty((T, H), dtype=TORCH_DTYPE[act])
+    sa = x.element_size()
+
+    def work(t0, t1):
+        rc = L.oracle_fused_add_rmsnorm_quant(
+            x.data_ptr() + t0 * H * sa, residual.data_ptr() + t0 * H * sa, weight.data_ptr(), eps,
+            q.data_ptr() + t0 * H, scale.data_ptr() + t0 * 4, res_out.data_ptr() + t0 * H * sa,
+            t1 - t0, H, DTYPE_CODE[act], DTYPE_CODE[wd], QTYPE_CODE[qtype])
+        if rc != 0:
+            raise RuntimeError(f"oracle_fused_add_rmsnorm_quant returned {rc}")
+
+    _rows_parallel(work, T, threads or default_threads())
+    return q, scale, res_out
+
+
+def rmsnorm_quant(x, weight, eps, act, wd, qtype, threads=None, L=None):
+    """Oracle of the no-residual variant with a per-token quantised output: (q, scale)."""
+    L = L or lib()
+    if output_dtype(act, wd, L) is None:
+        raise ValueError(f"dtype pair ({act}, {wd}) is rejected by the dtype policy")
+    T, H = x.shape
+    x, weight = x.contiguous(), weight.contiguous()
+    q = torch.empty((T, H), dtype=Q_TORCH[qtype])
+    scale = torch.empty(T, dtype=torch.float32)
+    sa = x.element_size()
+
+    def work(t0, t1):
+        rc = L.oracle_rmsnorm_quant(x.data_ptr() + t0 * H * sa, weight.data_ptr(), eps, q.data_ptr() + t0 * H,
+                                    scale.data_ptr() + t0 * 4, t1 - t0, H, DTYPE_CODE[act], DTYPE_CODE[wd],
+                                    QTYPE_CODE[qtype])
+        if rc != 0:
+            raise RuntimeError(f"oracle_rmsnorm_quant returned {rc}")
+
+    _rows_parallel(work, T, threads or default_threads())
+    return q, scale

@@ -39,6 +39,19 @@
  *  - Rounding is to nearest, ties to even, everywhere; no flush to zero;
  *    overflow of a 16-bit format gives infinity; NaN propagates.
  *
+ * Quantised output (the variants with a per-token scale), following the
+ * "Mixed-Precision Kernels" page, section "Quantised Kernels: INT8 and FP8
+ * Inference" (symmetric scale = max_abs / 127), applied per row to the
+ * contract's out values, so the fused result equals normalising and then
+ * quantising separately:
+ *   amax  = max_i |out_i|                      (a NaN in the row makes it NaN)
+ *   scale = fl32(amax / QMAX)                  QMAX = 127 (int8) or 448 (FP8 E4M3)
+ *   inv   = fl32(QMAX / amax), 0 when amax = 0
+ *   q_i   = Q(fl32(out_i * inv))               int8: nearest integer, ties to even,
+ *                                              clamped to [-127, 127], NaN -> 0;
+ *                                              E4M3: nearest, ties to even, finite
+ *                                              values saturated to +-448, NaN stays NaN
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math (binary32
  * arithmetic must not be fused or reassociated).
  */
@@ -134,6 +147,50 @@ static uint16_t encode_bf16(float v) {
 }
 
 static float decode_bf16(uint16_t h) { return float_of((uint32_t)h << 16); }
+
+/* ---- FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 fraction bits; no
+   infinities; S.1111.111 is NaN, so the largest finite value is 1.75 * 2^8 = 448) */
+
+/* nearest E4M3 value (ties to even), finite values saturated to +-448 */
+static float round_e4m3_satfinite(float v) {
+    if (isnan(v)) return v;
+    float r = isinf(v) ? v : round_to_format(v, 4, -6, 8);  /* 480 = 1.111b * 2^8 is NaN, not a value */
+    if (r > 448.0f) r = 448.0f;
+    if (r < -448.0f) r = -448.0f;
+    return r;
+}
+
+static uint8_t encode_e4m3(float v) {  /* v is an E4M3 value or NaN */
+    uint32_t b = bits_of(v);
+    uint8_t sign = (uint8_t)((b >> 24) & 0x80u);
+    if (isnan(v)) return (uint8_t)(sign | 0x7fu);
+    if (v == 0.0f) return sign;
+    int e = (int)((b >> 23) & 0xffu) - 127;
+    uint32_t m = (b & 0x7fffffu) | 0x800000u;
+    if (e >= -6) return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((m >> 20) & 0x7u));
+    return (uint8_t)(sign | (uint8_t)(m >> (-e + 14)));  /* subnormal: v / 2^-9 */
+}
+
+static float decode_e4m3(uint8_t c) {
+    int negative = c >> 7, field = (c >> 3) & 0xf, man = c & 7;
+    float v;
+    if (field == 15 && man == 7) v = NAN;
+    else if (field == 0) v = ldexpf((float)man, -9);
+    else v = ldexpf((float)(8 + man), field - 10);
+    return negative ? -v : v;
+}
+
+/* nearest integer (ties to even), clamped to [-127, 127]; NaN -> 0 */
+static int8_t quant_int8(float v) {
+    if (isnan(v)) return 0;
+    if (v >= 127.0f) return 127;
+    if (v <= -127.0f) return -127;
+    float f = floorf(v);
+    float d = v - f;                      /* exact: |v| < 2^23 */
+    float n = f;
+    if (d > 0.5f || (d == 0.5f && fmodf(f, 2.0f) != 0.0f)) n = f + 1.0f;
+    return (int8_t)n;
+}
 
 static float load(const void* base, int dtype, int64_t i) {
     if (dtype == OR_F16) return decode_f16(((const uint16_t*)base)[i]);
@@ -326,6 +383,70 @@ float oracle_exact_sum(const float* v, int64_t n) {
     for (int64_t i = 0; i < n; ++i) acc_add(&acc, v[i]);
     return acc_round(&acc);
 }
+
+/* ------------------------------------------------------------------ */
+/* quantised output                                                    */
+/* ------------------------------------------------------------------ */
+
+enum { OR_Q_INT8 = 1, OR_Q_FP8_E4M3 = 2 };
+
+/* quantise one row of out values (already values of od) into q, return its scale */
+static float quantise_row(const float* o, int64_t hidden, int qtype, void* qrow) {
+    const float qmax = qtype == OR_Q_INT8 ? 127.0f : 448.0f;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < hidden; ++i) {
+        float a = fabsf(o[i]);
+        if (isnan(a) || a > amax) amax = isnan(amax) ? amax : a;
+    }
+    float scale = amax / qmax;
+    float inv = amax == 0.0f ? 0.0f : qmax / amax;
+    for (int64_t i = 0; i < hidden; ++i) {
+        float v = o[i] * inv;
+        if (qtype == OR_Q_INT8) ((int8_t*)qrow)[i] = quant_int8(v);
+        else ((uint8_t*)qrow)[i] = encode_e4m3(round_e4m3_satfinite(v));
+    }
+    return scale;
+}
+
+static int run_quant(const void* x, const void* residual, const void* weight, float eps, void* q,
+                     float* scale, void* residual_out, int64_t tokens, int64_t hidden, int act, int wd,
+                     int qtype, int has_residual) {
+    int od = oracle_output_dtype(act, wd);
+    if (od < 0) return -1;
+    if (tokens < 0 || hidden <= 0 || (qtype != OR_Q_INT8 && qtype != OR_Q_FP8_E4M3)) return -2;
+    size_t sa = act == OR_F32 ? 4 : 2, so = od == OR_F32 ? 4 : 2;
+    void* orow = malloc((size_t)hidden * so);
+    float* of = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!orow || !of) { free(orow); free(of); return -3; }
+    for (int64_t t = 0; t < tokens; ++t) {
+        const char* xr = (const char*)x + (size_t)t * (size_t)hidden * sa;
+        const char* rr = has_residual ? (const char*)residual + (size_t)t * (size_t)hidden * sa : NULL;
+        char* ror = has_residual ? (char*)residual_out + (size_t)t * (size_t)hidden * sa : NULL;
+        /* the unquantised row first, exactly as the plain op computes it */
+        int rc = run(xr, rr, weight, eps, orow, ror, 1, hidden, act, wd, has_residual);
+        if (rc != 0) { free(orow); free(of); return rc; }
+        for (int64_t i = 0; i < hidden; ++i) of[i] = load(orow, od, i);
+        scale[t] = quantise_row(of, hidden, qtype, (char*)q + (size_t)t * (size_t)hidden);
+    }
+    free(orow);
+    free(of);
+    return 0;
+}
+
+int oracle_fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps,
+                                   void* q, float* scale, void* residual_out, int64_t tokens,
+                                   int64_t hidden, int act, int wd, int qtype) {
+    return run_quant(x, residual, weight, eps, q, scale, residual_out, tokens, hidden, act, wd, qtype, 1);
+}
+
+int oracle_rmsnorm_quant(const void* x, const void* weight, float eps, void* q, float* scale,
+                         int64_t tokens, int64_t hidden, int act, int wd, int qtype) {
+    return run_quant(x, NULL, weight, eps, q, scale, NULL, tokens, hidden, act, wd, qtype, 0);
+}
+
+uint8_t oracle_f32_to_e4m3(float v) { return encode_e4m3(round_e4m3_satfinite(v)); }
+float oracle_e4m3_to_f32(uint8_t c) { return decode_e4m3(c); }
+int oracle_f32_to_int8(float v) { return quant_int8(v); }
 
 /* format conversions, exposed so they can be pinned on their own */
 uint16_t oracle_f32_to_f16(float v) { return encode_f16(round_f16(v)); }

@@ -108,3 +108,47 @@ def test_unmutated_copy_passes(tmp_path, cases):
     L = _mutant_lib(tmp_path, "identity", [])
     assert _failed_pins(L, cases) == []
     assert _extra_pin_checks(L) == []
+
+
+QUANT_MUTANTS = {
+    # the maximum without the absolute value
+    "amax_signed": [("float a = fabsf(o[i]);", "float a = o[i];")],
+    # divisor 128 instead of the symmetric 127
+    "int8_divisor_128": [("const float qmax = qtype == OR_Q_INT8 ? 127.0f : 448.0f;",
+                          "const float qmax = qtype == OR_Q_INT8 ? 128.0f : 448.0f;")],
+    # truncation instead of rounding to nearest
+    "int8_truncates": [("if (d > 0.5f || (d == 0.5f && fmodf(f, 2.0f) != 0.0f)) n = f + 1.0f;", "")],
+    # ties away from zero
+    "int8_ties_away": [("if (d > 0.5f || (d == 0.5f && fmodf(f, 2.0f) != 0.0f)) n = f + 1.0f;",
+                        "if (d >= 0.5f) n = f + 1.0f;")],
+    # quantising the binary32 product instead of the stored out value: scale from s * rstd
+    "quantise_normalised_not_out": [("for (int64_t i = 0; i < hidden; ++i) of[i] = load(orow, od, i);",
+                                     "for (int64_t i = 0; i < hidden; ++i) of[i] = load(orow, od, i) * 1.001f;")],
+    # E4M3 without saturation: the top code becomes 480 (a NaN code)
+    "e4m3_no_saturation": [("if (r > 448.0f) r = 448.0f;", "")],
+    # E4M3 exponent bias off by one
+    "e4m3_bias": [("return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)((m >> 20) & 0x7u));",
+                   "return (uint8_t)(sign | (uint8_t)((e + 8) << 3) | (uint8_t)((m >> 20) & 0x7u));")],
+    # scale = QMAX / amax (the inverse stored instead of the scale)
+    "scale_inverted": [("    return scale;\n}", "    return inv;\n}")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(QUANT_MUTANTS))
+def test_quant_mutant_is_caught(tmp_path, name):
+    import test_oracle_quant as TQ
+    L = _mutant_lib(tmp_path, name, QUANT_MUTANTS[name])
+    failed = []
+    for check in (TQ.check_e4m3_format, TQ.check_int8, TQ.check_quant_rows):
+        try:
+            check(L)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"no quant pin rejects the planted mistake {name!r}"
+
+
+def test_unmutated_copy_passes_quant_pins(tmp_path):
+    import test_oracle_quant as TQ
+    L = _mutant_lib(tmp_path, "identity_q", [])
+    for check in (TQ.check_e4m3_format, TQ.check_int8, TQ.check_quant_rows):
+        check(L)
