@@ -114,6 +114,31 @@ int far_validate_strided(const void* x, int64_t x_row_stride, const void* residu
                          const void* residual_out, int64_t residual_out_row_stride, int64_t tokens, int64_t hidden,
                          int dtype, int has_residual);
 
+/*
+ * Quantised output: the same two operations followed by a per-token symmetric
+ * quantisation of out (the "Mixed-Precision Kernels" page, section "Quantised
+ * Kernels: INT8 and FP8 Inference": scale = max_abs / 127), applied to the
+ * values out would have, so the result equals normalising and quantising apart:
+ *   amax_t = max_i |out_ti|,  scale[t] = fl32(amax_t / QMAX),
+ *   q_ti = Q(fl32(out_ti * fl32(QMAX / amax_t)))   (q = 0 for an all-zero row)
+ *   FAR_Q_INT8:     QMAX = 127; nearest integer, ties to even, within +-127; NaN -> 0
+ *   FAR_Q_FP8_E4M3: QMAX = 448; nearest E4M3 value, ties to even, finite values
+ *                   saturated to +-448; NaN stays NaN
+ *   q              [tokens, hidden] one byte an element (int8, or E4M3 codes), device
+ *   scale          [tokens] binary32, device; dequantise as q * scale
+ *   residual_out   as for fused_add_rmsnorm
+ * q and scale may not overlap any other buffer.  FAR_ERR_DTYPE for an unknown qtype.
+ */
+#define FAR_Q_INT8 1
+#define FAR_Q_FP8_E4M3 2
+
+int fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps, void* q,
+                            float* scale, void* residual_out, int64_t tokens, int64_t hidden, int dtype, int qtype,
+                            void* stream);
+
+int rmsnorm_quant(const void* x, const void* weight, float eps, void* q, float* scale, int64_t tokens,
+                  int64_t hidden, int dtype, int qtype, void* stream);
+
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
 int far_output_dtype(int dtype);
 
@@ -209,6 +234,9 @@ int far_selftest_wait_timeout(uint32_t timeout_us, void* stream);
 int far_set_launch_override(int kind, int nch, int groups, int stages);
 int far_describe_launch(int64_t tokens, int64_t hidden, int dtype, int has_residual, int* out6);
 int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int sms, int* out8);
+/* the same for the quantised entry points (qtype FAR_Q_INT8 or FAR_Q_FP8_E4M3) */
+int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int qtype, int sms,
+                           int* out8);
 
 #ifdef __cplusplus
 }

@@ -45,6 +45,12 @@ lib.rmsnorm_strided.argtypes = [_vp, _i64, _vp, _f32, _vp, _i64, _i64, _i64, _in
 lib.rmsnorm_strided.restype = _int
 lib.far_validate_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _f32, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int]
 lib.far_validate_strided.restype = _int
+lib.fused_add_rmsnorm_quant.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp]
+lib.fused_add_rmsnorm_quant.restype = _int
+lib.rmsnorm_quant.argtypes = [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _int, _vp]
+lib.rmsnorm_quant.restype = _int
+lib.far_plan_quant_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
+lib.far_plan_quant_for_sms.restype = _int
 lib.far_output_dtype.argtypes = [_int]
 lib.far_output_dtype.restype = _int
 lib.far_status_string.argtypes = [_int]
@@ -219,4 +225,53 @@ def plan_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, re
     """The launch plan for a device with `sms` SMs (host logic only, no GPU needed)."""
     buf = (ctypes.c_int * 8)()
     _check(lib.far_plan_for_sms(tokens, hidden, dtypes(act, wd), int(residual), sms, ctypes.addressof(buf)))
+    return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))
+
+
+QUANT = {"int8": 1, "fp8": 2}
+
+
+def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor, eps: float,
+                            qtype: str = "int8", q: torch.Tensor | None = None, scale: torch.Tensor | None = None,
+                            residual_out: torch.Tensor | None = None, stream=None):
+    """(q, scale, residual_out): the fused op with a per-token quantised output.
+
+    q is int8 for "int8" and uint8 E4M3 codes for "fp8" (view as torch.float8_e4m3fn);
+    dequantise as q * scale[:, None].
+    """
+    if not (x.is_contiguous() and residual.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("x, residual and weight must be contiguous")
+    tokens, hidden = _rows(x)
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8 if qtype == "int8" else torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(tokens, dtype=torch.float32, device=x.device)
+    if residual_out is None:
+        residual_out = torch.empty_like(x)
+    _check(lib.fused_add_rmsnorm_quant(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(q), _ptr(scale),
+                                       _ptr(residual_out), tokens, hidden, dtypes(x.dtype, weight.dtype),
+                                       QUANT[qtype], _stream_handle(stream)))
+    return q, scale, residual_out
+
+
+def rmsnorm_quant(x: torch.Tensor, weight: torch.Tensor, eps: float, qtype: str = "int8",
+                  q: torch.Tensor | None = None, scale: torch.Tensor | None = None, stream=None):
+    """(q, scale): the no-residual variant with a per-token quantised output."""
+    if not (x.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("x and weight must be contiguous")
+    tokens, hidden = _rows(x)
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.int8 if qtype == "int8" else torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(tokens, dtype=torch.float32, device=x.device)
+    _check(lib.rmsnorm_quant(_ptr(x), _ptr(weight), eps, _ptr(q), _ptr(scale), tokens, hidden,
+                             dtypes(x.dtype, weight.dtype), QUANT[qtype], _stream_handle(stream)))
+    return q, scale
+
+
+def plan_quant_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool, qtype: str,
+                       sms: int) -> dict:
+    buf = (ctypes.c_int * 8)()
+    _check(lib.far_plan_quant_for_sms(tokens, hidden, dtypes(act, wd), int(residual), QUANT[qtype], sms,
+                                      ctypes.addressof(buf)))
     return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))

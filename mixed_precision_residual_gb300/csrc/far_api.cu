@@ -140,6 +140,9 @@ struct Call {
   int act, wd, od;
   bool residual;
   Strides st;  // elements
+  int quant = kQuantNone;  // quantised output: q [tokens, hidden] bytes and scale [tokens]
+  void* q = nullptr;
+  float* scale = nullptr;
 };
 
 int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
@@ -155,10 +158,10 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
   const int64_t max_stride = widest > wider ? widest : wider;
   if (tokens > (INT64_MAX / 8) / max_stride) return FAR_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps == INFINITY) return FAR_ERR_EPS;
-  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual, sd};
+  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual, sd, c.quant, c.q, c.scale};
   if (tokens == 0) return FAR_OK;
   if (!x || !w || !out || (residual && (!r || !res_out))) return FAR_ERR_NULL;
-  const int64_t sa = dsize(c.act), so = dsize(c.od);
+  const int64_t sa = dsize(c.act), so = c.quant ? 1 : dsize(c.od);  // a quantised output is one byte
   const Region X = region(x, tokens, hidden * sa, sd.x * sa);
   const Region O = region(out, tokens, hidden * so, sd.out * so);
   const Region W = region(w, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
@@ -169,6 +172,34 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
     if (bad_overlap(O, R) || regions_overlap(O, RO)) return FAR_ERR_ALIAS;
     if (bad_overlap(RO, X) || bad_overlap(RO, R) || regions_overlap(RO, W)) return FAR_ERR_ALIAS;
   }
+  return FAR_OK;
+}
+
+// the quantised entry points: q and scale replace out and must share no byte with anything
+int validate_quant(const void* x, const void* r, const void* w, float eps, void* q, float* scale, void* res_out,
+                   int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, Call& c) {
+  if (qtype != kQuantInt8 && qtype != kQuantFp8) return FAR_ERR_DTYPE;
+  c.quant = qtype;
+  c.q = q;
+  c.scale = scale;
+  // validate the rest with q standing in for out (the out checks then cover q's bytes too)
+  int st = validate(x, r, w, eps, q, res_out, tokens, hidden, dtype, residual, c);
+  if (st != FAR_OK || tokens == 0) return st;
+  if (!scale) return FAR_ERR_NULL;
+  const int64_t sa = dsize(c.act);
+  const Region Q = region(q, tokens, hidden, hidden);
+  const Region S = region(scale, 1, tokens * 4, tokens * 4);
+  const Region X = region(x, tokens, hidden * sa, hidden * sa);
+  const Region W = region(w, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
+  // q: one byte an element, never an exact alias of an input
+  if (regions_overlap(Q, X) || regions_overlap(S, X) || regions_overlap(S, Q) || regions_overlap(S, W))
+    return FAR_ERR_ALIAS;
+  if (residual) {
+    const Region R = region(r, tokens, hidden * sa, hidden * sa);
+    const Region RO = region(res_out, tokens, hidden * sa, hidden * sa);
+    if (regions_overlap(Q, R) || regions_overlap(S, R) || regions_overlap(S, RO)) return FAR_ERR_ALIAS;
+  }
+  c.out = nullptr;
   return FAR_OK;
 }
 
@@ -187,6 +218,9 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   p.hidden = (int32_t)c.hidden;
   p.hidden_f = (float)c.hidden;
   p.eps = c.eps;
+  p.q = c.q;
+  p.scale = c.scale;
+  L.quant = c.quant;
   p.status = status;
   p.timeout_ns = kWaitTimeoutNs;
   L.stream = stream;
@@ -201,8 +235,10 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   // the bulk-copy path needs every row start on a 16-byte boundary
   const bool rows_aligned = p.x_stride % 16 == 0 && p.out_stride % 16 == 0 &&
                             (!c.residual || (p.r_stride % 16 == 0 && p.res_stride % 16 == 0));
+  const void* out_ptr = c.quant ? c.q : c.out;
   bool staged = g_force_kind.load() != kGeneric && row_bytes % 16 == 0 && rows_aligned && aligned16(c.x) &&
-                aligned16(c.w) && aligned16(c.out) && (!c.residual || (aligned16(c.r) && aligned16(c.res_out)));
+                aligned16(c.w) && aligned16(out_ptr) && (!c.residual || (aligned16(c.r) && aligned16(c.res_out))) &&
+                (!c.quant || ((uintptr_t)c.scale & 3u) == 0);
   int nch = 0, G = 0, groups = 0, stages = 0;
   uint32_t stage_bytes = 0, w_bytes = (uint32_t)((c.hidden * sw + 15) / 16 * 16);
   size_t smem = 0;
@@ -219,7 +255,8 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     //  - with an fp32 output, the groups keep about 128 KB (fused) or 120 KB (variant) of
     //    rows in progress per SM, one slot each.
     const int64_t C = row_bytes / 16;
-    const bool packed = packed_rows(c.residual, c.act);
+    // packed x leaves room for 16 warps; a quantised output also keeps out in registers
+    const bool packed = packed_rows(c.residual, c.act) && !c.quant;
     int slots_per_group = c.residual ? 1 : 2;
     nch = 8;
     G = (int)((C + 255) / 256);
@@ -238,7 +275,21 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
       one_group = true;
-    } else if (c.od == FAR_F32) {
+    } else if (c.quant && C > 128) {
+      // quantised output (a second per-row reduction, the row maximum, lengthens each
+      // row's critical path, so several groups must overlap it): measured best were
+      // 4 chunks a thread for the fused op and 8 for the variant when that still gives
+      // 4+ warps a row, 3 groups at most, one ring slot per group (two for rows of 8+ warps)
+      const bool eight = !c.residual && (C + 255) / 256 >= 4;
+      nch = eight ? 8 : 4;
+      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+      if (G > kMaxConsumerWarps) {
+        nch = 8;
+        G = (int)((C + 255) / 256);
+      }
+      group_cap = 3;
+      slots_per_group = (c.residual && G >= 8) ? 2 : 1;
+    } else if (c.od == FAR_F32 && !c.quant) {
       // fp32 output (or fp32 activations): rows are long in bytes; keep about 128 KB
       // (fused) or 120 KB (variant) of rows in progress per SM, one ring slot per group
       const int64_t row_total = c.hidden * (c.residual ? (3 * sa + dsize(c.od)) : (sa + dsize(c.od)));
@@ -271,19 +322,19 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       groups = one_group ? 1 : max_consumer_warps(nch, packed) / G;
       if (groups > group_cap) groups = group_cap;
       if (groups > rows_per_sm) groups = (int)(rows_per_sm > 0 ? rows_per_sm : 1);
-      if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch, packed_rows(c.residual, c.act)))
+      if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch, packed))
         groups = g_force_groups.load();
       stage_bytes = (uint32_t)(((row_bytes + 127) / 128 * 128) * (c.residual ? 2 : 1));
       int want = one_group ? 4 : groups * slots_per_group;
       if (want < 2) want = 2;
       // as many ring slots as wanted and as fit in shared memory
       stages = want > 32 ? 32 : want;
-      while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes) > (size_t)kMaxDynamicSmem)
+      while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant) > (size_t)kMaxDynamicSmem)
         --stages;
       const int forced = g_force_stages.load();
       if (forced >= 2) {
         stages = forced;
-        while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes) > (size_t)kMaxDynamicSmem)
+        while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant) > (size_t)kMaxDynamicSmem)
           --stages;
       }
       if (groups > stages) groups = stages;
@@ -294,7 +345,7 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       if (stages < 2) {
         staged = false;
       } else {
-        smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes);
+        smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant);
       }
     }
   }
@@ -330,10 +381,18 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
   cudaError_t e;
-  switch (c.act) {
-    case FAR_F16: e = launch_act_f16(c.wd, c.residual, L); break;
-    case FAR_BF16: e = launch_act_bf16(c.wd, c.residual, L); break;
-    default: e = launch_act_f32(c.wd, c.residual, L); break;
+  if (c.quant) {
+    switch (c.act) {
+      case FAR_F16: e = launch_q_act_f16(c.wd, c.residual, L); break;
+      case FAR_BF16: e = launch_q_act_bf16(c.wd, c.residual, L); break;
+      default: e = launch_q_act_f32(c.wd, c.residual, L); break;
+    }
+  } else {
+    switch (c.act) {
+      case FAR_F16: e = launch_act_f16(c.wd, c.residual, L); break;
+      case FAR_BF16: e = launch_act_bf16(c.wd, c.residual, L); break;
+      default: e = launch_act_f32(c.wd, c.residual, L); break;
+    }
   }
   return e == cudaSuccess ? FAR_OK : cuda_fail(e);
 }
@@ -342,6 +401,17 @@ int run(const void* x, const void* r, const void* w, float eps, void* out, void*
         int64_t hidden, int dtype, bool residual, void* stream, const Strides* strides = nullptr) {
   Call c;
   int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c, strides);
+  if (st != FAR_OK || tokens == 0) return st;
+  DeviceState* dev = nullptr;
+  st = current_device(dev);
+  if (st != FAR_OK) return st;
+  return launch(c, *dev, static_cast<cudaStream_t>(stream));
+}
+
+int run_quant(const void* x, const void* r, const void* w, float eps, void* q, float* scale, void* res_out,
+              int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, void* stream) {
+  Call c;
+  int st = validate_quant(x, r, w, eps, q, scale, res_out, tokens, hidden, dtype, qtype, residual, c);
   if (st != FAR_OK || tokens == 0) return st;
   DeviceState* dev = nullptr;
   st = current_device(dev);
@@ -558,6 +628,17 @@ int rmsnorm_strided(const void* x, int64_t x_row_stride, const void* weight, flo
   return run(x, nullptr, weight, eps, out, nullptr, tokens, hidden, dtype, false, stream, &sd);
 }
 
+int fused_add_rmsnorm_quant(const void* x, const void* residual, const void* weight, float eps, void* q,
+                            float* scale, void* residual_out, int64_t tokens, int64_t hidden, int dtype, int qtype,
+                            void* stream) {
+  return run_quant(x, residual, weight, eps, q, scale, residual_out, tokens, hidden, dtype, qtype, true, stream);
+}
+
+int rmsnorm_quant(const void* x, const void* weight, float eps, void* q, float* scale, int64_t tokens,
+                  int64_t hidden, int dtype, int qtype, void* stream) {
+  return run_quant(x, nullptr, weight, eps, q, scale, nullptr, tokens, hidden, dtype, qtype, false, stream);
+}
+
 int far_output_dtype(int dtype) {
   int act, wd, od;
   int st = decode(dtype, act, wd, od);
@@ -669,6 +750,26 @@ int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual
   out8[5] = (int)L.grid.x;
   out8[6] = (int)L.block.x;
   out8[7] = (int)L.smem;
+  return FAR_OK;
+}
+
+int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int qtype, int sms,
+                           int* out8) {
+  if (sms < 1 || !out8) return FAR_ERR_SHAPE;
+  Call c;
+  const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
+  const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;
+  int st = validate_quant(base, has_residual ? base + span : nullptr, base + 2 * span, 1e-6f,
+                          const_cast<char*>(base + 3 * span), reinterpret_cast<float*>(const_cast<char*>(base + 5 * span)),
+                          has_residual ? const_cast<char*>(base + 4 * span) : nullptr, tokens, hidden, dtype, qtype,
+                          has_residual != 0, c);
+  if (st != FAR_OK) return st;
+  if (tokens == 0) return FAR_ERR_SHAPE;
+  Launch L;
+  st = plan(c, sms, nullptr, nullptr, L);
+  if (st != FAR_OK) return st;
+  int vals[8] = {L.kind, L.nch, L.p.warps_per_row, L.p.groups, L.p.stages, (int)L.grid.x, (int)L.block.x, (int)L.smem};
+  for (int i = 0; i < 8; ++i) out8[i] = vals[i];
   return FAR_OK;
 }
 

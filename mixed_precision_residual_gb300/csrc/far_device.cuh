@@ -8,6 +8,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "far.h"
@@ -237,6 +238,47 @@ __device__ __forceinline__ DW dw_warp_allreduce(DW a) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) a = dw_combine(a, dw_shfl_xor(a, off));
   return a;
+}
+
+// ---------------------------------------------------------------------------
+// quantised output: per-row maximum, scale, and the two byte formats
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_max_allreduce(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// running max of |v| over packed 16-bit pairs, NaN-propagating
+template <int DT> __device__ __forceinline__ uint32_t habs_max2(uint32_t m, uint32_t v);
+template <> __device__ __forceinline__ uint32_t habs_max2<FAR_F16>(uint32_t m, uint32_t v) {
+  __half2 r = __hmax2_nan(*reinterpret_cast<__half2*>(&m), __habs2(*reinterpret_cast<__half2*>(&v)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+template <> __device__ __forceinline__ uint32_t habs_max2<FAR_BF16>(uint32_t m, uint32_t v) {
+  __nv_bfloat162 r =
+      __hmax2_nan(*reinterpret_cast<__nv_bfloat162*>(&m), __habs2(*reinterpret_cast<__nv_bfloat162*>(&v)));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// four values scaled into quantised bytes, packed little-endian into one word
+//   Q = 1: int8, nearest integer with ties to even, saturated (the scaled values never
+//          pass +-127.5, so the saturation bound of -128 is never reached); NaN -> 0
+//   Q = 2: FP8 E4M3, nearest with ties to even, finite values saturated to +-448
+template <int Q> __device__ __forceinline__ uint32_t quantise4(float a, float b, float c, float d);
+template <> __device__ __forceinline__ uint32_t quantise4<1>(float a, float b, float c, float d) {
+  uint32_t qa, qb, qc, qd;
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(qa) : "f"(a));
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(qb) : "f"(b));
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(qc) : "f"(c));
+  asm("cvt.rni.sat.s8.f32 %0, %1;" : "=r"(qd) : "f"(d));
+  return __byte_perm(__byte_perm(qa, qb, 0x0040), __byte_perm(qc, qd, 0x0040), 0x5410);
+}
+template <> __device__ __forceinline__ uint32_t quantise4<2>(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return __byte_perm(lo, hi, 0x5410);
 }
 
 // rstd from the row's sum of squares, IEEE-rounded at every step:

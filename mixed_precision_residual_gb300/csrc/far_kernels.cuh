@@ -27,8 +27,9 @@
 
 namespace far {
 
-template <int ACT, int WD, bool RES, int NCH, bool EXACT>
-__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) staged_kernel(const Params p) {
+template <int ACT, int WD, bool RES, int NCH, bool EXACT, int Q = kQuantNone>
+__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q == kQuantNone), 1)
+    staged_kernel(const Params p) {
   constexpr int SA = dtype_size<ACT>::value;
   constexpr int SW = dtype_size<WD>::value;
   constexpr int OD = promote(ACT, WD);
@@ -39,12 +40,15 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
   // no residual and 16-bit x: s = x exactly, so x stays packed between the passes
   constexpr bool PACKED = packed_rows(RES, ACT);
 
+  constexpr int NRED = reduce_buffers(Q);  // cross-warp reduction buffers per group
+
   extern __shared__ __align__(128) unsigned char smem[];
   const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
-  // layout: full[stages] | empty[stages] | reduce[groups][2] | partials[groups][2][G] | w | ring
+  // layout: full[stages] | empty[stages] | reduce[groups][NRED] | partials[groups][NRED][G] | w | ring
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  float2* partials = reinterpret_cast<float2*>(smem + (size_t)(2 * stages + 2 * groups) * 8);
-  const size_t head = ((size_t)(2 * stages + 2 * groups) * 8 + (size_t)groups * 2 * G * 8 + 127) / 128 * 128;
+  float2* partials = reinterpret_cast<float2*>(smem + (size_t)(2 * stages + NRED * groups) * 8);
+  const size_t head =
+      ((size_t)(2 * stages + NRED * groups) * 8 + (size_t)groups * NRED * G * 8 + 127) / 128 * 128;
   unsigned char* wsm = smem + head;
   unsigned char* ring = wsm + (p.w_smem_bytes + 127) / 128 * 128;
   const uint32_t r_off = (p.row_bytes + 127u) & ~127u;  // residual row inside a slot
@@ -77,7 +81,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
       mbar_init(smem_addr(&bars[i]), 1);           // full: the producer's arrive + bytes
       mbar_init(smem_addr(&bars[stages + i]), G);  // empty: one arrive per consumer warp
     }
-    for (int i = 0; i < 2 * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
+    for (int i = 0; i < NRED * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
     fence_barrier_init();
     // the first `stages` rows need no free slot: start them now, under the weight load
     for (int64_t k = 0; k < first; ++k) issue(k, (int)k);
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
       // every warp of the group publishes its sum, then combines all G of them
       // with the same fixed butterfly over lanes 0..G8-1, so all agree bit for bit
       const int buf = (int)(it & 1u);
-      float2* part = partials + (size_t)(g * 2 + buf) * G;
-      const uint32_t rbar = smem_addr(&bars[2 * stages + g * 2 + buf]);
+      float2* part = partials + (size_t)(g * NRED + buf) * G;
+      const uint32_t rbar = smem_addr(&bars[2 * stages + g * NRED + buf]);
       if (lane == 0) {
         part[wg] = make_float2(tot.hi, tot.lo);
         mbar_arrive(rbar);
@@ -203,10 +207,15 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
     }
     const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
 
-    // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w)
+    // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w).
+    // With a quantised output the out values stay in registers (packed) until the
+    // row's largest |out| is known.
     const int64_t row = b + k * nb;
-    char* orow = static_cast<char*>(p.out) + row * p.out_stride;
+    char* orow = Q ? nullptr : static_cast<char*>(p.out) + row * p.out_stride;
     char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
+    uint32_t okeep[Q ? NCH : 1][Q ? OB / 4 : 1];
+    float amax = 0.f;
+    uint32_t amax2 = 0u;  // packed running max of |out| for a 16-bit out
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
@@ -237,11 +246,66 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT)), 1) st
           for (int e = 0; e < V; ++e) o[e] = __fmul_rn(o[e], wf[e]);
           narrow<OD, V>(o, ow);
         }
-        store_bytes<OB>(orow + (size_t)c * OB, ow);
+        if constexpr (Q) {
+          if constexpr (OD == FAR_F32) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) amax = max_nan(amax, fabsf(__uint_as_float(ow[e])));
+          } else {
+            // |out| of two 16-bit values at a time (max of 16-bit values is exact)
+#pragma unroll
+            for (int e = 0; e < OB / 4; ++e) amax2 = habs_max2<OD>(amax2, ow[e]);
+          }
+#pragma unroll
+          for (int e = 0; e < OB / 4; ++e) okeep[j][e] = ow[e];
+        } else {
+          store_bytes<OB>(orow + (size_t)c * OB, ow);
+        }
         if constexpr (RES) {
           uint32_t rw[4];
           narrow<ACT, V>(sj, rw);
           store_bytes<16>(rrow + (size_t)c * 16, rw);
+        }
+      }
+    }
+    if constexpr (Q) {
+      if constexpr (OD != FAR_F32) {
+        const float2 m2 = widen2<OD>(amax2);
+        amax = max_nan(m2.x, m2.y);
+      }
+      // the row's largest |out|: warp, then group (its own pair of buffers), all lanes agree
+      amax = warp_max_allreduce(amax);
+      if (G > 1) {
+        const int buf = 2 + (int)(it & 1u);
+        float2* part = partials + (size_t)(g * NRED + buf) * G;
+        const uint32_t rbar = smem_addr(&bars[2 * stages + g * NRED + buf]);
+        if (lane == 0) {
+          part[wg] = make_float2(amax, 0.f);
+          mbar_arrive(rbar);
+        }
+        if (!mbar_wait(rbar, (it >> 1) & 1u, p.timeout_ns, p.status)) return;
+        float m = part[lane < G ? lane : 0].x;
+        amax = warp_max_allreduce(m);
+      }
+      // scale = amax / QMAX; q = Q(out * (QMAX / amax)), 0 for an all-zero row
+      constexpr float QMAX = Q == kQuantInt8 ? 127.0f : 448.0f;
+      const float inv = amax == 0.f ? 0.f : __fdiv_rn(QMAX, amax);
+      if (wg == 0 && lane == 0) p.scale[row] = __fdiv_rn(amax, QMAX);
+      unsigned char* qrow = static_cast<unsigned char*>(p.q) + row * (int64_t)p.hidden;
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = (j * G + wg) * 32 + lane;
+        if (EXACT || c < C) {
+          float of[V];
+          widen<OD, V>(okeep[j], of);
+          uint32_t qw[V / 4];
+#pragma unroll
+          for (int e = 0; e < V / 4; ++e)
+            qw[e] = quantise4<Q>(__fmul_rn(of[4 * e], inv), __fmul_rn(of[4 * e + 1], inv),
+                                 __fmul_rn(of[4 * e + 2], inv), __fmul_rn(of[4 * e + 3], inv));
+          if constexpr (V == 8)
+            store_bytes<8>(qrow + (size_t)c * 8, qw);
+          else
+            asm volatile("st.global.b32 [%0], %1;" ::"l"(qrow + (size_t)c * 4), "r"(qw[0]) : "memory");
         }
       }
     }
@@ -271,11 +335,12 @@ template <int DT> __device__ __forceinline__ float round_one(float v) {
   else return v;
 }
 
-template <int ACT, int WD, bool RES>
+template <int ACT, int WD, bool RES, int Q = kQuantNone>
 __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p) {
   constexpr int OD = promote(ACT, WD);
   constexpr int NW = kGenericThreads / 32;
   __shared__ float2 part[NW];
+  __shared__ float mpart[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t H = p.hidden;
   for (int64_t row = blockIdx.x; row < p.tokens; row += gridDim.x) {
@@ -294,8 +359,9 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
     for (int i = 1; i < NW; ++i) tot = dw_combine(tot, DW{part[i].x, part[i].y});
     __syncthreads();  // `part` is reused by the next row
     const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
-    char* orow = static_cast<char*>(p.out) + row * p.out_stride;
+    char* orow = Q ? nullptr : static_cast<char*>(p.out) + row * p.out_stride;
     char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
+    float amax = 0.f;
     for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
       float s = load_elem<ACT>(xr, i);  // each element is read and written by the same thread
       if constexpr (RES) {
@@ -303,28 +369,50 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
         store_elem<ACT>(rrow, i, s);
       }
       const float n = round_one<WD>(__fmul_rn(s, rstd));
-      store_elem<OD>(orow, i, __fmul_rn(n, load_elem<WD>(p.w, i)));
+      const float o = __fmul_rn(n, load_elem<WD>(p.w, i));
+      if constexpr (Q) amax = max_nan(amax, fabsf(round_one<OD>(o)));
+      else store_elem<OD>(orow, i, o);
+    }
+    if constexpr (Q) {
+      // third pass: the row's largest |out|, then the quantised bytes (out recomputed)
+      amax = warp_max_allreduce(amax);
+      if (lane == 0) mpart[warp] = amax;
+      __syncthreads();
+      float m = mpart[0];
+      for (int i = 1; i < NW; ++i) m = max_nan(m, mpart[i]);
+      __syncthreads();  // `mpart` is reused by the next row
+      constexpr float QMAX = Q == kQuantInt8 ? 127.0f : 448.0f;
+      const float inv = m == 0.f ? 0.f : __fdiv_rn(QMAX, m);
+      if (threadIdx.x == 0) p.scale[row] = __fdiv_rn(m, QMAX);
+      unsigned char* qrow = static_cast<unsigned char*>(p.q) + row * H;
+      for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+        float s = load_elem<ACT>(xr, i);
+        if constexpr (RES) s = __fadd_rn(s, load_elem<ACT>(rr, i));
+        const float n = round_one<WD>(__fmul_rn(s, rstd));
+        const float v = __fmul_rn(round_one<OD>(__fmul_rn(n, load_elem<WD>(p.w, i))), inv);
+        qrow[i] = (unsigned char)(quantise4<Q>(v, 0.f, 0.f, 0.f) & 0xffu);
+      }
     }
   }
 }
 
 cudaError_t ensure_smem_attribute(const void* func, size_t bytes);
 
-template <int ACT, int WD, bool RES>
+template <int ACT, int WD, bool RES, int Q>
 cudaError_t launch_typed(const Launch& L) {
   void (*k)(Params) = nullptr;
   if (L.kind == kGeneric) {
-    k = generic_kernel<ACT, WD, RES>;
+    k = generic_kernel<ACT, WD, RES, Q>;
   } else {
     switch (L.nch * 2 + (L.exact ? 1 : 0)) {
-      case 2: k = staged_kernel<ACT, WD, RES, 1, false>; break;
-      case 3: k = staged_kernel<ACT, WD, RES, 1, true>; break;
-      case 4: k = staged_kernel<ACT, WD, RES, 2, false>; break;
-      case 5: k = staged_kernel<ACT, WD, RES, 2, true>; break;
-      case 8: k = staged_kernel<ACT, WD, RES, 4, false>; break;
-      case 9: k = staged_kernel<ACT, WD, RES, 4, true>; break;
-      case 16: k = staged_kernel<ACT, WD, RES, 8, false>; break;
-      case 17: k = staged_kernel<ACT, WD, RES, 8, true>; break;
+      case 2: k = staged_kernel<ACT, WD, RES, 1, false, Q>; break;
+      case 3: k = staged_kernel<ACT, WD, RES, 1, true, Q>; break;
+      case 4: k = staged_kernel<ACT, WD, RES, 2, false, Q>; break;
+      case 5: k = staged_kernel<ACT, WD, RES, 2, true, Q>; break;
+      case 8: k = staged_kernel<ACT, WD, RES, 4, false, Q>; break;
+      case 9: k = staged_kernel<ACT, WD, RES, 4, true, Q>; break;
+      case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q>; break;
+      case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q>; break;
       default: return cudaErrorInvalidValue;
     }
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);
@@ -334,9 +422,20 @@ cudaError_t launch_typed(const Launch& L) {
   return cudaGetLastError();
 }
 
+// the plain output
 template <int ACT, int WD>
 cudaError_t launch_res(bool residual, const Launch& L) {
-  return residual ? launch_typed<ACT, WD, true>(L) : launch_typed<ACT, WD, false>(L);
+  return residual ? launch_typed<ACT, WD, true, kQuantNone>(L) : launch_typed<ACT, WD, false, kQuantNone>(L);
+}
+
+// a quantised output (int8 or FP8 E4M3)
+template <int ACT, int WD>
+cudaError_t launch_quant(bool residual, const Launch& L) {
+  if (L.quant == kQuantInt8)
+    return residual ? launch_typed<ACT, WD, true, kQuantInt8>(L) : launch_typed<ACT, WD, false, kQuantInt8>(L);
+  if (L.quant == kQuantFp8)
+    return residual ? launch_typed<ACT, WD, true, kQuantFp8>(L) : launch_typed<ACT, WD, false, kQuantFp8>(L);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace far

@@ -45,15 +45,20 @@ struct Params {
   int64_t res_stride;    // ... of residual_out
   uint32_t w_smem_bytes; // hidden * sizeof(wd), rounded up to 16
   uint32_t stage_bytes;  // bytes of one ring slot (x row, then residual row), 128-aligned
+  void* q;               // quantised output [tokens, hidden] bytes (quantised variants)
+  float* scale;          // per-row scale [tokens] (quantised variants)
   unsigned int* status;  // device error word
   uint64_t timeout_ns;
 };
 
 enum Kind { kStaged = 0, kGeneric = 1 };
 
+enum QuantKind { kQuantNone = 0, kQuantInt8 = 1, kQuantFp8 = 2 };
+
 struct Launch {
   Params p;
   int kind;
+  int quant;   // QuantKind
   int nch;     // 16-byte chunks per thread (staged kernel): 1, 2, 4 or 8
   bool exact;  // chunks == nch * warps_per_row * 32: no per-chunk bounds test
   dim3 grid, block;
@@ -61,11 +66,16 @@ struct Launch {
   cudaStream_t stream;
 };
 
+// cross-warp reduction buffers per group: two (the sum of squares, double-buffered over
+// rows), four with a quantised output (the row maximum too)
+__host__ __device__ constexpr int reduce_buffers(int q) { return q ? 4 : 2; }
+
 // shared-memory bytes the staged kernel needs for a plan
 inline size_t staged_smem_bytes(int stages, int groups, int warps_per_row, uint32_t w_smem_bytes,
-                                uint32_t stage_bytes) {
-  size_t bars = (size_t)(2 * stages + 2 * groups) * 8;
-  size_t red = (size_t)groups * 2 * warps_per_row * 8;
+                                uint32_t stage_bytes, int q = 0) {
+  const int nred = reduce_buffers(q);
+  size_t bars = (size_t)(2 * stages + nred * groups) * 8;
+  size_t red = (size_t)groups * nred * warps_per_row * 8;
   size_t head = (bars + red + 127) / 128 * 128;
   return head + (w_smem_bytes + 127) / 128 * 128 + (size_t)stages * stage_bytes;
 }
@@ -74,6 +84,9 @@ inline size_t staged_smem_bytes(int stages, int groups, int warps_per_row, uint3
 cudaError_t launch_act_f16(int wd, bool residual, const Launch& L);
 cudaError_t launch_act_bf16(int wd, bool residual, const Launch& L);
 cudaError_t launch_act_f32(int wd, bool residual, const Launch& L);
+cudaError_t launch_q_act_f16(int wd, bool residual, const Launch& L);
+cudaError_t launch_q_act_bf16(int wd, bool residual, const Launch& L);
+cudaError_t launch_q_act_f32(int wd, bool residual, const Launch& L);
 
 // the argument checks and the device-buffer launch behind the public entry points (far_api.cu)
 int check_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,

@@ -190,3 +190,26 @@ def test_strided_validation(far):
     # the no-residual variant ignores the residual arguments
     assert strided(far, res=0, r=B, ro=B, **{k: v for k, v in ok.items() if k not in ("r", "ro")}) == 0
     assert strided(far, res=0, r=None, ro=None, x=B, xs=256, out=B + 100, os_=256) == 5
+
+
+def test_quantised_launch_plans_are_consistent(far):
+    """The planner's quantised plans: slots belong to one group, the CTA fits the 12-warp
+    (8 chunks) or 16-warp budget of the quantised kernels, shared memory fits, rows covered."""
+    T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
+    try:
+        for override in [(-1, 0, 0, 0), (0, 8, 3, 0), (0, 4, 2, 3), (0, 2, 0, 0), (0, 8, 8, 8)]:
+            far.set_launch_override(*override)
+            for (act, wd), hidden, tokens, res, qtype in itertools.product(
+                    [(T16, T16), (B16, B16), (B16, F32), (F32, F32)], [8, 1000, 4096, 5120, 8192, 16384],
+                    [1, 151, 4096, 65536], (True, False), ("int8", "fp8")):
+                p = far.plan_quant_for_sms(tokens, hidden, act, wd, res, qtype, 152)
+                if p["kind"] == 1:
+                    continue
+                G, g, st = p["warps_per_row"], p["groups"], p["stages"]
+                assert st >= 2 and st % g == 0, p
+                assert g * G <= (12 if p["nch"] == 8 else 16), p
+                assert p["threads"] == (1 + g * G) * 32 and p["smem"] <= 227 * 1024
+                chunks = hidden * (4 if act == F32 else 2) // 16
+                assert (G - 1) * 32 * p["nch"] < chunks <= G * 32 * p["nch"], p
+    finally:
+        far.set_launch_override()

@@ -1,0 +1,122 @@
+"""The quantised-output variants (per-token scale, int8 or FP8 E4M3) against the
+oracle, through the C ABI.  The gate: residual_out bit for bit; scale bit for bit
+(it is a function of the row maximum, exact whenever out matches); q equal
+wherever out matches the oracle, and within one quantisation step where out
+differs by its allowed one ULP (fewer than 1% of elements)."""
+import numpy as np
+import pytest
+import torch
+
+import far_gen
+import oracle
+from gpu_helpers import gate
+from oracle_pins import bits_equal
+
+pytestmark = pytest.mark.gpu
+PAIRS = [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "f32"), ("f32", "f32"), ("f32", "bf16"),
+         ("f32", "f16")]
+
+
+@pytest.fixture(scope="module")
+def far():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import mixed_precision_residual_gb300 as far
+
+    far.set_launch_override()
+    return far
+
+
+def _q_gate(q, scale, ref_q, ref_scale, where):
+    assert bits_equal(scale, ref_scale), f"{where}: scale differs"
+    a = q.numpy().astype(np.int64)
+    b = ref_q.numpy().astype(np.int64)
+    if q.dtype == torch.uint8:  # E4M3 codes: compare decoded values, NaN equal to NaN
+        av = q.view(torch.float8_e4m3fn).float().numpy()
+        bv = ref_q.view(torch.float8_e4m3fn).float().numpy()
+        same = (av == bv) | (np.isnan(av) & np.isnan(bv))
+        # one E4M3 step apart where out itself differs by one ULP
+        step_ok = np.abs(np.abs(a & 0x7F) - np.abs(b & 0x7F)) <= 1
+        assert (same | step_ok).all(), f"{where}: q differs by more than one E4M3 step"
+    else:
+        same = a == b
+        assert (np.abs(a - b) <= 1).all(), f"{where}: q differs by more than one int8 step"
+    frac = float((~same).mean())
+    assert frac < 0.01, f"{where}: {frac:.4%} of q differ"
+
+
+def run_quant(far, d, qtype, residual=True):
+    x, r, w = d["x"].cuda(), d["r"].cuda(), d["w"].cuda()
+    if residual:
+        q, scale, res = far.fused_add_rmsnorm_quant(x, r, w, d["eps"], qtype)
+    else:
+        q, scale = far.rmsnorm_quant(x, w, d["eps"], qtype)
+        res = None
+    assert far.device_status() == 0
+    return q.cpu(), scale.cpu(), None if res is None else res.cpu()
+
+
+def check_quant(far, d, where):
+    for qtype in ("int8", "fp8"):
+        q, scale, res = run_quant(far, d, qtype, True)
+        rq, rs, rres = oracle.fused_add_rmsnorm_quant(d["x"], d["r"], d["w"], d["eps"], d["act"], d["wd"], qtype)
+        assert bits_equal(res, rres), f"{where} {qtype}: residual_out differs"
+        _q_gate(q.view(torch.uint8) if qtype == "fp8" else q, scale, rq, rs, f"{where} {qtype} fused")
+        q, scale, _ = run_quant(far, d, qtype, False)
+        rq, rs = oracle.rmsnorm_quant(d["x"], d["w"], d["eps"], d["act"], d["wd"], qtype)
+        _q_gate(q.view(torch.uint8) if qtype == "fp8" else q, scale, rq, rs, f"{where} {qtype} rmsnorm")
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+def test_workloads(far, name):
+    check_quant(far, far_gen.make_inputs(name), name)
+
+
+@pytest.mark.parametrize("name", ["c4", "c5"])
+def test_workload_rows(far, name):
+    check_quant(far, far_gen.make_inputs(name, rows=600), name)
+
+
+@pytest.mark.parametrize("act,wd", PAIRS)
+@pytest.mark.parametrize("hidden", [1, 8, 100, 2048, 4096, 5120, 8192])
+def test_dtype_pairs(far, act, wd, hidden):
+    d = far_gen.custom_inputs(act, wd, 33, hidden, seed=hidden + 1, scale_lo=1e-3, scale_hi=30)
+    check_quant(far, d, f"{act}/{wd} H={hidden}")
+
+
+def test_generic_path_and_plans(far):
+    d = far_gen.custom_inputs("f16", "f16", 200, 8192, seed=9)
+    try:
+        for plan in [(1, 0, 0, 0), (0, 4, 1, 2), (0, 8, 1, 0), (0, 2, 0, 0)]:
+            far.set_launch_override(*plan)
+            check_quant(far, d, f"plan {plan}")
+    finally:
+        far.set_launch_override()
+
+
+def test_special_rows(far):
+    """All-zero rows (scale 0, q 0), rows with NaN (NaN scale) and infinity."""
+    d = far_gen.custom_inputs("bf16", "bf16", 8, 1024, seed=2)
+    x, r = d["x"].clone(), d["r"].clone()
+    x[0] = 0.0
+    r[0] = 0.0
+    x[1, 5] = float("nan")
+    x[2, 9] = float("inf")
+    check_quant(far, dict(d, x=x, r=r), "special rows")
+
+
+def test_quant_rejections(far):
+    x = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
+    w = torch.ones(64, dtype=torch.float16, device="cuda")
+    scale = torch.empty(4, dtype=torch.float32, device="cuda")
+    q = torch.empty((4, 64), dtype=torch.int8, device="cuda")
+    st = far.lib.fused_add_rmsnorm_quant(x.data_ptr(), x.data_ptr(), w.data_ptr(), 1e-6, q.data_ptr(),
+                                         scale.data_ptr(), x.data_ptr(), 4, 64, far.dtypes(x.dtype, w.dtype), 3,
+                                         torch.cuda.current_stream().cuda_stream)
+    assert st == 2  # unknown quantisation type
+    st = far.lib.rmsnorm_quant(x.data_ptr(), w.data_ptr(), 1e-6, x.data_ptr(), scale.data_ptr(), 4, 64,
+                               far.dtypes(x.dtype, w.dtype), 1, torch.cuda.current_stream().cuda_stream)
+    assert st == 5  # q over x
