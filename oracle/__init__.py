@@ -83,6 +83,14 @@ def bind(path: str) -> ctypes.CDLL:
     l.oracle_e4m3_to_f32.restype = f32
     l.oracle_f32_to_int8.argtypes = [f32]
     l.oracle_f32_to_int8.restype = i32
+    l.oracle_fused_add_layernorm.argtypes = [vp, vp, vp, vp, f32, vp, vp, i64, i64, i32, i32]
+    l.oracle_fused_add_layernorm.restype = i32
+    l.oracle_layernorm.argtypes = [vp, vp, vp, f32, vp, i64, i64, i32, i32]
+    l.oracle_layernorm.restype = i32
+    l.oracle_ln_row_stats.argtypes = [vp, vp, f32, i64, i64, i32, vp, vp]
+    l.oracle_ln_row_stats.restype = i32
+    l.oracle_exact_signed_sum.argtypes = [vp, i64]
+    l.oracle_exact_signed_sum.restype = f32
     return l
 
 
@@ -237,3 +245,67 @@ def rmsnorm_quant(x, weight, eps, act, wd, qtype, threads=None, L=None):
 
     _rows_parallel(work, T, threads or default_threads())
     return q, scale
+
+
+def fused_add_layernorm(x, residual, gamma, beta, eps, act, wd, threads=None, L=None):
+    """Oracle of fused residual-add + LayerNorm on CPU tensors: (out, residual_out)."""
+    L = L or lib()
+    od = output_dtype(act, wd, L)
+    if od is None:
+        raise ValueError(f"dtype pair ({act}, {wd}) is rejected by the dtype policy")
+    T, H = x.shape
+    x, residual, gamma, beta = x.contiguous(), residual.contiguous(), gamma.contiguous(), beta.contiguous()
+    out = torch.empty((T, H), dtype=TORCH_DTYPE[od])
+    res_out = torch.empty((T, H), dtype=TORCH_DTYPE[act])
+    sa, so = x.element_size(), out.element_size()
+
+    def work(t0, t1):
+        rc = L.oracle_fused_add_layernorm(x.data_ptr() + t0 * H * sa, residual.data_ptr() + t0 * H * sa,
+                                          gamma.data_ptr(), beta.data_ptr(), eps, out.data_ptr() + t0 * H * so,
+                                          res_out.data_ptr() + t0 * H * sa, t1 - t0, H, DTYPE_CODE[act],
+                                          DTYPE_CODE[wd])
+        if rc != 0:
+            raise RuntimeError(f"oracle_fused_add_layernorm returned {rc}")
+
+    _rows_parallel(work, T, threads or default_threads())
+    return out, res_out
+
+
+def layernorm(x, gamma, beta, eps, act, wd, threads=None, L=None):
+    """Oracle of LayerNorm without a residual on CPU tensors: out."""
+    L = L or lib()
+    od = output_dtype(act, wd, L)
+    if od is None:
+        raise ValueError(f"dtype pair ({act}, {wd}) is rejected by the dtype policy")
+    T, H = x.shape
+    x, gamma, beta = x.contiguous(), gamma.contiguous(), beta.contiguous()
+    out = torch.empty((T, H), dtype=TORCH_DTYPE[od])
+    sa, so = x.element_size(), out.element_size()
+
+    def work(t0, t1):
+        rc = L.oracle_layernorm(x.data_ptr() + t0 * H * sa, gamma.data_ptr(), beta.data_ptr(), eps,
+                                out.data_ptr() + t0 * H * so, t1 - t0, H, DTYPE_CODE[act], DTYPE_CODE[wd])
+        if rc != 0:
+            raise RuntimeError(f"oracle_layernorm returned {rc}")
+
+    _rows_parallel(work, T, threads or default_threads())
+    return out
+
+
+def ln_row_stats(x, residual, eps, act, L=None):
+    """Per-row (mean, rstd) of the fused LayerNorm as binary32 numpy arrays."""
+    L = L or lib()
+    T, H = x.shape
+    mean = np.empty(T, np.float32)
+    rstd = np.empty(T, np.float32)
+    rc = L.oracle_ln_row_stats(x.contiguous().data_ptr(),
+                               None if residual is None else residual.contiguous().data_ptr(), eps, T, H,
+                               DTYPE_CODE[act], mean.ctypes.data, rstd.ctypes.data)
+    if rc != 0:
+        raise RuntimeError(f"oracle_ln_row_stats returned {rc}")
+    return mean, rstd
+
+
+def exact_signed_sum(values, L=None):
+    v = np.ascontiguousarray(values, dtype=np.float32)
+    return np.float32((L or lib()).oracle_exact_signed_sum(v.ctypes.data, v.size))

@@ -52,6 +52,17 @@
  *                                              E4M3: nearest, ties to even, finite
  *                                              values saturated to +-448, NaN stays NaN
  *
+ * LayerNorm under the same contract (the "Mixed-Precision Kernels" page, section
+ * "Kernel-Level Mechanics: Cast Placement and Fusion": widen on load, mean and
+ * variance in binary32, narrow on store), taken in two passes over the row
+ * rather than the sketch's E[s^2] - mean^2:
+ *   mean  = fl32(RN32(sum_i s_i) / hidden)     correctly rounded exact signed sum
+ *   d_i   = fl32(s_i - mean)
+ *   var   = fl32(RN32(sum_i fl32(d_i * d_i)) / hidden)
+ *   rstd  = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   n_i   = RNE_wd(fl32(d_i * rstd))           cast to the weight dtype first
+ *   out_i = RNE_od(fl32(fl32(n_i * gamma_i) + beta_i))   gamma, beta in the weight dtype
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math (binary32
  * arithmetic must not be fused or reassociated).
  */
@@ -271,6 +282,47 @@ static float acc_round(const exact_acc* a) {
     return (float)mag;  /* exact, or infinity when the rounded sum reaches 2^128 */
 }
 
+/* exact signed sum: the magnitudes of positive and negative terms in two
+   accumulators, their difference taken exactly, then rounded once */
+typedef struct { exact_acc pos, neg; } signed_acc;
+
+static void sacc_init(signed_acc* a) { acc_init(&a->pos); acc_init(&a->neg); }
+
+static void sacc_add(signed_acc* a, float v) {
+    if (isnan(v)) { a->pos.has_nan = 1; return; }
+    if (isinf(v)) { if (v > 0) a->pos.has_pinf = 1; else a->neg.has_pinf = 1; return; }
+    if (v > 0) acc_add(&a->pos, v);
+    else if (v < 0) acc_add(&a->neg, -v);
+}
+
+/* -1, 0, +1 as the magnitude in A is below, equal to, above the one in B */
+static int acc_compare(const exact_acc* A, const exact_acc* B) {
+    for (int k = ACC_LIMBS - 1; k >= 0; --k) {
+        if (A->limb[k] != B->limb[k]) return A->limb[k] > B->limb[k] ? 1 : -1;
+    }
+    return 0;
+}
+
+static float sacc_round(const signed_acc* a) {
+    if (a->pos.has_nan || (a->pos.has_pinf && a->neg.has_pinf)) return NAN;
+    if (a->pos.has_pinf) return INFINITY;
+    if (a->neg.has_pinf) return -INFINITY;
+    int c = acc_compare(&a->pos, &a->neg);
+    if (c == 0) return 0.0f;  /* x + (-x) is +0 under round to nearest */
+    const exact_acc* big = c > 0 ? &a->pos : &a->neg;
+    const exact_acc* small = c > 0 ? &a->neg : &a->pos;
+    exact_acc diff;
+    acc_init(&diff);
+    uint64_t borrow = 0;
+    for (int k = 0; k < ACC_LIMBS; ++k) {
+        uint64_t t = (uint64_t)big->limb[k] - (uint64_t)small->limb[k] - borrow;
+        diff.limb[k] = (uint32_t)t;
+        borrow = (t >> 63) & 1u;  /* wrapped below zero */
+    }
+    float m = acc_round(&diff);
+    return c > 0 ? m : -m;
+}
+
 /* ------------------------------------------------------------------ */
 /* dtype policy                                                        */
 /* ------------------------------------------------------------------ */
@@ -382,6 +434,108 @@ float oracle_exact_sum(const float* v, int64_t n) {
     acc_init(&acc);
     for (int64_t i = 0; i < n; ++i) acc_add(&acc, v[i]);
     return acc_round(&acc);
+}
+
+/* ------------------------------------------------------------------ */
+/* LayerNorm                                                           */
+/* ------------------------------------------------------------------ */
+
+/* mean and rstd of one row of binary32 sums s[0..hidden); d[] receives s - mean */
+static float ln_row_stats(const float* s, float* d, int64_t hidden, float eps, float* mean_out) {
+    signed_acc sa;
+    sacc_init(&sa);
+    for (int64_t i = 0; i < hidden; ++i) sacc_add(&sa, s[i]);
+    float S1 = sacc_round(&sa);
+    float mean = S1 / (float)hidden;
+    exact_acc acc;
+    acc_init(&acc);
+    for (int64_t i = 0; i < hidden; ++i) {
+        d[i] = s[i] - mean;
+        float sq = d[i] * d[i];
+        acc_add(&acc, sq);
+    }
+    float S2 = acc_round(&acc);
+    float var = S2 / (float)hidden;
+    float tv = var + eps;
+    float root = sqrtf(tv);
+    if (mean_out) *mean_out = mean;
+    return 1.0f / root;
+}
+
+static int run_ln(const void* x, const void* residual, const void* gamma, const void* beta, float eps,
+                  void* out, void* residual_out, int64_t tokens, int64_t hidden, int act, int wd,
+                  int has_residual) {
+    int od = oracle_output_dtype(act, wd);
+    if (od < 0) return -1;
+    if (tokens < 0 || hidden <= 0) return -2;
+    size_t sa = act == OR_F32 ? 4 : 2, so = od == OR_F32 ? 4 : 2;
+    float* s = (float*)malloc((size_t)hidden * sizeof(float));
+    float* d = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!s || !d) { free(s); free(d); return -3; }
+    for (int64_t t = 0; t < tokens; ++t) {
+        const char* xr = (const char*)x + (size_t)t * (size_t)hidden * sa;
+        const char* rr = has_residual ? (const char*)residual + (size_t)t * (size_t)hidden * sa : NULL;
+        char* orow = (char*)out + (size_t)t * (size_t)hidden * so;
+        char* rorow = has_residual ? (char*)residual_out + (size_t)t * (size_t)hidden * sa : NULL;
+        for (int64_t i = 0; i < hidden; ++i) {
+            float xf = load(xr, act, i);
+            if (has_residual) {
+                s[i] = xf + load(rr, act, i);
+                store(rorow, act, i, round_to(act, s[i]));
+            } else {
+                s[i] = xf;
+            }
+        }
+        float rstd = ln_row_stats(s, d, hidden, eps, NULL);
+        for (int64_t i = 0; i < hidden; ++i) {
+            float a = d[i] * rstd;
+            float n = round_to(wd, a);                  /* weight dtype first */
+            float t1 = n * load(gamma, wd, i);          /* then the scale ... */
+            float u = t1 + load(beta, wd, i);           /* ... and the shift */
+            store(orow, od, i, round_to(od, u));
+        }
+    }
+    free(s);
+    free(d);
+    return 0;
+}
+
+int oracle_fused_add_layernorm(const void* x, const void* residual, const void* gamma, const void* beta,
+                               float eps, void* out, void* residual_out, int64_t tokens, int64_t hidden,
+                               int act, int wd) {
+    return run_ln(x, residual, gamma, beta, eps, out, residual_out, tokens, hidden, act, wd, 1);
+}
+
+int oracle_layernorm(const void* x, const void* gamma, const void* beta, float eps, void* out,
+                     int64_t tokens, int64_t hidden, int act, int wd) {
+    return run_ln(x, NULL, gamma, beta, eps, out, NULL, tokens, hidden, act, wd, 0);
+}
+
+/* per-row mean and rstd of the fused LayerNorm (for pins) */
+int oracle_ln_row_stats(const void* x, const void* residual, float eps, int64_t tokens, int64_t hidden,
+                        int act, float* mean, float* rstd) {
+    size_t sa = act == OR_F32 ? 4 : 2;
+    float* s = (float*)malloc((size_t)hidden * sizeof(float));
+    float* d = (float*)malloc((size_t)hidden * sizeof(float));
+    if (!s || !d) { free(s); free(d); return -3; }
+    for (int64_t t = 0; t < tokens; ++t) {
+        const char* xr = (const char*)x + (size_t)t * (size_t)hidden * sa;
+        const char* rr = residual ? (const char*)residual + (size_t)t * (size_t)hidden * sa : NULL;
+        for (int64_t i = 0; i < hidden; ++i)
+            s[i] = rr ? load(xr, act, i) + load(rr, act, i) : load(xr, act, i);
+        rstd[t] = ln_row_stats(s, d, hidden, eps, &mean[t]);
+    }
+    free(s);
+    free(d);
+    return 0;
+}
+
+/* correctly rounded binary32 sum of n binary32 values of any sign */
+float oracle_exact_signed_sum(const float* v, int64_t n) {
+    signed_acc a;
+    sacc_init(&a);
+    for (int64_t i = 0; i < n; ++i) sacc_add(&a, v[i]);
+    return sacc_round(&a);
 }
 
 /* ------------------------------------------------------------------ */

@@ -152,3 +152,43 @@ def test_unmutated_copy_passes_quant_pins(tmp_path):
     L = _mutant_lib(tmp_path, "identity_q", [])
     for check in (TQ.check_e4m3_format, TQ.check_int8, TQ.check_quant_rows):
         check(L)
+
+
+LN_MUTANTS = {
+    # the "Mixed-Precision Kernels" page's one-pass sketch: var = E[s^2] - mean^2
+    "one_pass_variance": [("        d[i] = s[i] - mean;\n        float sq = d[i] * d[i];",
+                           "        d[i] = s[i] - mean;\n        float sq = s[i] * s[i];"),
+                          ("    float var = S2 / (float)hidden;\n    float tv = var + eps;",
+                           "    float var = S2 / (float)hidden - mean * mean;\n    float tv = var + eps;")],
+    "mean_over_h_minus_1": [("    float mean = S1 / (float)hidden;",
+                             "    float mean = S1 / (float)(hidden > 1 ? hidden - 1 : 1);")],
+    "beta_before_cast": [("            float n = round_to(wd, a);                  /* weight dtype first */",
+                          "            float n = round_to(wd, a + load(beta, wd, i) / load(gamma, wd, i));")],
+    "no_weight_cast_ln": [("            float n = round_to(wd, a);                  /* weight dtype first */",
+                           "            float n = a;")],
+    "beta_dropped": [("            float u = t1 + load(beta, wd, i);           /* ... and the shift */",
+                      "            float u = t1;")],
+    "signed_sum_drops_negatives": [("    else if (v < 0) acc_add(&a->neg, -v);", "")],
+    "ln_eps_dropped": [("    float tv = var + eps;\n    float root = sqrtf(tv);\n    if (mean_out)",
+                        "    float tv = var;\n    float root = sqrtf(tv);\n    if (mean_out)")],
+}
+
+
+@pytest.mark.parametrize("name", sorted(LN_MUTANTS))
+def test_layernorm_mutant_is_caught(tmp_path, name):
+    import test_oracle_layernorm as TL
+    L = _mutant_lib(tmp_path, name, LN_MUTANTS[name])
+    failed = []
+    for check in (TL.check_signed_sum, TL.check_steps, TL.check_closed_forms, TL.check_fp64):
+        try:
+            check(L)
+        except AssertionError:
+            failed.append(check.__name__)
+    assert failed, f"no LayerNorm pin rejects the planted mistake {name!r}"
+
+
+def test_unmutated_copy_passes_layernorm_pins(tmp_path):
+    import test_oracle_layernorm as TL
+    L = _mutant_lib(tmp_path, "identity_ln", [])
+    for check in (TL.check_signed_sum, TL.check_steps, TL.check_closed_forms, TL.check_fp64):
+        check(L)
