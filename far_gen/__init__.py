@@ -29,7 +29,7 @@ _SRC = os.path.join(_HERE, "gen.c")
 _LIB = os.path.join(_HERE, "_build", "libfargen.so")
 
 # stream ids: one independent random sequence per role
-STREAM_X, STREAM_R, STREAM_W, STREAM_SCALE, STREAM_OUTLIER, STREAM_SIGN = 1, 2, 3, 4, 5, 6
+STREAM_X, STREAM_R, STREAM_W, STREAM_SCALE, STREAM_OUTLIER, STREAM_SIGN, STREAM_BETA = 1, 2, 3, 4, 5, 6, 7
 
 TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
@@ -231,3 +231,8 @@ def custom_inputs(act: str, wd: str, tokens: int, hidden: int, seed: int = 0,
     w = Workload(f"custom_{act}_{wd}_{tokens}x{hidden}", act, wd, tokens, hidden, eps,
                  "rowscale", scale_lo, scale_hi)
     return make_inputs(w, seed)
+
+
+def ln_beta(d: dict, seed: int = 0, sd: float = 0.1) -> torch.Tensor:
+    """A LayerNorm shift for inputs `d`: [hidden] in the weight dtype, N(0, sd^2)."""
+    return torch.from_numpy(normal(seed, STREAM_BETA, 0, d["hidden"], 0.0, sd)).to(d["w"].dtype)

@@ -139,6 +139,31 @@ int fused_add_rmsnorm_quant(const void* x, const void* residual, const void* wei
 int rmsnorm_quant(const void* x, const void* weight, float eps, void* q, float* scale, int64_t tokens,
                   int64_t hidden, int dtype, int qtype, void* stream);
 
+/*
+ * LayerNorm under the same rounding contract (the "Mixed-Precision Kernels" page,
+ * section "Kernel-Level Mechanics: Cast Placement and Fusion": activations widened
+ * on load, mean and variance accumulated in binary32, the result narrowed on store),
+ * with the variance taken about the mean in a second pass over s instead of the
+ * section's E[s^2] - mean^2 form:
+ *   s_i           = fl32(x_i + residual_i)          (s_i = x_i for layernorm)
+ *   residual_out_i = RNE_act(s_i)                    (fused_add_layernorm only)
+ *   mean          = fl32(RN32(sum_i s_i) / hidden)
+ *   d_i           = fl32(s_i - mean)
+ *   var           = fl32(RN32(sum_i fl32(d_i * d_i)) / hidden)
+ *   rstd          = fl32(1 / fl32(sqrt(fl32(var + eps))))
+ *   n_i           = RNE_wd(fl32(d_i * rstd))         (cast to the weight dtype first)
+ *   out_i         = RNE_od(fl32(fl32(n_i * gamma_i) + beta_i))
+ * gamma and beta are [hidden] device vectors in the weight dtype wd; everything else
+ * (dtype codes, layout, ownership, aliasing, asynchrony, statuses) is as for
+ * fused_add_rmsnorm / rmsnorm with gamma in the weight's place.  beta is read-only:
+ * FAR_ERR_NULL when it is NULL (tokens > 0), FAR_ERR_ALIAS when an output overlaps it.
+ */
+int fused_add_layernorm(const void* x, const void* residual, const void* gamma, const void* beta, float eps,
+                        void* out, void* residual_out, int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+int layernorm(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
+              int64_t hidden, int dtype, void* stream);
+
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
 int far_output_dtype(int dtype);
 
@@ -237,6 +262,10 @@ int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual
 /* the same for the quantised entry points (qtype FAR_Q_INT8 or FAR_Q_FP8_E4M3) */
 int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int qtype, int sms,
                            int* out8);
+/* the same for the LayerNorm entry points, with beta `beta_offset` bytes (0..15) past a
+   16-byte boundary (every other buffer aligned) */
+int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int beta_offset, int sms,
+                        int* out8);
 
 #ifdef __cplusplus
 }

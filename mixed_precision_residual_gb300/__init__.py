@@ -51,6 +51,12 @@ lib.rmsnorm_quant.argtypes = [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _int, 
 lib.rmsnorm_quant.restype = _int
 lib.far_plan_quant_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
 lib.far_plan_quant_for_sms.restype = _int
+lib.fused_add_layernorm.argtypes = [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _vp]
+lib.fused_add_layernorm.restype = _int
+lib.layernorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
+lib.layernorm.restype = _int
+lib.far_plan_ln_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
+lib.far_plan_ln_for_sms.restype = _int
 lib.far_output_dtype.argtypes = [_int]
 lib.far_output_dtype.restype = _int
 lib.far_status_string.argtypes = [_int]
@@ -274,4 +280,56 @@ def plan_quant_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dty
     buf = (ctypes.c_int * 8)()
     _check(lib.far_plan_quant_for_sms(tokens, hidden, dtypes(act, wd), int(residual), QUANT[qtype], sms,
                                       ctypes.addressof(buf)))
+    return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))
+
+
+def fused_add_layernorm(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor,
+                        eps: float, out: torch.Tensor | None = None, residual_out: torch.Tensor | None = None,
+                        stream=None):
+    """out, residual_out = LayerNorm(x + residual) * gamma + beta under the rounding contract.
+
+    x, residual: contiguous [..., hidden] CUDA tensors of one dtype; gamma, beta:
+    contiguous [hidden] in the weight dtype.  Outputs are allocated when not given.
+    """
+    if not all(t.is_contiguous() for t in (x, residual, gamma, beta)):
+        raise ValueError("x, residual, gamma and beta must be contiguous")
+    if residual.dtype != x.dtype or beta.dtype != gamma.dtype:
+        raise ValueError("x and residual, gamma and beta must share a dtype")
+    code = dtypes(x.dtype, gamma.dtype)
+    if out is None:
+        out = torch.empty(x.shape, dtype=output_dtype(x.dtype, gamma.dtype), device=x.device)
+    if residual_out is None:
+        residual_out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    tokens, hidden = _rows(x)
+    if (gamma.numel() != hidden or beta.numel() != hidden or residual.shape != x.shape or out.shape != x.shape
+            or residual_out.shape != x.shape or not out.is_contiguous() or not residual_out.is_contiguous()):
+        raise ValueError("shape mismatch or non-contiguous output")
+    _check(lib.fused_add_layernorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), eps, _ptr(out),
+                                   _ptr(residual_out), tokens, hidden, code, _stream_handle(stream)))
+    return out, residual_out
+
+
+def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
+              out: torch.Tensor | None = None, stream=None):
+    """out = LayerNorm(x) * gamma + beta under the rounding contract (no residual)."""
+    if not all(t.is_contiguous() for t in (x, gamma, beta)):
+        raise ValueError("x, gamma and beta must be contiguous")
+    if beta.dtype != gamma.dtype:
+        raise ValueError("gamma and beta must share a dtype")
+    code = dtypes(x.dtype, gamma.dtype)
+    if out is None:
+        out = torch.empty(x.shape, dtype=output_dtype(x.dtype, gamma.dtype), device=x.device)
+    tokens, hidden = _rows(x)
+    if gamma.numel() != hidden or beta.numel() != hidden or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("shape mismatch or non-contiguous output")
+    _check(lib.layernorm(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(out), tokens, hidden, code,
+                         _stream_handle(stream)))
+    return out
+
+
+def plan_ln_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool, sms: int,
+                    beta_offset: int = 0) -> dict:
+    buf = (ctypes.c_int * 8)()
+    _check(lib.far_plan_ln_for_sms(tokens, hidden, dtypes(act, wd), int(residual), beta_offset, sms,
+                                   ctypes.addressof(buf)))
     return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))

@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfar.so")
 SOURCES = ["far_api.cu", "far_inst_f16.cu", "far_inst_bf16.cu", "far_inst_f32.cu", "far_inst_q_f16.cu",
-           "far_inst_q_bf16.cu", "far_inst_q_f32.cu", "far_noalloc.cu"]
+           "far_inst_q_bf16.cu", "far_inst_q_f32.cu", "far_inst_ln_f16.cu", "far_inst_ln_bf16.cu",
+           "far_inst_ln_f32.cu", "far_noalloc.cu"]
 HEADERS = ["far_device.cuh", "far_kernels.cuh", "far_params.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",

@@ -1,4 +1,4 @@
-// C ABI of the fused residual-add + RMSNorm library (declared in include/far.h):
+// C ABI of the fused residual-add + RMSNorm (and LayerNorm) library (declared in include/far.h):
 // host-side validation, the launch plan, the device error word, the
 // host-buffer (end-to-end) pipeline and the bounded-wait self test.
 #include <cuda_runtime.h>
@@ -143,6 +143,8 @@ struct Call {
   int quant = kQuantNone;  // quantised output: q [tokens, hidden] bytes and scale [tokens]
   void* q = nullptr;
   float* scale = nullptr;
+  bool ln = false;            // LayerNorm: gamma in w, beta [hidden] in the weight dtype
+  const void* beta = nullptr;
 };
 
 int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
@@ -158,7 +160,8 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
   const int64_t max_stride = widest > wider ? widest : wider;
   if (tokens > (INT64_MAX / 8) / max_stride) return FAR_ERR_SHAPE;
   if (!(eps >= 0.0f) || eps == INFINITY) return FAR_ERR_EPS;
-  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual, sd, c.quant, c.q, c.scale};
+  c = Call{x, r, w, eps, out, res_out, tokens, hidden, c.act, c.wd, c.od, residual, sd, c.quant, c.q, c.scale,
+           c.ln, c.beta};
   if (tokens == 0) return FAR_OK;
   if (!x || !w || !out || (residual && (!r || !res_out))) return FAR_ERR_NULL;
   const int64_t sa = dsize(c.act), so = c.quant ? 1 : dsize(c.od);  // a quantised output is one byte
@@ -172,7 +175,21 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
     if (bad_overlap(O, R) || regions_overlap(O, RO)) return FAR_ERR_ALIAS;
     if (bad_overlap(RO, X) || bad_overlap(RO, R) || regions_overlap(RO, W)) return FAR_ERR_ALIAS;
   }
+  if (c.ln) {  // LayerNorm's shift: read-only, so no output may touch it
+    if (!c.beta) return FAR_ERR_NULL;
+    const Region B = region(c.beta, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
+    if (regions_overlap(O, B)) return FAR_ERR_ALIAS;
+    if (residual && regions_overlap(region(res_out, tokens, hidden * sa, sd.res * sa), B)) return FAR_ERR_ALIAS;
+  }
   return FAR_OK;
+}
+
+// the LayerNorm entry points: gamma in the weight's place, plus beta
+int validate_ln(const void* x, const void* r, const void* gamma, const void* beta, float eps, void* out,
+                void* res_out, int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c) {
+  c.ln = true;
+  c.beta = beta;
+  return validate(x, r, gamma, eps, out, res_out, tokens, hidden, dtype, residual, c);
 }
 
 // the quantised entry points: q and scale replace out and must share no byte with anything
@@ -212,6 +229,8 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   p.x = c.x;
   p.r = c.r;
   p.w = c.w;
+  p.beta = c.beta;
+  L.ln = c.ln;
   p.out = c.out;
   p.res_out = c.res_out;
   p.tokens = c.tokens;
@@ -237,10 +256,12 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
                             (!c.residual || (p.r_stride % 16 == 0 && p.res_stride % 16 == 0));
   const void* out_ptr = c.quant ? c.q : c.out;
   bool staged = g_force_kind.load() != kGeneric && row_bytes % 16 == 0 && rows_aligned && aligned16(c.x) &&
-                aligned16(c.w) && aligned16(out_ptr) && (!c.residual || (aligned16(c.r) && aligned16(c.res_out))) &&
+                aligned16(c.w) && (!c.ln || aligned16(c.beta)) && aligned16(out_ptr) &&
+                (!c.residual || (aligned16(c.r) && aligned16(c.res_out))) &&
                 (!c.quant || ((uintptr_t)c.scale & 3u) == 0);
   int nch = 0, G = 0, groups = 0, stages = 0;
   uint32_t stage_bytes = 0, w_bytes = (uint32_t)((c.hidden * sw + 15) / 16 * 16);
+  if (c.ln) w_bytes *= 2;  // gamma, then beta at the next 16-byte boundary
   size_t smem = 0;
   if (staged) {
     // Launch table (measured on GB300 over nch x groups x slots, L2 flushed between launches):
@@ -255,8 +276,9 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     //  - with an fp32 output, the groups keep about 128 KB (fused) or 120 KB (variant) of
     //    rows in progress per SM, one slot each.
     const int64_t C = row_bytes / 16;
-    // packed x leaves room for 16 warps; a quantised output also keeps out in registers
-    const bool packed = packed_rows(c.residual, c.act) && !c.quant;
+    // packed x leaves room for 16 warps; a quantised output also keeps out in registers,
+    // and LayerNorm keeps the binary32 deviations s - mean
+    const bool packed = packed_rows(c.residual, c.act) && !c.quant && !c.ln;
     int slots_per_group = c.residual ? 1 : 2;
     nch = 8;
     G = (int)((C + 255) / 256);
@@ -275,6 +297,19 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
       one_group = true;
+    } else if (c.ln && C > 128) {
+      // LayerNorm (two reductions a row, the mean's then the squared deviations', and
+      // more arithmetic an element than RMSNorm): measured best were 8 chunks a thread
+      // and as many groups as 12 warps hold, one ring slot each, but only 2 groups for
+      // fused rows of 4+ warps (3 with an fp32 output of 16-bit activations), 5 for
+      // shorter fused rows (10 for one-warp rows), and 5 for the variant with an fp32
+      // output of 16-bit activations
+      nch = 8;
+      G = (int)((C + 255) / 256);
+      const bool wide_out = c.od == FAR_F32 && c.act != FAR_F32;
+      if (c.residual) group_cap = G >= 4 ? (wide_out ? 3 : 2) : (G == 1 ? 10 : 5);
+      else group_cap = wide_out ? 5 : kMaxConsumerWarps;
+      slots_per_group = 1;
     } else if (c.quant && C > 128) {
       // quantised output (a second per-row reduction, the row maximum, lengthens each
       // row's critical path, so several groups must overlap it): measured best were
@@ -329,12 +364,12 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       if (want < 2) want = 2;
       // as many ring slots as wanted and as fit in shared memory
       stages = want > 32 ? 32 : want;
-      while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant) > (size_t)kMaxDynamicSmem)
+      while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant, c.ln) > (size_t)kMaxDynamicSmem)
         --stages;
       const int forced = g_force_stages.load();
       if (forced >= 2) {
         stages = forced;
-        while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant) > (size_t)kMaxDynamicSmem)
+        while (stages >= 2 && staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant, c.ln) > (size_t)kMaxDynamicSmem)
           --stages;
       }
       if (groups > stages) groups = stages;
@@ -345,7 +380,7 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       if (stages < 2) {
         staged = false;
       } else {
-        smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant);
+        smem = staged_smem_bytes(stages, groups, G, w_bytes, stage_bytes, c.quant, c.ln);
       }
     }
   }
@@ -381,7 +416,13 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
   cudaError_t e;
-  if (c.quant) {
+  if (c.ln) {
+    switch (c.act) {
+      case FAR_F16: e = launch_ln_act_f16(c.wd, c.residual, L); break;
+      case FAR_BF16: e = launch_ln_act_bf16(c.wd, c.residual, L); break;
+      default: e = launch_ln_act_f32(c.wd, c.residual, L); break;
+    }
+  } else if (c.quant) {
     switch (c.act) {
       case FAR_F16: e = launch_q_act_f16(c.wd, c.residual, L); break;
       case FAR_BF16: e = launch_q_act_bf16(c.wd, c.residual, L); break;
@@ -412,6 +453,17 @@ int run_quant(const void* x, const void* r, const void* w, float eps, void* q, f
               int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, void* stream) {
   Call c;
   int st = validate_quant(x, r, w, eps, q, scale, res_out, tokens, hidden, dtype, qtype, residual, c);
+  if (st != FAR_OK || tokens == 0) return st;
+  DeviceState* dev = nullptr;
+  st = current_device(dev);
+  if (st != FAR_OK) return st;
+  return launch(c, *dev, static_cast<cudaStream_t>(stream));
+}
+
+int run_ln(const void* x, const void* r, const void* gamma, const void* beta, float eps, void* out, void* res_out,
+           int64_t tokens, int64_t hidden, int dtype, bool residual, void* stream) {
+  Call c;
+  int st = validate_ln(x, r, gamma, beta, eps, out, res_out, tokens, hidden, dtype, residual, c);
   if (st != FAR_OK || tokens == 0) return st;
   DeviceState* dev = nullptr;
   st = current_device(dev);
@@ -639,6 +691,16 @@ int rmsnorm_quant(const void* x, const void* weight, float eps, void* q, float* 
   return run_quant(x, nullptr, weight, eps, q, scale, nullptr, tokens, hidden, dtype, qtype, false, stream);
 }
 
+int fused_add_layernorm(const void* x, const void* residual, const void* gamma, const void* beta, float eps,
+                        void* out, void* residual_out, int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  return run_ln(x, residual, gamma, beta, eps, out, residual_out, tokens, hidden, dtype, true, stream);
+}
+
+int layernorm(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
+              int64_t hidden, int dtype, void* stream) {
+  return run_ln(x, nullptr, gamma, beta, eps, out, nullptr, tokens, hidden, dtype, false, stream);
+}
+
 int far_output_dtype(int dtype) {
   int act, wd, od;
   int st = decode(dtype, act, wd, od);
@@ -763,6 +825,25 @@ int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_re
                           const_cast<char*>(base + 3 * span), reinterpret_cast<float*>(const_cast<char*>(base + 5 * span)),
                           has_residual ? const_cast<char*>(base + 4 * span) : nullptr, tokens, hidden, dtype, qtype,
                           has_residual != 0, c);
+  if (st != FAR_OK) return st;
+  if (tokens == 0) return FAR_ERR_SHAPE;
+  Launch L;
+  st = plan(c, sms, nullptr, nullptr, L);
+  if (st != FAR_OK) return st;
+  int vals[8] = {L.kind, L.nch, L.p.warps_per_row, L.p.groups, L.p.stages, (int)L.grid.x, (int)L.block.x, (int)L.smem};
+  for (int i = 0; i < 8; ++i) out8[i] = vals[i];
+  return FAR_OK;
+}
+
+int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int beta_offset, int sms,
+                        int* out8) {
+  if (sms < 1 || !out8 || beta_offset < 0 || beta_offset > 15) return FAR_ERR_SHAPE;
+  Call c;
+  const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
+  const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;
+  int st = validate_ln(base, has_residual ? base + span : nullptr, base + 2 * span, base + 5 * span + beta_offset, 1e-6f,
+                       const_cast<char*>(base + 3 * span), has_residual ? const_cast<char*>(base + 4 * span) : nullptr,
+                       tokens, hidden, dtype, has_residual != 0, c);
   if (st != FAR_OK) return st;
   if (tokens == 0) return FAR_ERR_SHAPE;
   Launch L;

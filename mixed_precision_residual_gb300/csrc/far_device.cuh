@@ -142,6 +142,65 @@ template <> __device__ __forceinline__ float2 square2_mixed<FAR_BF16>(uint32_t x
   return make_float2(q0, q1);
 }
 
+// LayerNorm's affine step on two lanes, fl32(fl32(n * g) + b), for n, g and b of one
+// 16-bit dtype packed in pairs: the mixed fma with a -0 addend rounds the exact product
+// once (so it is fl32(n * g), underflow and overflow included), and the mixed add widens
+// b exactly and rounds the sum once.
+template <int DT> __device__ __forceinline__ float2 affine2_mixed(uint32_t n2, uint32_t g2, uint32_t b2);
+template <> __device__ __forceinline__ float2 affine2_mixed<FAR_F16>(uint32_t n2, uint32_t g2, uint32_t b2) {
+  float o0, o1;
+  asm("{\n\t.reg .b16 n0, n1, g0, g1, b0, b1;\n\t.reg .f32 t0, t1;\n\t"
+      "mov.b32 {n0, n1}, %2;\n\tmov.b32 {g0, g1}, %3;\n\tmov.b32 {b0, b1}, %4;\n\t"
+      "fma.rn.f32.f16 t0, n0, g0, 0f80000000;\n\tfma.rn.f32.f16 t1, n1, g1, 0f80000000;\n\t"
+      "add.rn.f32.f16 %0, b0, t0;\n\tadd.rn.f32.f16 %1, b1, t1;\n\t}"
+      : "=f"(o0), "=f"(o1) : "r"(n2), "r"(g2), "r"(b2));
+  return make_float2(o0, o1);
+}
+template <> __device__ __forceinline__ float2 affine2_mixed<FAR_BF16>(uint32_t n2, uint32_t g2, uint32_t b2) {
+  float o0, o1;
+  asm("{\n\t.reg .b16 n0, n1, g0, g1, b0, b1;\n\t.reg .f32 t0, t1;\n\t"
+      "mov.b32 {n0, n1}, %2;\n\tmov.b32 {g0, g1}, %3;\n\tmov.b32 {b0, b1}, %4;\n\t"
+      "fma.rn.f32.bf16 t0, n0, g0, 0f80000000;\n\tfma.rn.f32.bf16 t1, n1, g1, 0f80000000;\n\t"
+      "add.rn.f32.bf16 %0, b0, t0;\n\tadd.rn.f32.bf16 %1, b1, t1;\n\t}"
+      : "=f"(o0), "=f"(o1) : "r"(n2), "r"(g2), "r"(b2));
+  return make_float2(o0, o1);
+}
+
+// ---------------------------------------------------------------------------
+// packed binary32 pairs (add / sub / mul .f32x2): each half rounds exactly as the
+// scalar instruction does (to nearest even, subnormals kept), two lanes an issue.
+// Unlike the scalar forms with an explicit rounding mode, a packed multiply (or a
+// packed fma with a -0 addend) whose result feeds a packed add is fused into one
+// multiply-add by the compiler, --fmad=false notwithstanding (measured: the outputs
+// then equal the single-rounding result).  So a product that a packed add consumes
+// is always formed by the scalar mul.rn, which is never fused.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpk(uint64_t v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return make_float2(a, b);
+}
+__device__ __forceinline__ uint64_t add_x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // vector memory access of N bytes (N = 8, 16 or 32), N-aligned
 template <int N> __device__ __forceinline__ void load_bytes(const void* p, uint32_t* w) {
   if constexpr (N == 8) {
@@ -230,6 +289,29 @@ __device__ __forceinline__ float dw_value(DW a) {
   return isfinite(a.hi) ? __fadd_rn(a.hi, a.lo) : a.hi;
 }
 
+// TwoSum (Knuth): s + e == a + b exactly, for any signs and any order of a and b
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+}
+
+// acc += v for a binary32 v of any sign (the LayerNorm mean's sum)
+__device__ __forceinline__ void dw_add_signed(DW& acc, float v) {
+  float s, e;
+  two_sum(acc.hi, v, s, e);
+  acc.hi = s;
+  acc.lo = __fadd_rn(acc.lo, e);
+}
+
+// a + b for signed double words; commutative bit for bit (the TwoSum error is exact)
+__device__ __forceinline__ DW dw_combine_signed(DW a, DW b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  return DW{s, __fadd_rn(__fadd_rn(a.lo, b.lo), e)};
+}
+
 __device__ __forceinline__ DW dw_shfl_xor(DW a, int off) {
   return DW{__shfl_xor_sync(0xffffffffu, a.hi, off), __shfl_xor_sync(0xffffffffu, a.lo, off)};
 }
@@ -237,6 +319,32 @@ __device__ __forceinline__ DW dw_shfl_xor(DW a, int off) {
 __device__ __forceinline__ DW dw_warp_allreduce(DW a) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) a = dw_combine(a, dw_shfl_xor(a, off));
+  return a;
+}
+
+// Two independent double-word chains in the two halves of packed pairs: TwoSum in each
+// half (any signs, any order), so a pair of values costs seven packed instructions.
+struct DW2 {
+  uint64_t hi, lo;
+};
+__device__ __forceinline__ void dw2_add(DW2& acc, uint64_t v) {
+  const uint64_t s = add_x2(acc.hi, v);
+  const uint64_t bv = sub_x2(s, acc.hi);
+  const uint64_t av = sub_x2(s, bv);
+  const uint64_t e = add_x2(sub_x2(acc.hi, av), sub_x2(v, bv));
+  acc.hi = s;
+  acc.lo = add_x2(acc.lo, e);
+}
+// the two chains of a DW2 folded into one double word
+__device__ __forceinline__ DW dw2_fold(DW2 a) {
+  const float2 h = unpk(a.hi), l = unpk(a.lo);
+  return dw_combine_signed(DW{h.x, l.x}, DW{h.y, l.y});
+}
+
+// the same butterfly for sums of either sign (TwoSum in place of the ordered Fast2Sum)
+__device__ __forceinline__ DW dw_warp_allreduce_signed(DW a) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) a = dw_combine_signed(a, dw_shfl_xor(a, off));
   return a;
 }
 

@@ -1,0 +1,15 @@
+// Instantiations and launcher of the LayerNorm kernels for activations in f32.
+#include "far_kernels.cuh"
+
+namespace far {
+
+cudaError_t launch_ln_act_f32(int wd, bool residual, const Launch& L) {
+  switch (wd) {
+    case FAR_F16: return launch_ln<FAR_F32, FAR_F16>(residual, L);
+    case FAR_BF16: return launch_ln<FAR_F32, FAR_BF16>(residual, L);
+    case FAR_F32: return launch_ln<FAR_F32, FAR_F32>(residual, L);
+    default: return cudaErrorInvalidValue;  // the pair is rejected before any launch
+  }
+}
+
+}  // namespace far

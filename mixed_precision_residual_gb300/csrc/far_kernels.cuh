@@ -1,4 +1,5 @@
-// Kernels for fused residual-add + RMSNorm and its no-residual variant.
+// Kernels for fused residual-add + RMSNorm and its no-residual variant (and, under
+// the same rounding contract, fused residual-add + LayerNorm and its variant).
 //
 // staged_kernel -- the hot path.  Persistent (one CTA per SM), warp-specialised:
 //   warp 0, lane 0 (producer) bulk-copies each row of x and of the residual into
@@ -27,8 +28,31 @@
 
 namespace far {
 
-template <int ACT, int WD, bool RES, int NCH, bool EXACT, int Q = kQuantNone>
-__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q == kQuantNone), 1)
+// Reduce a double word across the G warps of a group: every warp publishes its
+// value in buffer `buf`, then all combine the G values with the same butterfly over
+// lanes 0..G8-1, so every lane of every warp ends with the same bits.  False when
+// the bounded wait ran out (the caller then stops).
+template <typename Combine>
+__device__ __forceinline__ bool group_reduce(DW& v, float2* partials, uint64_t* bars, int red_base, int g,
+                                             int nred, int buf, int G, int G8, int wg, int lane, uint32_t use,
+                                             const Params& p, Combine combine) {
+  float2* part = partials + (size_t)(g * nred + buf) * G;
+  const uint32_t rbar = smem_addr(&bars[red_base + g * nred + buf]);
+  if (lane == 0) {
+    part[wg] = make_float2(v.hi, v.lo);
+    mbar_arrive(rbar);
+  }
+  if (!mbar_wait(rbar, (use >> 1) & 1u, p.timeout_ns, p.status)) return false;
+  const int src = lane & (G8 - 1);
+  const float2 mine = src < G ? part[src] : make_float2(0.f, 0.f);
+  DW t{mine.x, mine.y};
+  for (int off = G8 >> 1; off > 0; off >>= 1) t = combine(t, dw_shfl_xor(t, off));
+  v = t;
+  return true;
+}
+
+template <int ACT, int WD, bool RES, int NCH, bool EXACT, int Q = kQuantNone, bool LN = false>
+__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q == kQuantNone && !LN), 1)
     staged_kernel(const Params p) {
   constexpr int SA = dtype_size<ACT>::value;
   constexpr int SW = dtype_size<WD>::value;
@@ -38,9 +62,10 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
   constexpr int WB = V * SW;   // weight bytes per chunk: 8, 16 or 32
   constexpr int OB = V * SO;   // output bytes per chunk: 16 or 32
   // no residual and 16-bit x: s = x exactly, so x stays packed between the passes
-  constexpr bool PACKED = packed_rows(RES, ACT);
+  // (LayerNorm needs the binary32 deviations s - mean instead)
+  constexpr bool PACKED = packed_rows(RES, ACT) && !LN;
 
-  constexpr int NRED = reduce_buffers(Q);  // cross-warp reduction buffers per group
+  constexpr int NRED = reduce_buffers(Q, LN);  // cross-warp reduction buffers per group
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
@@ -86,14 +111,20 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
     // the first `stages` rows need no free slot: start them now, under the weight load
     for (int64_t k = 0; k < first; ++k) issue(k, (int)k);
   }
-  {  // the weight row, once per CTA (16-byte aligned; hidden * SW is even)
+  // LayerNorm's shift row sits right after the scale row in shared memory
+  unsigned char* bsm = wsm + (size_t)((p.hidden * SW + 15) / 16 * 16);
+  {  // the weight row (and LayerNorm's shift row), once per CTA (16-byte aligned; hidden * SW is even)
     const int nbytes = p.hidden * SW;
     const int n16 = nbytes >> 4;
-    const uint4* src = reinterpret_cast<const uint4*>(p.w);
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(wsm)[i] = src[i];
-    const uint16_t* src2 = reinterpret_cast<const uint16_t*>(p.w);
-    for (int i = (n16 << 3) + threadIdx.x; i < (nbytes >> 1); i += blockDim.x)
-      reinterpret_cast<uint16_t*>(wsm)[i] = src2[i];
+    for (int k = 0; k < (LN ? 2 : 1); ++k) {
+      const void* srcp = k == 0 ? p.w : p.beta;
+      unsigned char* dstp = k == 0 ? wsm : bsm;
+      const uint4* src = reinterpret_cast<const uint4*>(srcp);
+      for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4*>(dstp)[i] = src[i];
+      const uint16_t* src2 = reinterpret_cast<const uint16_t*>(srcp);
+      for (int i = (n16 << 3) + threadIdx.x; i < (nbytes >> 1); i += blockDim.x)
+        reinterpret_cast<uint16_t*>(dstp)[i] = src2[i];
+    }
   }
   __syncthreads();
 
@@ -136,6 +167,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
     float s[PACKED ? 1 : NCH][PACKED ? 1 : V];
     uint32_t xk[PACKED ? NCH : 1][PACKED ? V / 2 : 1];  // the packed x of the no-residual variant
     DW acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // four independent chains
+    DW2 accp[2] = {{0ull, 0ull}, {0ull, 0ull}};  // LayerNorm: four chains in packed pairs
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
       const int c = (j * G + wg) * 32 + lane;
@@ -172,8 +204,13 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
         } else {
           widen<ACT, V>(xw, s[j]);
         }
+        if constexpr (LN) {
 #pragma unroll
-        for (int e = 0; e < V; ++e) dw_add(acc[e & 3], __fmul_rn(s[j][e], s[j][e]));
+          for (int e = 0; e < V / 2; ++e) dw2_add(accp[e & 1], pk(s[j][2 * e], s[j][2 * e + 1]));  // for the mean
+        } else {
+#pragma unroll
+          for (int e = 0; e < V; ++e) dw_add(acc[e & 3], __fmul_rn(s[j][e], s[j][e]));
+        }
       } else {
 #pragma unroll
         for (int e = 0; e < V; ++e) s[j][e] = 0.f;
@@ -187,32 +224,56 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
       phase ^= 1u;
     }
 
-    DW tot = dw_warp_allreduce(dw_combine(dw_combine(acc[0], acc[1]), dw_combine(acc[2], acc[3])));
-    if (G > 1) {
-      // every warp of the group publishes its sum, then combines all G of them
-      // with the same fixed butterfly over lanes 0..G8-1, so all agree bit for bit
-      const int buf = (int)(it & 1u);
-      float2* part = partials + (size_t)(g * NRED + buf) * G;
-      const uint32_t rbar = smem_addr(&bars[2 * stages + g * NRED + buf]);
-      if (lane == 0) {
-        part[wg] = make_float2(tot.hi, tot.lo);
-        mbar_arrive(rbar);
+    const int64_t row = b + k * nb;
+    float rstd;
+    if constexpr (LN) {
+      // LayerNorm: mean from the exact-per-addition signed sum; then d = s - mean in place,
+      // residual_out stored from s on the way, and the sum of the squared deviations
+      DW tot = dw_warp_allreduce_signed(dw_combine_signed(dw2_fold(accp[0]), dw2_fold(accp[1])));
+      if (G > 1 && !group_reduce(tot, partials, bars, 2 * stages, g, NRED, (int)(it & 1u), G, G8, wg, lane, it, p,
+                                 dw_combine_signed))
+        return;
+      const float mean = __fdiv_rn(dw_value(tot), p.hidden_f);
+      const uint64_t mean2 = pk(mean, mean);
+      char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
+      DW2 accq[2] = {{0ull, 0ull}, {0ull, 0ull}};
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const int c = (j * G + wg) * 32 + lane;
+        if (EXACT || c < C) {
+          if constexpr (RES) {
+            uint32_t rw[4];
+            narrow<ACT, V>(s[j], rw);
+            store_bytes<16>(rrow + (size_t)c * 16, rw);
+          }
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e) {
+            const float2 df = unpk(sub_x2(pk(s[j][2 * e], s[j][2 * e + 1]), mean2));  // d = fl32(s - mean)
+            s[j][2 * e] = df.x;
+            s[j][2 * e + 1] = df.y;
+            // fl32(d * d) by the scalar multiply, which the compiler never fuses into the add
+            dw2_add(accq[e & 1], pk(__fmul_rn(df.x, df.x), __fmul_rn(df.y, df.y)));
+          }
+        }
       }
-      if (!mbar_wait(rbar, (it >> 1) & 1u, p.timeout_ns, p.status)) return;
-      const int src = lane & (G8 - 1);
-      const float2 mine = src < G ? part[src] : make_float2(0.f, 0.f);
-      DW t{mine.x, mine.y};
-      for (int off = G8 >> 1; off > 0; off >>= 1) t = dw_combine(t, dw_shfl_xor(t, off));
-      tot = t;
+      DW tot2 = dw_warp_allreduce(dw_combine(dw2_fold(accq[0]), dw2_fold(accq[1])));
+      if (G > 1 && !group_reduce(tot2, partials, bars, 2 * stages, g, NRED, 2 + (int)(it & 1u), G, G8, wg, lane,
+                                 it, p, dw_combine))
+        return;
+      rstd = row_rstd(dw_value(tot2), p.hidden_f, p.eps);
+    } else {
+      DW tot = dw_warp_allreduce(dw_combine(dw_combine(acc[0], acc[1]), dw_combine(acc[2], acc[3])));
+      if (G > 1 && !group_reduce(tot, partials, bars, 2 * stages, g, NRED, (int)(it & 1u), G, G8, wg, lane, it, p,
+                                 dw_combine))
+        return;
+      rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
     }
-    const float rstd = row_rstd(dw_value(tot), p.hidden_f, p.eps);
 
     // pass 2 (from registers): residual_out = RNE_act(s); out = RNE_od(RNE_wd(s * rstd) * w).
     // With a quantised output the out values stay in registers (packed) until the
     // row's largest |out| is known.
-    const int64_t row = b + k * nb;
     char* orow = Q ? nullptr : static_cast<char*>(p.out) + row * p.out_stride;
-    char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
+    char* rrow = (RES && !LN) ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
     uint32_t okeep[Q ? NCH : 1][Q ? OB / 4 : 1];
     float amax = 0.f;
     uint32_t amax2 = 0u;  // packed running max of |out| for a 16-bit out
@@ -229,7 +290,28 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
         uint32_t ww[WB / 4];
         load_bytes<WB>(wsm + (size_t)c * WB, ww);
         uint32_t ow[OB / 4];
-        if constexpr (WD == OD && WD != FAR_F32) {
+        if constexpr (LN) {
+          // out = RNE_od(fl32(fl32(RNE_wd(d * rstd) * gamma) + beta)), two lanes at a time
+          uint32_t bw[WB / 4];
+          load_bytes<WB>(bsm + (size_t)c * WB, bw);
+          const uint64_t rstd2 = pk(rstd, rstd);
+          float o[V];
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e) {
+            const float2 a = unpk(mul_x2(pk(sj[2 * e], sj[2 * e + 1]), rstd2));
+            float2 u;
+            if constexpr (WD == FAR_F32) {
+              // binary32 gamma and beta (the cast is the identity): scalar multiply and add
+              u.x = __fadd_rn(__fmul_rn(a.x, __uint_as_float(ww[2 * e])), __uint_as_float(bw[2 * e]));
+              u.y = __fadd_rn(__fmul_rn(a.y, __uint_as_float(ww[2 * e + 1])), __uint_as_float(bw[2 * e + 1]));
+            } else {
+              u = affine2_mixed<WD>(narrow2<WD>(a.x, a.y), ww[e], bw[e]);  // cast to the weight dtype first
+            }
+            o[2 * e] = u.x;
+            o[2 * e + 1] = u.y;
+          }
+          narrow<OD, V>(o, ow);
+        } else if constexpr (WD == OD && WD != FAR_F32) {
           // 16-bit weight and output (then act == wd): cast to the weight dtype,
           // then one packed multiply rounds the exact product once
 #pragma unroll
@@ -260,7 +342,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
         } else {
           store_bytes<OB>(orow + (size_t)c * OB, ow);
         }
-        if constexpr (RES) {
+        if constexpr (RES && !LN) {
           uint32_t rw[4];
           narrow<ACT, V>(sj, rw);
           store_bytes<16>(rrow + (size_t)c * 16, rw);
@@ -335,7 +417,56 @@ template <int DT> __device__ __forceinline__ float round_one(float v) {
   else return v;
 }
 
-template <int ACT, int WD, bool RES, int Q = kQuantNone>
+// a double word summed over the CTA: warps first, then the warp values in a fixed order
+// (every thread ends with the same bits); `part` is free again on return
+template <int NW, typename Combine, typename WarpReduce>
+__device__ __forceinline__ DW block_reduce(DW acc, float2* part, int warp, int lane, Combine combine,
+                                           WarpReduce warp_reduce) {
+  acc = warp_reduce(acc);
+  if (lane == 0) part[warp] = make_float2(acc.hi, acc.lo);
+  __syncthreads();
+  DW tot{part[0].x, part[0].y};
+  for (int i = 1; i < NW; ++i) tot = combine(tot, DW{part[i].x, part[i].y});
+  __syncthreads();
+  return tot;
+}
+
+// LayerNorm, one row per CTA in three passes over the row (the re-reads come from L1/L2):
+// the signed sum of s for the mean, the sum of the squared deviations, then the outputs
+template <int ACT, int WD, bool RES>
+__device__ __forceinline__ void generic_ln_row(const Params& p, int64_t row, float2* part, int warp, int lane) {
+  constexpr int OD = promote(ACT, WD);
+  constexpr int NW = kGenericThreads / 32;
+  const int64_t H = p.hidden;
+  const char* xr = static_cast<const char*>(p.x) + row * p.x_stride;
+  const char* rr = RES ? static_cast<const char*>(p.r) + row * p.r_stride : nullptr;
+  auto s_at = [&](int64_t i) {
+    float s = load_elem<ACT>(xr, i);
+    if constexpr (RES) s = __fadd_rn(s, load_elem<ACT>(rr, i));
+    return s;
+  };
+  DW acc{0.f, 0.f};
+  for (int64_t i = threadIdx.x; i < H; i += blockDim.x) dw_add_signed(acc, s_at(i));
+  const DW tot = block_reduce<NW>(acc, part, warp, lane, dw_combine_signed, dw_warp_allreduce_signed);
+  const float mean = __fdiv_rn(dw_value(tot), p.hidden_f);
+  DW acc2{0.f, 0.f};
+  for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+    const float d = __fsub_rn(s_at(i), mean);
+    dw_add(acc2, __fmul_rn(d, d));
+  }
+  const DW tot2 = block_reduce<NW>(acc2, part, warp, lane, dw_combine, dw_warp_allreduce);
+  const float rstd = row_rstd(dw_value(tot2), p.hidden_f, p.eps);
+  char* orow = static_cast<char*>(p.out) + row * p.out_stride;
+  char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
+  for (int64_t i = threadIdx.x; i < H; i += blockDim.x) {
+    const float s = s_at(i);  // each element is read and written by the same thread
+    if constexpr (RES) store_elem<ACT>(rrow, i, s);
+    const float n = round_one<WD>(__fmul_rn(__fsub_rn(s, mean), rstd));
+    store_elem<OD>(orow, i, __fadd_rn(__fmul_rn(n, load_elem<WD>(p.w, i)), load_elem<WD>(p.beta, i)));
+  }
+}
+
+template <int ACT, int WD, bool RES, int Q = kQuantNone, bool LN = false>
 __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p) {
   constexpr int OD = promote(ACT, WD);
   constexpr int NW = kGenericThreads / 32;
@@ -344,6 +475,10 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t H = p.hidden;
   for (int64_t row = blockIdx.x; row < p.tokens; row += gridDim.x) {
+    if constexpr (LN) {
+      generic_ln_row<ACT, WD, RES>(p, row, part, warp, lane);
+      continue;
+    }
     const char* xr = static_cast<const char*>(p.x) + row * p.x_stride;
     const char* rr = RES ? static_cast<const char*>(p.r) + row * p.r_stride : nullptr;
     DW acc{0.f, 0.f};
@@ -398,21 +533,21 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
 
 cudaError_t ensure_smem_attribute(const void* func, size_t bytes);
 
-template <int ACT, int WD, bool RES, int Q>
+template <int ACT, int WD, bool RES, int Q, bool LN = false>
 cudaError_t launch_typed(const Launch& L) {
   void (*k)(Params) = nullptr;
   if (L.kind == kGeneric) {
-    k = generic_kernel<ACT, WD, RES, Q>;
+    k = generic_kernel<ACT, WD, RES, Q, LN>;
   } else {
     switch (L.nch * 2 + (L.exact ? 1 : 0)) {
-      case 2: k = staged_kernel<ACT, WD, RES, 1, false, Q>; break;
-      case 3: k = staged_kernel<ACT, WD, RES, 1, true, Q>; break;
-      case 4: k = staged_kernel<ACT, WD, RES, 2, false, Q>; break;
-      case 5: k = staged_kernel<ACT, WD, RES, 2, true, Q>; break;
-      case 8: k = staged_kernel<ACT, WD, RES, 4, false, Q>; break;
-      case 9: k = staged_kernel<ACT, WD, RES, 4, true, Q>; break;
-      case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q>; break;
-      case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q>; break;
+      case 2: k = staged_kernel<ACT, WD, RES, 1, false, Q, LN>; break;
+      case 3: k = staged_kernel<ACT, WD, RES, 1, true, Q, LN>; break;
+      case 4: k = staged_kernel<ACT, WD, RES, 2, false, Q, LN>; break;
+      case 5: k = staged_kernel<ACT, WD, RES, 2, true, Q, LN>; break;
+      case 8: k = staged_kernel<ACT, WD, RES, 4, false, Q, LN>; break;
+      case 9: k = staged_kernel<ACT, WD, RES, 4, true, Q, LN>; break;
+      case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q, LN>; break;
+      case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q, LN>; break;
       default: return cudaErrorInvalidValue;
     }
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);
@@ -436,6 +571,13 @@ cudaError_t launch_quant(bool residual, const Launch& L) {
   if (L.quant == kQuantFp8)
     return residual ? launch_typed<ACT, WD, true, kQuantFp8>(L) : launch_typed<ACT, WD, false, kQuantFp8>(L);
   return cudaErrorInvalidValue;
+}
+
+// LayerNorm (plain output)
+template <int ACT, int WD>
+cudaError_t launch_ln(bool residual, const Launch& L) {
+  return residual ? launch_typed<ACT, WD, true, kQuantNone, true>(L)
+                  : launch_typed<ACT, WD, false, kQuantNone, true>(L);
 }
 
 }  // namespace far

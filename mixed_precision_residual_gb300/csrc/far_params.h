@@ -27,7 +27,8 @@ constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s: far beyond any legit
 struct Params {
   const void* x;
   const void* r;         // residual (unused by the no-residual variant)
-  const void* w;         // weight [hidden]
+  const void* w;         // weight [hidden] (gamma of LayerNorm)
+  const void* beta;      // LayerNorm shift [hidden], weight dtype
   void* out;             // [tokens, hidden] od
   void* res_out;         // [tokens, hidden] act (unused by the no-residual variant)
   int64_t tokens;
@@ -43,7 +44,7 @@ struct Params {
   int64_t r_stride;      // ... of the residual
   int64_t out_stride;    // ... of out
   int64_t res_stride;    // ... of residual_out
-  uint32_t w_smem_bytes; // hidden * sizeof(wd), rounded up to 16
+  uint32_t w_smem_bytes; // hidden * sizeof(wd), rounded up to 16 (twice that for LayerNorm: gamma, beta)
   uint32_t stage_bytes;  // bytes of one ring slot (x row, then residual row), 128-aligned
   void* q;               // quantised output [tokens, hidden] bytes (quantised variants)
   float* scale;          // per-row scale [tokens] (quantised variants)
@@ -59,6 +60,7 @@ struct Launch {
   Params p;
   int kind;
   int quant;   // QuantKind
+  bool ln;     // LayerNorm instead of RMSNorm
   int nch;     // 16-byte chunks per thread (staged kernel): 1, 2, 4 or 8
   bool exact;  // chunks == nch * warps_per_row * 32: no per-chunk bounds test
   dim3 grid, block;
@@ -67,13 +69,14 @@ struct Launch {
 };
 
 // cross-warp reduction buffers per group: two (the sum of squares, double-buffered over
-// rows), four with a quantised output (the row maximum too)
-__host__ __device__ constexpr int reduce_buffers(int q) { return q ? 4 : 2; }
+// rows), four with a quantised output (the row maximum too) or for LayerNorm (the sum
+// for the mean, then the sum of the squared deviations)
+__host__ __device__ constexpr int reduce_buffers(int q, bool ln = false) { return (q || ln) ? 4 : 2; }
 
 // shared-memory bytes the staged kernel needs for a plan
 inline size_t staged_smem_bytes(int stages, int groups, int warps_per_row, uint32_t w_smem_bytes,
-                                uint32_t stage_bytes, int q = 0) {
-  const int nred = reduce_buffers(q);
+                                uint32_t stage_bytes, int q = 0, bool ln = false) {
+  const int nred = reduce_buffers(q, ln);
   size_t bars = (size_t)(2 * stages + nred * groups) * 8;
   size_t red = (size_t)groups * nred * warps_per_row * 8;
   size_t head = (bars + red + 127) / 128 * 128;
@@ -87,6 +90,9 @@ cudaError_t launch_act_f32(int wd, bool residual, const Launch& L);
 cudaError_t launch_q_act_f16(int wd, bool residual, const Launch& L);
 cudaError_t launch_q_act_bf16(int wd, bool residual, const Launch& L);
 cudaError_t launch_q_act_f32(int wd, bool residual, const Launch& L);
+cudaError_t launch_ln_act_f16(int wd, bool residual, const Launch& L);
+cudaError_t launch_ln_act_bf16(int wd, bool residual, const Launch& L);
+cudaError_t launch_ln_act_f32(int wd, bool residual, const Launch& L);
 
 // the argument checks and the device-buffer launch behind the public entry points (far_api.cu)
 int check_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,

@@ -109,3 +109,37 @@ def check_both(far, d, where, offset=0, inplace=False):
     nout = far_norm(far, d, offset, inplace)
     b = gate(nout, oracle_norm(d), where=where + " rmsnorm")
     return a, b
+
+
+def square_sensitive_rows(dev: np.ndarray, S: np.ndarray, eps: float) -> np.ndarray:
+    """Rows whose rstd depends on rounding each square before the sum.
+
+    dev: [rows, hidden] binary32 values whose squares are summed (s for RMSNorm, the
+    deviations d for LayerNorm); S: the oracle's binary32 sums RN32(sum fl32(v^2)).
+    A row is kept when RN32 of the exact sum of the EXACT squares is another binary32
+    value and that changes fl32(1 / fl32(sqrt(fl32(fl32(S / H) + eps)))).  math.fsum
+    rounds correctly, so the sign of (exact sum - rounding boundary) it returns is exact.
+    """
+    import math
+
+    rows, H = dev.shape
+    keep = np.zeros(rows, bool)
+    for i in range(rows):
+        sq = [float(v) * float(v) for v in dev[i].astype(np.float64)]  # exact in binary64
+        r = np.float32(S[i])
+        up, down = np.nextafter(r, np.float32(np.inf)), np.nextafter(r, np.float32(-np.inf))
+        hi = (float(r) + float(up)) / 2
+        lo = (float(r) + float(down)) / 2
+        if math.fsum(sq + [-hi]) > 0:
+            alt = up
+        elif math.fsum(sq + [-lo]) < 0:
+            alt = down
+        else:
+            continue
+
+        def rstd(s):
+            var = np.float32(s / np.float32(H))
+            return np.float32(np.float32(1.0) / np.sqrt(np.float32(var + np.float32(eps))))
+
+        keep[i] = rstd(r) != rstd(alt)
+    return keep

@@ -213,3 +213,60 @@ def test_quantised_launch_plans_are_consistent(far):
                 assert (G - 1) * 32 * p["nch"] < chunks <= G * 32 * p["nch"], p
     finally:
         far.set_launch_override()
+
+
+def test_layernorm_validation(far):
+    """LayerNorm's checks (every call below is rejected before any CUDA call): beta
+    must be given, and no output may overlap it; the rest is RMSNorm's validation."""
+    x, r, g, b = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (5 << 30)
+    out, ro = FAKE + (3 << 30), FAKE + (4 << 30)
+    bf = code("bf16", "bf16")
+    L = far.lib
+    assert L.fused_add_layernorm(x, r, g, None, 1e-5, out, ro, 4, 64, bf, None) == 3
+    assert L.layernorm(x, g, None, 1e-5, out, 4, 64, bf, None) == 3
+    assert L.fused_add_layernorm(x, r, g, b, 1e-5, b + 64, ro, 4, 64, bf, None) == 5   # out over beta
+    assert L.fused_add_layernorm(x, r, g, b, 1e-5, out, b - 64, 4, 64, bf, None) == 5  # residual_out over beta
+    assert L.layernorm(x, g, b, 1e-5, b, 4, 64, bf, None) == 5
+    assert L.layernorm(x, g, b, 1e-5, out, 4, 64, code("f16", "bf16"), None) == 1
+    assert L.layernorm(x, g, b, -1.0, out, 4, 64, bf, None) == 6
+    assert L.layernorm(x, g, b, 1e-5, x + 2, 4, 64, bf, None) == 5
+    assert L.layernorm(None, None, None, 1e-5, None, 0, 64, bf, None) == 0  # zero tokens: a no-op
+
+
+def test_layernorm_launch_plans_are_consistent(far):
+    """LayerNorm plans: gamma and beta both in shared memory, four reduction buffers,
+    slots owned by one group, the CTA within its warp and shared-memory budgets."""
+    T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
+    try:
+        for override in [(-1, 0, 0, 0), (0, 8, 3, 0), (0, 4, 2, 3), (0, 2, 0, 0), (0, 8, 8, 8), (0, 1, 0, 0)]:
+            far.set_launch_override(*override)
+            for (act, wd), hidden, tokens, res, sms in itertools.product(
+                    [(T16, T16), (B16, B16), (B16, F32), (F32, F32), (F32, T16)],
+                    [1, 8, 1000, 4096, 5120, 8192, 16384, 32768], [1, 151, 4096, 65536], (True, False),
+                    (152, 1)):
+                p = far.plan_ln_for_sms(tokens, hidden, act, wd, res, sms)
+                if p["kind"] == 1:
+                    assert p["threads"] == 256 and p["smem"] == 0
+                    continue
+                G, g, st = p["warps_per_row"], p["groups"], p["stages"]
+                assert st >= 2 and st % g == 0, p
+                assert g * G <= (12 if p["nch"] == 8 else 16), p
+                assert p["threads"] == (1 + g * G) * 32 and p["smem"] <= 227 * 1024
+                sa, sw = (4 if act == F32 else 2), (4 if wd == F32 else 2)
+                chunks = hidden * sa // 16
+                assert (G - 1) * 32 * p["nch"] < chunks <= G * 32 * p["nch"], p
+                # shared memory holds gamma and beta besides the ring
+                w16 = -(-hidden * sw // 16) * 16
+                assert p["smem"] >= 2 * w16 + st * hidden * sa * (2 if res else 1), p
+    finally:
+        far.set_launch_override()
+
+
+def test_layernorm_plan_needs_aligned_beta(far):
+    """The staged kernel copies gamma and beta with 16-byte loads: a beta off a 16-byte
+    boundary must route the call to the generic kernel (host logic only)."""
+    B16 = torch.bfloat16
+    assert far.plan_ln_for_sms(4096, 4096, B16, B16, True, 152)["kind"] == 0
+    for off in (2, 8):
+        assert far.plan_ln_for_sms(4096, 4096, B16, B16, True, 152, beta_offset=off)["kind"] == 1
+        assert far.plan_ln_for_sms(4096, 4096, B16, B16, False, 152, beta_offset=off)["kind"] == 1

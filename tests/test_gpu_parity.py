@@ -10,7 +10,8 @@ import pytest
 import torch
 
 import far_gen
-from gpu_helpers import check_both, far_fused, far_norm, gate, oracle_fused, oracle_norm
+from gpu_helpers import (check_both, far_fused, far_norm, gate, oracle_fused, oracle_norm,
+                         square_sensitive_rows)
 from oracle_pins import bits_equal, golden
 
 pytestmark = pytest.mark.gpu
@@ -266,3 +267,28 @@ def test_strided_in_place(far):
     assert far.device_status() == 0
     ref_out, ref_res = oracle_fused(d)
     gate(xbig[:, :H].cpu(), ref_out, rbig[:, :H].cpu(), ref_res, "strided in place")
+
+
+def test_rounded_squares_are_summed(far):
+    """The sum of squares adds fl32(s * s), each square rounded, not the exact squares
+    (as a fused multiply-add would): rows where the two sums round to different binary32
+    values and so change rstd must still pass the gate, for both kernels."""
+    import numpy as np
+
+    import oracle
+
+    d = far_gen.custom_inputs("f32", "f32", 6000, 64, seed=31, scale_lo=0.5, scale_hi=2.0, eps=0.0)
+    x = d["x"].numpy()
+    S = np.array([oracle.exact_sum((row * row).astype(np.float32)) for row in x], np.float32)
+    rows = np.nonzero(square_sensitive_rows(x, S, 0.0))[0]
+    assert len(rows) >= 20, len(rows)
+    sel = dict(d, x=d["x"][rows].contiguous(), r=torch.zeros_like(d["x"][rows]), tokens=len(rows))
+    try:
+        for plan in [(-1, 0, 0, 0), (1, 0, 0, 0)]:
+            far.set_launch_override(*plan)
+            gate(far_norm(far, sel), oracle_norm(sel), where=f"rounded squares rmsnorm {plan}")
+            out, res = far_fused(far, sel)  # residual 0: s = x + 0 = x
+            ref_out, ref_res = oracle_fused(sel)
+            gate(out, ref_out, res, ref_res, where=f"rounded squares fused {plan}")
+    finally:
+        far.set_launch_override()
