@@ -15,8 +15,11 @@ from its own CUDA-event-timed launches, SM clocks sampled during the timed
 region, and the CPU oracle timed on the host cores as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl far|reference]
+                  [--op rmsnorm|layernorm|rmsnorm_int8|rmsnorm_fp8]
 Under torchrun each rank runs its own replica (weak scaling, no collective on
-the data path); rank 0 prints one JSON line.
+the data path); rank 0 prints one JSON line.  --op measures one of the other
+operations of the library the same way (its fused form, then its no-residual
+variant); the end-to-end leg exists for RMSNorm only (the host-buffer entry points).
 """
 from __future__ import annotations
 
@@ -38,6 +41,18 @@ if ROOT not in sys.path:
 import torch  # noqa: E402
 
 METRIC = "achieved HBM GB/s and tokens/s of fused add+RMSNorm at 1 GB300 (% of HBM peak)"
+OP_METRIC = {
+    "rmsnorm": METRIC,
+    "layernorm": "achieved HBM GB/s and tokens/s of fused add+LayerNorm at 1 GB300 (% of HBM peak)",
+    "rmsnorm_int8": "achieved HBM GB/s and tokens/s of fused add+RMSNorm with int8 per-token output at 1 GB300",
+    "rmsnorm_fp8": "achieved HBM GB/s and tokens/s of fused add+RMSNorm with FP8 E4M3 per-token output at 1 GB300",
+}
+OP_STEP = {
+    "rmsnorm": "fused_add_rmsnorm then rmsnorm on the same x",
+    "layernorm": "fused_add_layernorm then layernorm on the same x",
+    "rmsnorm_int8": "fused_add_rmsnorm_quant then rmsnorm_quant (int8) on the same x",
+    "rmsnorm_fp8": "fused_add_rmsnorm_quant then rmsnorm_quant (FP8 E4M3) on the same x",
+}
 WORKLOAD = "c5"
 CSRC = os.path.join(ROOT, "mixed_precision_residual_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -56,6 +71,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=4)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=sorted(OP_METRIC), default="rmsnorm")
     return ap.parse_args()
 
 
@@ -80,12 +96,37 @@ def job_rate(units_per_rank: float, world: int, ms_per_step: float) -> float:
     return units_per_rank * world / (ms_per_step * 1e-3)
 
 
-def step_bytes(tokens, hidden, act, wd, od):
-    """Algorithmic bytes of one step: (fused, variant)."""
+def step_bytes(tokens, hidden, act, wd, od, op="rmsnorm"):
+    """Algorithmic bytes of one step: (fused, variant).
+
+    Each input and output byte once, the weight once per launch (LayerNorm: gamma and
+    beta); a quantised output is one byte an element plus a binary32 scale per row."""
     sa, sw, so = DSIZE[act], DSIZE[wd], DSIZE[od]
-    fused = tokens * hidden * (2 * sa + sa + so) + hidden * sw
-    norm = tokens * hidden * (sa + so) + hidden * sw
+    nw = 2 if op == "layernorm" else 1
+    if op.startswith("rmsnorm_"):
+        fused = tokens * hidden * (3 * sa + 1) + 4 * tokens + hidden * sw
+        norm = tokens * hidden * (sa + 1) + 4 * tokens + hidden * sw
+        return fused, norm
+    fused = tokens * hidden * (2 * sa + sa + so) + nw * hidden * sw
+    norm = tokens * hidden * (sa + so) + nw * hidden * sw
     return fused, norm
+
+
+def oracle_step(op, d, x, r, threads):
+    """The oracle, as it stands, on rows x (and residual r): the fused op, then the variant."""
+    import oracle
+
+    act, wd, eps = d["act"], d["wd"], d["eps"]
+    if op == "rmsnorm":
+        oracle.fused_add_rmsnorm(x, r, d["w"], eps, act, wd, threads=threads)
+        oracle.rmsnorm(x, d["w"], eps, act, wd, threads=threads)
+    elif op == "layernorm":
+        oracle.fused_add_layernorm(x, r, d["w"], d["b"], eps, act, wd, threads=threads)
+        oracle.layernorm(x, d["w"], d["b"], eps, act, wd, threads=threads)
+    else:
+        q = op.split("_")[1]
+        oracle.fused_add_rmsnorm_quant(x, r, d["w"], eps, act, wd, q, threads=threads)
+        oracle.rmsnorm_quant(x, d["w"], eps, act, wd, q, threads=threads)
 
 
 KERNEL_SOURCES = ("far_kernels.cuh", "far_device.cuh", "far_params.h")
@@ -109,13 +150,13 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_from_profile(workload: str):
+def traffic_from_profile(workload: str, op: str = "rmsnorm"):
     """DRAM bytes per fused launch from a committed ncu summary, if the kernel sources still match."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
-    e = d.get(workload)
+    e = d.get(workload if op == "rmsnorm" else f"{workload}:{op}")
     if not e or e.get("source_hash") != source_hash():
         return None
     return e.get("dram_bytes_per_launch")
@@ -170,7 +211,7 @@ class ClockSampler:
                 "power_w_median": statistics.median(power) if power else None}
 
 
-def cpu_baseline(d, seconds: float):
+def cpu_baseline(d, seconds: float, op: str = "rmsnorm"):
     """The oracle, as it stands, on the first rows of the batch (fused + variant), host threads."""
     import oracle
 
@@ -182,17 +223,15 @@ def cpu_baseline(d, seconds: float):
     chunk = max(threads * 4, 64)
     while time.perf_counter() - t0 < seconds and rows_done < d["tokens"]:
         sl = slice(rows_done, min(d["tokens"], rows_done + chunk))
-        x, r = d["x"][sl], d["r"][sl]
-        oracle.fused_add_rmsnorm(x, r, d["w"], d["eps"], act, wd, threads=threads)
-        oracle.rmsnorm(x, d["w"], d["eps"], act, wd, threads=threads)
+        oracle_step(op, d, d["x"][sl], d["r"][sl], threads)
         rows_done = sl.stop
     el = time.perf_counter() - t0
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    fb, nb = step_bytes(rows_done, H, tdt[act], tdt[wd], tdt[od])
+    fb, nb = step_bytes(rows_done, H, tdt[act], tdt[wd], tdt[od], op)
     return {"value": round((fb + nb) / el / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "seconds": round(el, 2), "tokens_per_s": round(rows_done / el, 1),
-            "sample": f"first {rows_done} of {d['tokens']} rows of the {d['workload']} batch, fused add+RMSNorm "
-                      f"then the no-residual variant, oracle on {threads} host threads"}
+            "sample": f"first {rows_done} of {d['tokens']} rows of the {d['workload']} batch, {OP_STEP[op]}, "
+                      f"oracle on {threads} host threads"}
 
 
 def run_reference(args):
@@ -206,28 +245,27 @@ def run_reference(args):
     w = far_gen.WORKLOADS[args.workload]
     threads = oracle.default_threads()
     probe = far_gen.make_inputs(w, rows=threads * 2)
+    probe["b"] = far_gen.ln_beta(probe)
     t0 = time.perf_counter()
-    oracle.fused_add_rmsnorm(probe["x"], probe["r"], probe["w"], w.eps, w.act, w.wd, threads=threads)
-    oracle.rmsnorm(probe["x"], probe["w"], w.eps, w.act, w.wd, threads=threads)
+    oracle_step(args.op, probe, probe["x"], probe["r"], threads)
     per_row = (time.perf_counter() - t0) / (threads * 2)
     budget = 120.0  # seconds for all steps
     rows = int(max(threads, min(w.tokens, budget / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
     d = far_gen.make_inputs(w, rows=rows)
+    d["b"] = far_gen.ln_beta(d)
     for _ in range(args.warmup):
-        oracle.fused_add_rmsnorm(d["x"], d["r"], d["w"], w.eps, w.act, w.wd, threads=threads)
-        oracle.rmsnorm(d["x"], d["w"], w.eps, w.act, w.wd, threads=threads)
+        oracle_step(args.op, d, d["x"], d["r"], threads)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.fused_add_rmsnorm(d["x"], d["r"], d["w"], w.eps, w.act, w.wd, threads=threads)
-        oracle.rmsnorm(d["x"], d["w"], w.eps, w.act, w.wd, threads=threads)
+        oracle_step(args.op, d, d["x"], d["r"], threads)
     el = time.perf_counter() - t0
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
     od = "f32" if "f32" in (w.act, w.wd) else w.act
-    fb, nb = step_bytes(rows, w.hidden, tdt[w.act], tdt[w.wd], tdt[od])
+    fb, nb = step_bytes(rows, w.hidden, tdt[w.act], tdt[w.wd], tdt[od], args.op)
     value = (fb + nb) * args.steps / el / 1e9
-    sample = (f"{rows} of {w.tokens} rows of the {w.name} batch per step (fused add+RMSNorm then the "
-              f"no-residual variant), oracle on {threads} host threads")
-    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+    sample = (f"{rows} of {w.tokens} rows of the {w.name} batch per step ({OP_STEP[args.op]}), "
+              f"oracle on {threads} host threads")
+    line = {"impl": "reference", "metric": OP_METRIC[args.op], "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.act,
             "data": "synthetic (seeded Philox4x32-10 generator)",
@@ -264,23 +302,48 @@ def main():
 
     w = far_gen.WORKLOADS[args.workload]
     d = far_gen.make_inputs(w, seed=rank, rows=args.tokens or None)  # each rank its own batch (replica)
+    d["b"] = far_gen.ln_beta(d, seed=rank)
     dev = torch.device("cuda", local)
-    x, r, wt = d["x"].to(dev), d["r"].to(dev), d["w"].to(dev)
+    x, r, wt, bt = d["x"].to(dev), d["r"].to(dev), d["w"].to(dev), d["b"].to(dev)
     od = far.output_dtype(x.dtype, wt.dtype)
-    out = torch.empty(x.shape, dtype=od, device=dev)
+    quant = args.op.startswith("rmsnorm_")
+    out_dtype = torch.uint8 if quant else od
+    out = torch.empty(x.shape, dtype=out_dtype, device=dev)
     res = torch.empty_like(x)
-    out2 = torch.empty(x.shape, dtype=od, device=dev)
+    out2 = torch.empty(x.shape, dtype=out_dtype, device=dev)
     T, H = x.shape
+    sc1 = torch.empty(T, dtype=torch.float32, device=dev)
+    sc2 = torch.empty(T, dtype=torch.float32, device=dev)
     eps = d["eps"]
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     code = far.dtypes(x.dtype, wt.dtype)
     L = far.lib
-    xp, rp, wp, op, rop, o2p = (t.data_ptr() for t in (x, r, wt, out, res, out2))
+    xp, rp, wp, bp, op, rop, o2p = (t.data_ptr() for t in (x, r, wt, bt, out, res, out2))
+    s1p, s2p = sc1.data_ptr(), sc2.data_ptr()
+    qt = {"rmsnorm_int8": 1, "rmsnorm_fp8": 2}.get(args.op, 0)
+    if args.op == "rmsnorm":
+        def fused():
+            return L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh)
+
+        def variant():
+            return L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh)
+    elif args.op == "layernorm":
+        def fused():
+            return L.fused_add_layernorm(xp, rp, wp, bp, eps, op, rop, T, H, code, sh)
+
+        def variant():
+            return L.layernorm(xp, wp, bp, eps, o2p, T, H, code, sh)
+    else:
+        def fused():
+            return L.fused_add_rmsnorm_quant(xp, rp, wp, eps, op, s1p, rop, T, H, code, qt, sh)
+
+        def variant():
+            return L.rmsnorm_quant(xp, wp, eps, o2p, s2p, T, H, code, qt, sh)
 
     def step():
-        s1 = L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh)
-        s2 = L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh)
+        s1 = fused()
+        s2 = variant()
         if s1 or s2:
             raise RuntimeError(f"launch failed: {s1} {s2}")
 
@@ -300,11 +363,11 @@ def main():
     ev_start.record(stream)
     for k in range(args.steps):
         ev_f0[k].record(stream)
-        if L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh):
+        if fused():
             raise RuntimeError("fused launch failed")
         ev_f1[k].record(stream)
-        if L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh):
-            raise RuntimeError("rmsnorm launch failed")
+        if variant():
+            raise RuntimeError("variant launch failed")
     ev_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -316,13 +379,13 @@ def main():
     total_ms = max_over_ranks(ev_start.elapsed_time(ev_end), dist, dev)
     fused_ms = sum(a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)) / args.steps
     ms_per_step = total_ms / args.steps
-    fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od)
+    fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od, args.op)
     value = job_rate(fb + nb, world, ms_per_step) / 1e9
     tokens_per_s = job_rate(T, world, ms_per_step)
 
     # end to end through the host-buffer entry points: copies inside the timed region
     e2e = None
-    if args.e2e_steps > 0:
+    if args.e2e_steps > 0 and args.op == "rmsnorm":
         xh, rh, wh = d["x"].pin_memory(), d["r"].pin_memory(), d["w"].pin_memory()
         oh = torch.empty(x.shape, dtype=od, pin_memory=True)
         roh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
@@ -359,31 +422,43 @@ def main():
 
     peak, peak_kind = measured_peaks()
     achieved = fb / (fused_ms * 1e-3) / 1e9
-    traffic = traffic_from_profile(args.workload)
-    plan = far.describe_launch(T, H, x.dtype, wt.dtype, True)
+    traffic = traffic_from_profile(args.workload, args.op)
+    if args.op == "rmsnorm":
+        plan = far.describe_launch(T, H, x.dtype, wt.dtype, True)
+    elif args.op == "layernorm":
+        plan = far.plan_ln_for_sms(T, H, x.dtype, wt.dtype, True, torch.cuda.get_device_properties(dev).multi_processor_count)
+    else:
+        plan = far.plan_quant_for_sms(T, H, x.dtype, wt.dtype, True, args.op.split("_")[1],
+                                      torch.cuda.get_device_properties(dev).multi_processor_count)
+    kernel_name = {"rmsnorm": "fused add+RMSNorm", "layernorm": "fused add+LayerNorm",
+                   "rmsnorm_int8": "fused add+RMSNorm, int8 output",
+                   "rmsnorm_fp8": "fused add+RMSNorm, FP8 output"}[args.op]
     line = {
-        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "metric": OP_METRIC[args.op], "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16" if x.dtype == torch.float16 else str(x.dtype),
         "data": "synthetic (seeded Philox4x32-10 generator, per-row log-uniform scales)",
         "config": {"workload": f"{w.name}: {w.note}", "tokens": T, "hidden": H,
-                   "act_dtype": w.act, "weight_dtype": w.wd, "out_dtype": w.act if od == x.dtype else "f32",
-                   "eps": eps, "step": "fused_add_rmsnorm then rmsnorm on the same x",
+                   "act_dtype": w.act, "weight_dtype": w.wd, "out_dtype": {"rmsnorm_int8": "int8 + f32 scale per row",
+                                 "rmsnorm_fp8": "e4m3 + f32 scale per row"}.get(
+                       args.op, w.act if od == x.dtype else "f32"),
+                   "eps": eps, "step": OP_STEP[args.op],
                    "l2": "no flush: every tensor (1 GiB) is larger than the 129 MB L2",
-                   "parallelism": f"replicas x{world} (rows are independent; no collective)"},
+                   "parallelism": f"replicas x{world} (rows are independent; no collective)",
+                   "op": args.op},
         "tokens_per_s": round(tokens_per_s, 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "staged_kernel (fused add+RMSNorm)", "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": f"staged_kernel ({kernel_name})", "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": fb, "avg_launch_ms": round(fused_ms, 5),
                      "launch_plan": plan},
         "clocks": clk,
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds, args.op)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
