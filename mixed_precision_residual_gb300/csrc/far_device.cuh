@@ -335,6 +335,30 @@ __device__ __forceinline__ void dw2_add(DW2& acc, uint64_t v) {
   acc.hi = s;
   acc.lo = add_x2(acc.lo, e);
 }
+// The same two chains by the ordered Fast2Sum: the operand of larger magnitude first
+// (a compare and two selects, on the integer pipe), then three packed operations; exact
+// for any signs.  Half the floating-point work of TwoSum.
+__device__ __forceinline__ void dw2_add_ordered(DW2& acc, float v0, float v1) {
+  const float2 h = unpk(acc.hi);
+  const bool p0 = fabsf(h.x) >= fabsf(v0), p1 = fabsf(h.y) >= fabsf(v1);
+  const uint64_t big = pk(p0 ? h.x : v0, p1 ? h.y : v1);
+  const uint64_t small = pk(p0 ? v0 : h.x, p1 ? v1 : h.y);
+  const uint64_t s = add_x2(big, small);
+  acc.hi = s;
+  acc.lo = add_x2(acc.lo, sub_x2(small, sub_x2(s, big)));
+}
+// ... and for non-negative values, ordered by a NaN-propagating max / min pair; the
+// values enter through the max / min, so no multiply that formed them can be fused
+// into the add
+__device__ __forceinline__ void dw2_add_nonneg(DW2& acc, uint64_t v) {
+  const float2 h = unpk(acc.hi), q = unpk(v);
+  const uint64_t big = pk(max_nan(h.x, q.x), max_nan(h.y, q.y));
+  const uint64_t small = pk(min_nan(h.x, q.x), min_nan(h.y, q.y));
+  const uint64_t s = add_x2(big, small);
+  acc.hi = s;
+  acc.lo = add_x2(acc.lo, sub_x2(small, sub_x2(s, big)));
+}
+
 // the two chains of a DW2 folded into one double word
 __device__ __forceinline__ DW dw2_fold(DW2 a) {
   const float2 h = unpk(a.hi), l = unpk(a.lo);

@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
         }
         if constexpr (LN) {
 #pragma unroll
-          for (int e = 0; e < V / 2; ++e) dw2_add(accp[e & 1], pk(s[j][2 * e], s[j][2 * e + 1]));  // for the mean
+          for (int e = 0; e < V / 2; ++e) dw2_add_ordered(accp[e & 1], s[j][2 * e], s[j][2 * e + 1]);  // for the mean
         } else {
 #pragma unroll
           for (int e = 0; e < V; ++e) dw_add(acc[e & 3], __fmul_rn(s[j][e], s[j][e]));
@@ -248,11 +248,11 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q ==
           }
 #pragma unroll
           for (int e = 0; e < V / 2; ++e) {
-            const float2 df = unpk(sub_x2(pk(s[j][2 * e], s[j][2 * e + 1]), mean2));  // d = fl32(s - mean)
+            const uint64_t dv = sub_x2(pk(s[j][2 * e], s[j][2 * e + 1]), mean2);  // d = fl32(s - mean)
+            const float2 df = unpk(dv);
             s[j][2 * e] = df.x;
             s[j][2 * e + 1] = df.y;
-            // fl32(d * d) by the scalar multiply, which the compiler never fuses into the add
-            dw2_add(accq[e & 1], pk(__fmul_rn(df.x, df.x), __fmul_rn(df.y, df.y)));
+            dw2_add_nonneg(accq[e & 1], mul_x2(dv, dv));  // fl32(d * d), through max / min
           }
         }
       }
