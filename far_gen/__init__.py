@@ -30,6 +30,7 @@ _LIB = os.path.join(_HERE, "_build", "libfargen.so")
 
 # stream ids: one independent random sequence per role
 STREAM_X, STREAM_R, STREAM_W, STREAM_SCALE, STREAM_OUTLIER, STREAM_SIGN, STREAM_BETA = 1, 2, 3, 4, 5, 6, 7
+STREAM_GEMM_X, STREAM_GEMM_W, STREAM_GEMM_BIAS = 8, 9, 10
 
 TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
 
@@ -236,3 +237,14 @@ def custom_inputs(act: str, wd: str, tokens: int, hidden: int, seed: int = 0,
 def ln_beta(d: dict, seed: int = 0, sd: float = 0.1) -> torch.Tensor:
     """A LayerNorm shift for inputs `d`: [hidden] in the weight dtype, N(0, sd^2)."""
     return torch.from_numpy(normal(seed, STREAM_BETA, 0, d["hidden"], 0.0, sd)).to(d["w"].dtype)
+
+
+def gemm_inputs(M: int, N: int, K: int, seed: int = 0, bias: bool = True) -> dict:
+    """Operands of the fp16 GEMM: x [M, K] ~ N(0, 1), the transposed weight wt [N, K]
+    ~ N(0, 1/K) (so each output is about N(0, 1)), bias [N] ~ N(0, 0.1^2); fp16 CPU
+    tensors (each value drawn in binary64, rounded to binary32, then to fp16)."""
+    x = torch.from_numpy(normal(seed, STREAM_GEMM_X, 0, M * K, 0.0, 1.0)).reshape(M, K).to(torch.float16)
+    wt = torch.from_numpy(normal(seed, STREAM_GEMM_W, 0, N * K, 0.0, 1.0 / math.sqrt(max(K, 1))))
+    wt = wt.reshape(N, K).to(torch.float16)
+    b = torch.from_numpy(normal(seed, STREAM_GEMM_BIAS, 0, N, 0.0, 0.1)).to(torch.float16) if bias else None
+    return {"x": x, "wt": wt, "bias": b, "M": M, "N": N, "K": K}

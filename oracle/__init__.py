@@ -91,6 +91,8 @@ def bind(path: str) -> ctypes.CDLL:
     l.oracle_ln_row_stats.restype = i32
     l.oracle_exact_signed_sum.argtypes = [vp, i64]
     l.oracle_exact_signed_sum.restype = f32
+    l.oracle_gemm_f16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32]
+    l.oracle_gemm_f16.restype = i32
     return l
 
 
@@ -309,3 +311,33 @@ def ln_row_stats(x, residual, eps, act, L=None):
 def exact_signed_sum(values, L=None):
     v = np.ascontiguousarray(values, dtype=np.float32)
     return np.float32((L or lib()).oracle_exact_signed_sum(v.ctypes.data, v.size))
+
+
+def gemm_f16(x, wt, bias=None, out_dtype="f16", threads=None, L=None):
+    """Oracle of the fp16-storage / fp32-compute GEMM on CPU tensors.
+
+    x [M, K] and wt [N, K] fp16 (the transposed weight, row-major), bias [N] fp16 or
+    None.  out_dtype "f16": RNE_f16(RNE_f16(exact x @ wt^T) + bias); "f32": the exact
+    sum rounded once to binary32 (no bias)."""
+    L = L or lib()
+    if x.dtype != torch.float16 or wt.dtype != torch.float16 or (bias is not None and bias.dtype != torch.float16):
+        raise ValueError("the GEMM oracle takes fp16 operands")
+    if out_dtype == "f32" and bias is not None:
+        raise ValueError("the fp32 output takes no bias")
+    M, K = x.shape
+    N, K2 = wt.shape
+    if K != K2 or (bias is not None and bias.numel() != N):
+        raise ValueError("shape mismatch")
+    x, wt = x.contiguous(), wt.contiguous()
+    bias = None if bias is None else bias.contiguous()
+    out = torch.empty((M, N), dtype=TORCH_DTYPE[out_dtype])
+    so = out.element_size()
+
+    def work(t0, t1):
+        rc = L.oracle_gemm_f16(x.data_ptr() + t0 * K * 2, wt.data_ptr(), None if bias is None else bias.data_ptr(),
+                               out.data_ptr() + t0 * N * so, t1 - t0, N, K, DTYPE_CODE[out_dtype])
+        if rc != 0:
+            raise RuntimeError(f"oracle_gemm_f16 returned {rc}")
+
+    _rows_parallel(work, M, threads or default_threads())
+    return out

@@ -63,6 +63,11 @@
  *   n_i   = RNE_wd(fl32(d_i * rstd))           cast to the weight dtype first
  *   out_i = RNE_od(fl32(fl32(n_i * gamma_i) + beta_i))   gamma, beta in the weight dtype
  *
+ * GEMM with fp16 storage and fp32 compute (the Luminal page "Luminal FP16 Backend
+ * Repair and H100 Evidence", section "What Was Fixed"): the exact sum of the exact
+ * fp16 products, rounded once to fp16 (the projection cast), then the fp16 bias
+ * added with one more fp16 rounding; see oracle_gemm_f16.
+ *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math (binary32
  * arithmetic must not be fused or reassociated).
  */
@@ -607,3 +612,115 @@ uint16_t oracle_f32_to_f16(float v) { return encode_f16(round_f16(v)); }
 uint16_t oracle_f32_to_bf16(float v) { return encode_bf16(round_bf16(v)); }
 float oracle_f16_to_f32(uint16_t h) { return decode_f16(h); }
 float oracle_bf16_to_f32(uint16_t h) { return decode_bf16(h); }
+
+/* ------------------------------------------------------------------ */
+/* GEMM with fp16 storage and fp32 compute                             */
+/* ------------------------------------------------------------------ */
+/*
+ * The consumer projection of the Luminal page "Luminal FP16 Backend Repair and
+ * H100 Evidence" (section "What Was Fixed", the corrected adapter): the fp16
+ * operands are widened exactly, multiplied and summed in fp32, the result is
+ * cast to fp16 (the projection's rounding boundary), then the fp16 bias is added
+ * in fp16.  With x [M, K] and the transposed weight wt [N, K], both row-major:
+ *
+ *   p[m,n] = RNE_f16( sum_k x[m,k] * wt[n,k] )        (out_dtype fp16)
+ *   y[m,n] = RNE_f16( p[m,n] + bias[n] )              (bias optional)
+ *   out[m,n] = RN32( sum_k x[m,k] * wt[n,k] )         (out_dtype fp32, no bias)
+ *
+ * The sum is the exact sum, rounded once: "fp32 arithmetic" fixes no order of
+ * the additions, and the exact sum is the value every order approximates (the
+ * page's own reference evaluates it in fp64).  Each product of two fp16 values
+ * is exactly a binary32 value (22 significant bits, magnitudes from 2^-48 to
+ * below 2^32), so the products enter the exact accumulator unrounded.
+ */
+
+/* the exact non-negative sum in `a`, rounded to nearest (ties to even) in the binary
+   format with p significand bits and normal exponents emin..emax; infinity above it */
+static double acc_round_format(const exact_acc* a, int p, int emin, int emax) {
+    if (a->has_nan || (a->has_pinf && a->has_ninf)) return NAN;
+    if (a->has_pinf) return INFINITY;
+    if (a->has_ninf) return -INFINITY;
+    int top = -1;
+    for (int k = ACC_LIMBS * 32 - 1; k >= 0; --k)
+        if (acc_bit(a, k)) { top = k; break; }
+    if (top < 0) return 0.0;
+    int lead = top - 149;                            /* exponent of the leading bit */
+    int q = (lead > emin ? lead : emin) - (p - 1);   /* exponent of the last place kept */
+    int kq = q + 149;                                /* its bit index */
+    uint64_t keep = 0;
+    int guard = 0, sticky = 0;
+    for (int k = top; k >= 0; --k) {
+        int bit = acc_bit(a, k);
+        if (k >= kq) keep = (keep << 1) | (uint64_t)bit;
+        else if (k == kq - 1) guard = bit;
+        else if (bit) { sticky = 1; break; }
+    }
+    if (kq > 0 && guard && (sticky || (keep & 1u))) keep += 1;
+    double mag = kq > 0 ? ldexp((double)keep, q) : ldexp((double)keep, -149);
+    if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;
+    return mag;
+}
+
+/* the same for a signed sum */
+static double sacc_round_format(const signed_acc* a, int p, int emin, int emax) {
+    if (a->pos.has_nan || (a->pos.has_pinf && a->neg.has_pinf)) return NAN;
+    if (a->pos.has_pinf) return INFINITY;
+    if (a->neg.has_pinf) return -INFINITY;
+    int c = acc_compare(&a->pos, &a->neg);
+    if (c == 0) return 0.0;
+    const exact_acc* big = c > 0 ? &a->pos : &a->neg;
+    const exact_acc* small = c > 0 ? &a->neg : &a->pos;
+    exact_acc diff;
+    acc_init(&diff);
+    uint64_t borrow = 0;
+    for (int k = 0; k < ACC_LIMBS; ++k) {
+        uint64_t t = (uint64_t)big->limb[k] - (uint64_t)small->limb[k] - borrow;
+        diff.limb[k] = (uint32_t)t;
+        borrow = (t >> 63) & 1u;
+    }
+    double m = acc_round_format(&diff, p, emin, emax);
+    return c > 0 ? m : -m;
+}
+
+/* a binary64 value rounded to nearest (ties to even) in the fp16 format */
+static double round_double_f16(double v) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    const int p = 11, emin = -14, emax = 15;
+    int lead = ilogb(v);
+    int q = (lead > emin ? lead : emin) - (p - 1);
+    double scaled = ldexp(fabs(v), -q);   /* exact: a power-of-two scaling */
+    double keep = floor(scaled);
+    double rest = scaled - keep;          /* exact */
+    if (rest > 0.5 || (rest == 0.5 && fmod(keep, 2.0) != 0.0)) keep += 1.0;
+    double mag = ldexp(keep, q);
+    if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;
+    return v < 0 ? -mag : mag;
+}
+
+/* x [M, K], wt [N, K], bias [N] (or NULL): fp16 bit patterns; out [M, N] fp16 bits
+   (out_dtype OR_F16) or binary32 (OR_F32, bias must be NULL) */
+int oracle_gemm_f16(const uint16_t* x, const uint16_t* wt, const uint16_t* bias, void* out, int64_t M,
+                    int64_t N, int64_t K, int out_dtype) {
+    if (M < 0 || N < 0 || K < 0) return 4;
+    if (out_dtype != OR_F16 && out_dtype != OR_F32) return 2;
+    if (out_dtype == OR_F32 && bias) return 2;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            signed_acc acc;
+            sacc_init(&acc);
+            for (int64_t k = 0; k < K; ++k) {
+                float a = decode_f16(x[m * K + k]);
+                float b = decode_f16(wt[n * K + k]);
+                sacc_add(&acc, a * b);   /* exact: see above */
+            }
+            if (out_dtype == OR_F32) {
+                ((float*)out)[m * N + n] = (float)sacc_round_format(&acc, 24, -126, 127);
+                continue;
+            }
+            double p16 = sacc_round_format(&acc, 11, -14, 15);   /* the projection cast */
+            double y = bias ? round_double_f16(p16 + (double)decode_f16(bias[n])) : p16;
+            ((uint16_t*)out)[m * N + n] = encode_f16((float)y);   /* y is an fp16 value */
+        }
+    }
+    return 0;
+}

@@ -54,8 +54,8 @@ MUTANTS = {
                                 "return (uint16_t)(sign | (uint16_t)(m >> (-e)));")],
     # (">" instead of ">=" here would be an equivalent mutant: a value rounded to
     # exactly 2^16 encodes as the fp16 infinity anyway, and no |a| reaches it)
-    "overflow_exponent_off_by_one": [("if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;",
-                                      "if (mag >= ldexp(1.0, emax)) mag = INFINITY;")],
+    "overflow_exponent_off_by_one": [("if (mag >= ldexp(1.0, emax + 1)) mag = INFINITY;\n    float r = (float)mag;",
+                                      "if (mag >= ldexp(1.0, emax)) mag = INFINITY;\n    float r = (float)mag;")],
 }
 
 
@@ -197,3 +197,41 @@ def test_unmutated_copy_passes_layernorm_pins(tmp_path):
     L = _mutant_lib(tmp_path, "identity_ln", [])
     for check in (TL.check_signed_sum, TL.check_steps, TL.check_closed_forms, TL.check_fp64):
         check(L)
+
+
+GEMM_MUTANTS = {
+    # the page's rejected implementation: products rounded to fp16 before the sum
+    "gemm_products_rounded_to_f16": [("sacc_add(&acc, a * b);   /* exact: see above */",
+                                      "sacc_add(&acc, round_f16(a * b));")],
+    # the sum rounded to binary32 first, then to fp16 (double rounding)
+    "gemm_cast_through_f32": [("double p16 = sacc_round_format(&acc, 11, -14, 15);",
+                               "double p16 = round_double_f16((double)sacc_round(&acc));")],
+    # the bias added to the unrounded sum (across the projection's rounding boundary)
+    "gemm_bias_before_cast": [("double p16 = sacc_round_format(&acc, 11, -14, 15);",
+                               "if (bias) sacc_add(&acc, decode_f16(bias[n]));\n"
+                               "            double p16 = sacc_round_format(&acc, 11, -14, 15);"),
+                              ("double y = bias ? round_double_f16(p16 + (double)decode_f16(bias[n])) : p16;",
+                               "double y = p16;")],
+    # the weight read as [K, N] instead of the transposed [N, K] (kept in bounds)
+    "gemm_weight_not_transposed": [("float b = decode_f16(wt[n * K + k]);",
+                                    "float b = decode_f16(wt[(k * N + n) % (N * K)]);")],
+    # ties away from zero in the fp16 cast of the sum
+    "gemm_ties_away": [("if (kq > 0 && guard && (sticky || (keep & 1u))) keep += 1;",
+                        "if (kq > 0 && guard) keep += 1;")],
+    # (dropping the overflow test of the cast would be an equivalent mutant: a sum that
+    # rounds to 2^16 encodes as the fp16 infinity anyway, and no binary32 sum of fp16
+    # products reaches 2^128)
+}
+
+
+@pytest.mark.parametrize("name", sorted(GEMM_MUTANTS))
+def test_gemm_mutant_is_caught(tmp_path, name):
+    import test_oracle_gemm as TG
+    L = _mutant_lib(tmp_path, name, GEMM_MUTANTS[name])
+    failed = []
+    for check in TG.GEMM_CHECKS:
+        try:
+            check(L)
+        except (AssertionError, RuntimeError):
+            failed.append(check.__name__)
+    assert failed, f"no pin rejects the planted mistake {name!r}"
