@@ -248,3 +248,17 @@ def gemm_inputs(M: int, N: int, K: int, seed: int = 0, bias: bool = True) -> dic
     wt = wt.reshape(N, K).to(torch.float16)
     b = torch.from_numpy(normal(seed, STREAM_GEMM_BIAS, 0, N, 0.0, 0.1)).to(torch.float16) if bias else None
     return {"x": x, "wt": wt, "bias": b, "M": M, "N": N, "K": K}
+
+
+def gemm_dyadic_inputs(M: int, N: int, K: int, seed: int = 0) -> dict:
+    """GEMM operands on a dyadic grid: x, wt in {k/8 : -8 <= k <= 8}, bias in {k/16 : -16
+    <= k <= 16}.  Every product is a multiple of 2^-6 of magnitude <= 1, so every partial
+    sum of up to 2^10 products is exact in binary32 whatever the order of the additions."""
+    def grid(stream, n, half, scale):
+        u = uniform(seed, stream, 0, n)
+        return torch.from_numpy((np.floor(u * (2 * half + 1)) - half) / scale).to(torch.float16)
+
+    x = grid(STREAM_GEMM_X, M * K, 8, 8.0).reshape(M, K)
+    wt = grid(STREAM_GEMM_W, N * K, 8, 8.0).reshape(N, K)
+    b = grid(STREAM_GEMM_BIAS, N, 16, 16.0)
+    return {"x": x, "wt": wt, "bias": b, "M": M, "N": N, "K": K}

@@ -164,6 +164,35 @@ int fused_add_layernorm(const void* x, const void* residual, const void* gamma, 
 int layernorm(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
               int64_t hidden, int dtype, void* stream);
 
+/*
+ * The consumer GEMM with fp16 storage and fp32 compute (the Luminal page "Luminal FP16
+ * Backend Repair and H100 Evidence", section "What Was Fixed": the fp16 operands widened
+ * exactly, products and sums in fp32, the result cast to fp16, then the fp16 bias add):
+ *   x    [m, k] fp16, row-major, device
+ *   wt   [n, k] fp16, row-major, device: the transposed weight (y = x @ wt^T)
+ *   bias [n] fp16, device, or NULL
+ *   out  [m, n] row-major, device:
+ *     out_dtype FAR_F16: out = RNE_f16(RNE_f16(sum_k x[i,k] * wt[j,k]) + bias[j])
+ *     out_dtype FAR_F32: out = the binary32 sum (bias must be NULL)
+ * The order of the binary32 additions is not specified (tensor cores accumulate in
+ * their own order); each product of two fp16 values is exact in binary32.  Tensor
+ * cores (tcgen05) are used when k is a positive multiple of 8, n a multiple of 8 and
+ * every pointer 16-byte aligned; any other shape takes a plain kernel with the same
+ * contract.  out may not overlap x, wt or bias.  Statuses: FAR_ERR_DTYPE (out_dtype,
+ * or a bias with FAR_F32), FAR_ERR_SHAPE (a negative size or one above 2^31 - 1),
+ * FAR_ERR_NULL, FAR_ERR_ALIAS, FAR_ERR_CUDA.  Enqueued on `stream`; m == 0 or n == 0
+ * is a no-op; k == 0 gives RNE_f16(0 + bias).
+ */
+int gemm_f16_f32acc(const void* x, const void* wt, const void* bias, void* out, int64_t m, int64_t n, int64_t k,
+                    int out_dtype, void* stream);
+
+/* the GEMM's plan for a device with `sms` SMs (host logic only, aligned operands):
+   out6 = {kind (0 tensor cores, 1 plain), tile width, grid, threads, dynamic shared bytes, stages} */
+int far_plan_gemm_for_sms(int64_t m, int64_t n, int64_t k, int has_bias, int out_dtype, int sms, int* out6);
+/* process-wide override of the GEMM plan, for measurements and tests: kind -1 automatic,
+   0 tensor cores where feasible, 1 the plain kernel; bn 0 automatic, else 64, 128 or 256 */
+int far_set_gemm_override(int kind, int bn);
+
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
 int far_output_dtype(int dtype);
 

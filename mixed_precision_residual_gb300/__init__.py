@@ -57,6 +57,12 @@ lib.layernorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
 lib.layernorm.restype = _int
 lib.far_plan_ln_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
 lib.far_plan_ln_for_sms.restype = _int
+lib.gemm_f16_f32acc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
+lib.gemm_f16_f32acc.restype = _int
+lib.far_plan_gemm_for_sms.argtypes = [_i64, _i64, _i64, _int, _int, _int, _vp]
+lib.far_plan_gemm_for_sms.restype = _int
+lib.far_set_gemm_override.argtypes = [_int, _int]
+lib.far_set_gemm_override.restype = _int
 lib.far_output_dtype.argtypes = [_int]
 lib.far_output_dtype.restype = _int
 lib.far_status_string.argtypes = [_int]
@@ -333,3 +339,39 @@ def plan_ln_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype,
     _check(lib.far_plan_ln_for_sms(tokens, hidden, dtypes(act, wd), int(residual), beta_offset, sms,
                                    ctypes.addressof(buf)))
     return dict(zip(("kind", "nch", "warps_per_row", "groups", "stages", "grid", "threads", "smem"), list(buf)))
+
+
+_OUT_CODE = {torch.float16: 1, torch.float32: 0}
+
+
+def gemm_f16_f32acc(x: torch.Tensor, wt: torch.Tensor, bias: torch.Tensor | None = None,
+                    out: torch.Tensor | None = None, out_dtype: torch.dtype = torch.float16, stream=None):
+    """y = RNE_f16(RNE_f16(x @ wt^T) + bias) with fp32 products and sums (fp16 storage).
+
+    x [M, K] and wt [N, K] (the transposed weight) fp16, contiguous; bias [N] fp16 or
+    None; out_dtype torch.float32 returns the fp32 sums (no bias)."""
+    if x.dtype != torch.float16 or wt.dtype != torch.float16 or (bias is not None and bias.dtype != torch.float16):
+        raise ValueError("fp16 operands expected")
+    if not (x.is_contiguous() and wt.is_contiguous() and (bias is None or bias.is_contiguous())):
+        raise ValueError("contiguous operands expected")
+    M, K = x.shape
+    N, K2 = wt.shape
+    if K2 != K or (bias is not None and bias.numel() != N):
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    if out.shape != (M, N) or not out.is_contiguous() or out.dtype not in _OUT_CODE:
+        raise ValueError("out must be a contiguous [M, N] fp16 or fp32 tensor")
+    _check(lib.gemm_f16_f32acc(_ptr(x), _ptr(wt), _ptr(bias), _ptr(out), M, N, K, _OUT_CODE[out.dtype],
+                               _stream_handle(stream)))
+    return out
+
+
+def plan_gemm_for_sms(m: int, n: int, k: int, bias: bool, out_dtype: torch.dtype, sms: int) -> dict:
+    buf = (ctypes.c_int * 6)()
+    _check(lib.far_plan_gemm_for_sms(m, n, k, int(bias), _OUT_CODE[out_dtype], sms, ctypes.addressof(buf)))
+    return dict(zip(("kind", "bn", "grid", "threads", "smem", "stages"), list(buf)))
+
+
+def set_gemm_override(kind: int = -1, bn: int = 0) -> None:
+    _check(lib.far_set_gemm_override(kind, bn))

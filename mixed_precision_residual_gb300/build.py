@@ -20,8 +20,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfar.so")
 SOURCES = ["far_api.cu", "far_inst_f16.cu", "far_inst_bf16.cu", "far_inst_f32.cu", "far_inst_q_f16.cu",
            "far_inst_q_bf16.cu", "far_inst_q_f32.cu", "far_inst_ln_f16.cu", "far_inst_ln_bf16.cu",
-           "far_inst_ln_f32.cu", "far_noalloc.cu"]
-HEADERS = ["far_device.cuh", "far_kernels.cuh", "far_params.h"]
+           "far_inst_ln_f32.cu", "far_noalloc.cu", "far_gemm.cu"]
+HEADERS = ["far_device.cuh", "far_kernels.cuh", "far_params.h", "far_tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false",
                      "-ftz=false", "-prec-div=true", "-prec-sqrt=true",

@@ -633,6 +633,17 @@ int enqueue_device_call(const void* x, const void* r, const void* w, float eps, 
   return run(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, stream);
 }
 
+int device_info(unsigned int** status, int* sms) {
+  DeviceState* dev = nullptr;
+  int st = current_device(dev);
+  if (st != FAR_OK) return st;
+  *status = dev->status;
+  *sms = dev->sms;
+  return FAR_OK;
+}
+
+int cuda_error_status(cudaError_t e) { return cuda_fail(e); }
+
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream) {
   wait_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
   return cudaGetLastError();

@@ -1,0 +1,438 @@
+// GEMM with fp16 storage and fp32 compute: y = RNE_f16(RNE_f16(x @ wt^T) + bias), or the
+// fp32 accumulators (the Luminal page "Luminal FP16 Backend Repair and H100 Evidence",
+// section "What Was Fixed": operands widened exactly, fp32 products and sums, the result
+// cast to fp16, then the fp16 bias add).  x [M, K] and wt [N, K] are row-major, so both
+// operands are K-major.
+//
+// tc_gemm_kernel -- the tensor-core path.  One 128 x BN output tile per CTA:
+//   warp 0, one lane: TMA producer, a ring of STAGES (A, B) K-slices of 64 values,
+//     128-byte swizzled, completion counted on "full" mbarriers;
+//   warp 1: allocates BN TMEM columns; one lane issues tcgen05.mma (128 x BN x 16, fp16
+//     in, fp32 accumulators in TMEM), releasing each slice with tcgen05.commit on its
+//     "empty" mbarrier and signalling the finished tile on "acc_full";
+//   warps 2..5: epilogue, each reading its 32-lane quarter of TMEM (32 rows), casting
+//     to fp16, adding the bias in fp16 and storing.
+//   Every wait is bounded (FAR_ERR_TIMEOUT in the device error word on expiry).
+// generic_gemm_kernel -- any shape or alignment: one thread an output, products and
+//   sums in binary32 in the order of k.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <utility>
+
+#include "far.h"
+#include "far_params.h"
+#include "far_tcgen05.cuh"
+
+namespace far {
+
+struct GemmParams {
+  void* out;               // [M, N] fp16 or fp32
+  const __half* bias;      // [N] or NULL
+  const __half* x;         // generic kernel only
+  const __half* wt;        // generic kernel only
+  int32_t M, N, K;
+  int32_t out_f32;         // 1: fp32 accumulators, 0: fp16 (+ bias)
+  int32_t tiles_m;
+  unsigned int* status;
+  uint64_t timeout_ns;
+};
+
+constexpr int kGemmBM = 128;      // rows of an output tile (the MMA's M)
+constexpr int kGemmBK = 64;       // K values per pipeline slice: one 128-byte swizzle row
+constexpr int kGemmUK = 16;       // K of one tcgen05.mma for fp16
+constexpr int kGemmThreads = 192; // producer, MMA, 4 epilogue warps
+
+template <int BN>
+struct GemmShape {
+  static constexpr uint32_t a_bytes = kGemmBM * kGemmBK * 2;
+  static constexpr uint32_t b_bytes = BN * kGemmBK * 2;
+  static constexpr int stages = (BN == 256) ? 4 : (BN == 128) ? 6 : 8;
+  static constexpr uint32_t ring_bytes = stages * (a_bytes + b_bytes);
+  // ring (1024-aligned) + barriers (full, empty, acc_full) + TMEM address + alignment slack
+  static constexpr size_t smem_bytes = ring_bytes + (2 * stages + 1) * 8 + 16 + 1024;
+};
+
+// 32 fp32 accumulators of one row -> 32 outputs at out[row, col0 ..]
+__device__ __forceinline__ void gemm_store32(const GemmParams& p, int64_t row, int col0, const uint32_t (&r)[32]) {
+  if (row >= p.M) return;
+  const bool full = col0 + 32 <= p.N;
+  if (p.out_f32) {
+    float* o = static_cast<float*>(p.out) + row * (int64_t)p.N + col0;
+    if (full) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<uint4*>(o + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < p.N) o[j] = __uint_as_float(r[j]);
+    }
+    return;
+  }
+  __half* o = static_cast<__half*>(p.out) + row * (int64_t)p.N + col0;
+  if (full) {
+    uint32_t bw[16];
+    if (p.bias) {
+      const uint4* b4 = reinterpret_cast<const uint4*>(p.bias + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = b4[q];
+        bw[4 * q] = v.x; bw[4 * q + 1] = v.y; bw[4 * q + 2] = v.z; bw[4 * q + 3] = v.w;
+      }
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      __half2 h = __floats2half2_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));  // the cast
+      if (p.bias) h = __hadd2(h, *reinterpret_cast<const __half2*>(&bw[j]));  // fp16 add, one rounding
+      w[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(o + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (col0 + j < p.N) {
+        __half h = __float2half_rn(__uint_as_float(r[j]));
+        if (p.bias) h = __hadd(h, p.bias[col0 + j]);
+        o[j] = h;
+      }
+    }
+  }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const GemmParams p) {
+  using S = GemmShape<BN>;
+  constexpr int STAGES = S::stages;
+  constexpr uint32_t IDESC = umma_idesc_f16_f32(kGemmBM, BN);
+  extern __shared__ unsigned char smem_raw[];
+  // the 128-byte swizzle wants every tile on a 1024-byte boundary
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t a_base = sbase, b_base = sbase + STAGES * S::a_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::ring_bytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
+  const uint32_t acc_full = smem_addr(&bars[2 * STAGES]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tm = blockIdx.x % p.tiles_m, tn = blockIdx.x / p.tiles_m;
+  const int num_kb = (p.K + kGemmBK - 1) / kGemmBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);   // the producer's arrive + the bytes
+      mbar_init(empty0 + 8 * s, 1);  // one tcgen05.commit
+    }
+    mbar_init(acc_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      int kb = 0;
+      for (; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, p.status)) break;
+        mbar_arrive_expect_tx(full0 + 8 * s, S::a_bytes + S::b_bytes);
+        tma_load_2d(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, tm * kGemmBM, full0 + 8 * s);
+        tma_load_2d(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
+      }
+      // the copies of the last slices must have landed before the CTA may exit
+      for (int j = (kb > STAGES ? kb - STAGES : 0); j < kb; ++j)
+        mbar_wait(full0 + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u, p.timeout_ns, p.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % STAGES;
+        if (!mbar_wait(full0 + 8 * s, (uint32_t)(kb / STAGES) & 1u, p.timeout_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t a = a_base + s * S::a_bytes, b = b_base + s * S::b_bytes;
+#pragma unroll
+        for (int k = 0; k < kGemmBK / kGemmUK; ++k)
+          umma_f16(tmem, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), IDESC,
+                   (kb | k) != 0);
+        umma_commit(empty0 + 8 * s);  // the slice is free once these MMAs have read it
+      }
+      umma_commit(acc_full);  // the tile's accumulators are final
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // the TMEM lanes this warp may read: 32 * quarter ..
+    if (mbar_wait(acc_full, 0u, p.timeout_ns, p.status)) {
+      tc_fence_after();
+      const int64_t row = (int64_t)tm * kGemmBM + quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, r);
+        tmem_ld_wait(r);
+        const int col0 = tn * BN + c;
+        if (col0 < p.N) gemm_store32(p, row, col0, r);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// any shape, any alignment: out[m, n] = sum_k x[m, k] * wt[n, k] in binary32 (each product
+// of two fp16 values is exact), then the cast and the fp16 bias add
+__global__ void __launch_bounds__(256) generic_gemm_kernel(const GemmParams p) {
+  const int64_t total = (int64_t)p.M * p.N;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t m = i / p.N, n = i - m * p.N;
+    const __half* xr = p.x + m * (int64_t)p.K;
+    const __half* wr = p.wt + n * (int64_t)p.K;
+    float acc = 0.f;
+    for (int k = 0; k < p.K; ++k) acc = __fadd_rn(acc, __fmul_rn(__half2float(xr[k]), __half2float(wr[k])));
+    if (p.out_f32) {
+      static_cast<float*>(p.out)[i] = acc;
+    } else {
+      __half h = __float2half_rn(acc);
+      if (p.bias) h = __hadd(h, p.bias[n]);
+      static_cast<__half*>(p.out)[i] = h;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+std::mutex g_encode_mu;
+std::atomic<int> g_gemm_force_kind{-1}, g_gemm_force_bn{0};  // tuning override (-1 / 0: automatic)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_encode_mu);
+  if (!g_encode) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !f) return FAR_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  *fn = g_encode;
+  return FAR_OK;
+}
+
+// a row-major [rows, K] fp16 matrix read in boxes of box_rows x 64, 128-byte swizzled;
+// out-of-range elements of a box read as zero
+int encode_kmajor(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc;
+  int st = get_encoder(&enc);
+  if (st != FAR_OK) return st;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kGemmBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FAR_OK : FAR_ERR_CUDA;
+}
+
+struct GemmCall {
+  const void* x;
+  const void* wt;
+  const void* bias;
+  void* out;
+  int64_t M, N, K;
+  int out_dtype;
+};
+
+bool al16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate_gemm(const GemmCall& c) {
+  if (c.out_dtype != FAR_F16 && c.out_dtype != FAR_F32) return FAR_ERR_DTYPE;
+  if (c.out_dtype == FAR_F32 && c.bias) return FAR_ERR_DTYPE;
+  const int64_t lim = (int64_t)INT32_MAX;
+  if (c.M < 0 || c.N < 0 || c.K < 0 || c.M > lim || c.N > lim || c.K > lim) return FAR_ERR_SHAPE;
+  // byte sizes must fit in int64 comfortably
+  if ((c.M && c.N > (INT64_MAX / 8) / c.M) || (c.M && c.K > (INT64_MAX / 8) / c.M) ||
+      (c.N && c.K > (INT64_MAX / 8) / c.N))
+    return FAR_ERR_SHAPE;
+  if (c.M == 0 || c.N == 0) return FAR_OK;
+  if (!c.out || (c.K > 0 && (!c.x || !c.wt))) return FAR_ERR_NULL;
+  const uint64_t so = c.out_dtype == FAR_F32 ? 4 : 2;
+  auto span = [](const void* p, uint64_t bytes) { return std::pair<uint64_t, uint64_t>((uint64_t)(uintptr_t)p, (uint64_t)(uintptr_t)p + bytes); };
+  auto overlap = [](std::pair<uint64_t, uint64_t> a, std::pair<uint64_t, uint64_t> b) {
+    return a.first < b.second && b.first < a.second;
+  };
+  const auto O = span(c.out, (uint64_t)c.M * c.N * so);
+  if (c.K > 0 && (overlap(O, span(c.x, (uint64_t)c.M * c.K * 2)) || overlap(O, span(c.wt, (uint64_t)c.N * c.K * 2))))
+    return FAR_ERR_ALIAS;
+  if (c.bias && overlap(O, span(c.bias, (uint64_t)c.N * 2))) return FAR_ERR_ALIAS;
+  return FAR_OK;
+}
+
+struct GemmPlan {
+  int kind;   // 0 tensor cores, 1 generic
+  int bn;     // tile width
+  int grid, block;
+  size_t smem;
+};
+
+// tensor cores when TMA can read both operands (16-byte aligned rows and bases) and the
+// vector epilogue can write (N a multiple of 8, 16-byte aligned out and bias); the tile
+// width is the widest that still gives at least one tile per SM, else 64
+GemmPlan plan_gemm(const GemmCall& c, int sms) {
+  GemmPlan g{1, 0, 1, 256, 0};
+  const bool tc = c.K > 0 && c.K % 8 == 0 && c.N % 8 == 0 && al16(c.x) && al16(c.wt) && al16(c.out) &&
+                  (!c.bias || al16(c.bias));
+  const int64_t tiles_m = (c.M + kGemmBM - 1) / kGemmBM;
+  if (tc && g_gemm_force_kind.load() != 1) {
+    int bn = 64;
+    for (int cand : {256, 128}) {
+      if (tiles_m * ((c.N + cand - 1) / cand) >= sms) {
+        bn = cand;
+        break;
+      }
+    }
+    if (g_gemm_force_bn.load() > 0) bn = g_gemm_force_bn.load();
+    const int64_t tiles = tiles_m * ((c.N + bn - 1) / bn);
+    if (tiles <= INT32_MAX) {
+      g.kind = 0;
+      g.bn = bn;
+      g.grid = (int)tiles;
+      g.block = kGemmThreads;
+      g.smem = bn == 256 ? GemmShape<256>::smem_bytes : bn == 128 ? GemmShape<128>::smem_bytes
+                                                                   : GemmShape<64>::smem_bytes;
+      return g;
+    }
+  }
+  const int64_t total = c.M * c.N;
+  const int64_t blocks = (total + 255) / 256;
+  g.grid = (int)(blocks < (int64_t)sms * 16 ? blocks : (int64_t)sms * 16);
+  return g;
+}
+
+template <int BN>
+cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, const GemmPlan& g,
+                      cudaStream_t stream) {
+  static std::mutex mu;
+  static int done_dev = -1;  // the attribute is per device: set it on each new one
+  {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    if (done_dev != dev) {
+      cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)GemmShape<BN>::smem_bytes);
+      if (e != cudaSuccess) return e;
+      done_dev = dev;
+    }
+  }
+  tc_gemm_kernel<BN><<<g.grid, g.block, g.smem, stream>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t M, int64_t N, int64_t K,
+             int out_dtype, void* stream) {
+  GemmCall c{x, wt, bias, out, M, N, K, out_dtype};
+  int st = validate_gemm(c);
+  if (st != FAR_OK || M == 0 || N == 0) return st;
+  unsigned int* status = nullptr;
+  int sms = 0;
+  st = device_info(&status, &sms);
+  if (st != FAR_OK) return st;
+  const GemmPlan g = plan_gemm(c, sms);
+  GemmParams p{};
+  p.out = out;
+  p.bias = static_cast<const __half*>(bias);
+  p.x = static_cast<const __half*>(x);
+  p.wt = static_cast<const __half*>(wt);
+  p.M = (int32_t)M;
+  p.N = (int32_t)N;
+  p.K = (int32_t)K;
+  p.out_f32 = out_dtype == FAR_F32;
+  p.tiles_m = (int32_t)((M + kGemmBM - 1) / kGemmBM);
+  p.status = status;
+  p.timeout_ns = kWaitTimeoutNs;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (g.kind == 0) {
+    CUtensorMap ma, mb;
+    st = encode_kmajor(&ma, x, M, K, kGemmBM);
+    if (st == FAR_OK) st = encode_kmajor(&mb, wt, N, K, g.bn);
+    if (st != FAR_OK) return st;
+    e = g.bn == 256 ? launch_tc<256>(ma, mb, p, g, s)
+        : g.bn == 128 ? launch_tc<128>(ma, mb, p, g, s)
+                      : launch_tc<64>(ma, mb, p, g, s);
+  } else {
+    generic_gemm_kernel<<<g.grid, g.block, 0, s>>>(p);
+    e = cudaGetLastError();
+  }
+  return e == cudaSuccess ? FAR_OK : cuda_error_status(e);
+}
+
+int plan_gemm_for_sms(int64_t M, int64_t N, int64_t K, int has_bias, int out_dtype, int sms, int* out6) {
+  // stand-in addresses (aligned, disjoint): only the plan is computed
+  const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
+  GemmCall c{base, base + (1ll << 36), has_bias ? base + (2ll << 36) : nullptr, const_cast<char*>(base + (3ll << 36)),
+             M, N, K, out_dtype};
+  int st = validate_gemm(c);
+  if (st != FAR_OK) return st;
+  if (M == 0 || N == 0 || sms < 1) return FAR_ERR_SHAPE;
+  const GemmPlan g = plan_gemm(c, sms);
+  int v[6] = {g.kind, g.bn, g.grid, g.block, (int)g.smem, g.kind == 0 ? (g.bn == 256 ? 4 : g.bn == 128 ? 6 : 8) : 0};
+  for (int i = 0; i < 6; ++i) out6[i] = v[i];
+  return FAR_OK;
+}
+
+}  // namespace far
+
+extern "C" {
+
+int gemm_f16_f32acc(const void* x, const void* wt, const void* bias, void* out, int64_t m, int64_t n, int64_t k,
+                    int out_dtype, void* stream) {
+  return far::run_gemm(x, wt, bias, out, m, n, k, out_dtype, stream);
+}
+
+int far_set_gemm_override(int kind, int bn) {
+  if (kind < -1 || kind > 1 || (bn != 0 && bn != 64 && bn != 128 && bn != 256)) return FAR_ERR_SHAPE;
+  far::g_gemm_force_kind = kind;
+  far::g_gemm_force_bn = bn;
+  return FAR_OK;
+}
+
+int far_plan_gemm_for_sms(int64_t m, int64_t n, int64_t k, int has_bias, int out_dtype, int sms, int* out6) {
+  if (!out6) return FAR_ERR_NULL;
+  return far::plan_gemm_for_sms(m, n, k, has_bias, out_dtype, sms, out6);
+}
+
+}  // extern "C"

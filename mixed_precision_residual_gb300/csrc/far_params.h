@@ -100,6 +100,10 @@ int check_call(const void* x, const void* r, const void* w, float eps, void* out
 int enqueue_device_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
                         int64_t tokens, int64_t hidden, int dtype, bool residual, cudaStream_t stream);
 
+// the current device's error word and SM count, and a CUDA error as a status (far_api.cu)
+int device_info(unsigned int** status, int* sms);
+int cuda_error_status(cudaError_t e);
+
 // the bounded-wait self test (far_api.cu)
 cudaError_t launch_wait_selftest(unsigned int* status, uint64_t timeout_ns, cudaStream_t stream);
 

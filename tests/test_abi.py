@@ -270,3 +270,35 @@ def test_layernorm_plan_needs_aligned_beta(far):
     for off in (2, 8):
         assert far.plan_ln_for_sms(4096, 4096, B16, B16, True, 152, beta_offset=off)["kind"] == 1
         assert far.plan_ln_for_sms(4096, 4096, B16, B16, False, 152, beta_offset=off)["kind"] == 1
+
+
+def test_gemm_validation(far):
+    """The GEMM's checks, every call rejected before any CUDA call (or a no-op)."""
+    L = far.lib
+    x, wt, b, out = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+    assert L.gemm_f16_f32acc(x, wt, None, out, 4, 8, 16, 7, None) == 2         # unknown out dtype
+    assert L.gemm_f16_f32acc(x, wt, b, out, 4, 8, 16, 0, None) == 2            # a bias with fp32 out
+    assert L.gemm_f16_f32acc(x, wt, None, out, -1, 8, 16, 1, None) == 4
+    assert L.gemm_f16_f32acc(x, wt, None, out, 4, 8, 1 << 31, 1, None) == 4
+    assert L.gemm_f16_f32acc(None, wt, None, out, 4, 8, 16, 1, None) == 3
+    assert L.gemm_f16_f32acc(x, wt, None, None, 4, 8, 16, 1, None) == 3
+    assert L.gemm_f16_f32acc(x, wt, None, x + 8, 4, 8, 16, 1, None) == 5       # out over x
+    assert L.gemm_f16_f32acc(x, wt, b, b - 16, 4, 8, 16, 1, None) == 5         # out over the bias
+    assert L.gemm_f16_f32acc(None, None, None, None, 0, 8, 16, 1, None) == 0   # empty output: no-op
+
+
+def test_gemm_plans(far):
+    """Tensor cores for aligned shapes with k and n multiples of 8, else the plain kernel;
+    the tile width keeps a tile per SM where it can; the shared memory fits."""
+    T16, F32 = torch.float16, torch.float32
+    p = far.plan_gemm_for_sms(1024, 1024, 768, True, T16, 152)
+    assert p["kind"] == 0 and p["bn"] == 64 and p["grid"] == 8 * 16
+    p = far.plan_gemm_for_sms(8192, 8192, 8192, False, F32, 152)
+    assert p["kind"] == 0 and p["bn"] == 256 and p["grid"] == 64 * 32
+    assert far.plan_gemm_for_sms(4096, 2048, 4096, True, T16, 152)["bn"] == 256
+    assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["bn"] == 128  # 8 x 16 tiles of 256 < 152
+    for m, n, k in [(100, 8, 8), (1, 8, 4096), (5000, 1000, 64)]:
+        p = far.plan_gemm_for_sms(m, n, k, True, T16, 152)
+        assert p["kind"] == 0 and p["smem"] <= 227 * 1024 and p["threads"] == 192
+    for m, n, k in [(64, 12, 64), (64, 64, 12), (64, 64, 0), (3, 5, 7)]:
+        assert far.plan_gemm_for_sms(m, n, k, True, T16, 152)["kind"] == 1
