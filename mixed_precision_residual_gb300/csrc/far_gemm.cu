@@ -4,14 +4,17 @@
 // cast to fp16, then the fp16 bias add).  x [M, K] and wt [N, K] are row-major, so both
 // operands are K-major.
 //
-// tc_gemm_kernel -- the tensor-core path.  One 128 x BN output tile per CTA:
+// tc_gemm_kernel -- the tensor-core path.  Persistent: each CTA walks 128 x BN output
+// tiles (grid-stride over an L2-grouped tile order):
 //   warp 0, one lane: TMA producer, a ring of STAGES (A, B) K-slices of 64 values,
-//     128-byte swizzled, completion counted on "full" mbarriers;
-//   warp 1: allocates BN TMEM columns; one lane issues tcgen05.mma (128 x BN x 16, fp16
-//     in, fp32 accumulators in TMEM), releasing each slice with tcgen05.commit on its
-//     "empty" mbarrier and signalling the finished tile on "acc_full";
-//   warps 2..5: epilogue, each reading its 32-lane quarter of TMEM (32 rows), casting
-//     to fp16, adding the bias in fp16 and storing.
+//     128-byte swizzled, completion counted on "full" mbarriers, running across tiles;
+//   warp 1: allocates two accumulators of BN TMEM columns; one lane issues tcgen05.mma
+//     (128 x BN x 16, fp16 in, fp32 accumulators in TMEM), releasing each slice with
+//     tcgen05.commit on its "empty" mbarrier and signalling a finished tile on
+//     "acc_full" of its accumulator;
+//   warps 2..5: epilogue, one tile behind: each reads its 32-lane quarter of TMEM (32
+//     rows), casts to fp16, adds the bias in fp16, stores, and frees its quarter of the
+//     accumulator ("acc_empty"), so a tile's epilogue overlaps the next tile's MMAs.
 //   Every wait is bounded (FAR_ERR_TIMEOUT in the device error word on expiry).
 // generic_gemm_kernel -- any shape or alignment: one thread an output, products and
 //   sums in binary32 in the order of k.
@@ -39,7 +42,8 @@ struct GemmParams {
   const __half* wt;        // generic kernel only
   int32_t M, N, K;
   int32_t out_f32;         // 1: fp32 accumulators, 0: fp16 (+ bias)
-  int32_t tiles_m;
+  int32_t tiles_m, tiles_n, num_tiles;
+  int32_t group_m;         // tile rows per L2 group of the tile order
   unsigned int* status;
   uint64_t timeout_ns;
 };
@@ -55,8 +59,9 @@ struct GemmShape {
   static constexpr uint32_t b_bytes = BN * kGemmBK * 2;
   static constexpr int stages = (BN == 256) ? 4 : (BN == 128) ? 6 : 8;
   static constexpr uint32_t ring_bytes = stages * (a_bytes + b_bytes);
-  // ring (1024-aligned) + barriers (full, empty, acc_full) + TMEM address + alignment slack
-  static constexpr size_t smem_bytes = ring_bytes + (2 * stages + 1) * 8 + 16 + 1024;
+  // ring (1024-aligned) + barriers (full, empty, acc_full x2, acc_empty x2) + TMEM address
+  // + alignment slack
+  static constexpr size_t smem_bytes = ring_bytes + (2 * stages + 4) * 8 + 16 + 1024;
 };
 
 // 32 fp32 accumulators of one row -> 32 outputs at out[row, col0 ..]
@@ -109,6 +114,18 @@ __device__ __forceinline__ void gemm_store32(const GemmParams& p, int64_t row, i
   }
 }
 
+// The t-th output tile in an L2-friendly order: tiles go in groups of `group` tile rows,
+// column-major inside a group, so the CTAs running at one time share A and B panels.
+__host__ __device__ inline void gemm_tile_coords(int t, int tiles_m, int tiles_n, int group, int& tm, int& tn) {
+  const int per_group = group * tiles_n;
+  const int g = t / per_group;
+  const int first_m = g * group;
+  const int gm = (tiles_m - first_m) < group ? (tiles_m - first_m) : group;  // the last group may be narrower
+  const int r = t - g * per_group;
+  tm = first_m + r % gm;
+  tn = r / gm;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -116,6 +133,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   using S = GemmShape<BN>;
   constexpr int STAGES = S::stages;
   constexpr uint32_t IDESC = umma_idesc_f16_f32(kGemmBM, BN);
+  constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators: 128, 256 or 512 columns
   extern __shared__ unsigned char smem_raw[];
   // the 128-byte swizzle wants every tile on a 1024-byte boundary
   const uint32_t raw = smem_addr(smem_raw);
@@ -123,12 +141,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   const uint32_t a_base = sbase, b_base = sbase + STAGES * S::a_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::ring_bytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
   const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
-  const uint32_t acc_full = smem_addr(&bars[2 * STAGES]);
+  const uint32_t acc_full0 = smem_addr(&bars[2 * STAGES]), acc_empty0 = smem_addr(&bars[2 * STAGES + 2]);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tm = blockIdx.x % p.tiles_m, tn = blockIdx.x / p.tiles_m;
   const int num_kb = (p.K + kGemmBK - 1) / kGemmBK;
 
   if (threadIdx.x == 0) {
@@ -136,11 +153,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(full0 + 8 * s, 1);   // the producer's arrive + the bytes
       mbar_init(empty0 + 8 * s, 1);  // one tcgen05.commit
     }
-    mbar_init(acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full0 + 8 * a, 1);   // one tcgen05.commit: the accumulator is final
+      mbar_init(acc_empty0 + 8 * a, 4);  // each epilogue warp has read its quarter
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(tmem_slot), BN);
+    tmem_alloc(smem_addr(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -150,59 +170,85 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer ----------------
+      // ---------------- TMA producer: every slice of every tile of this CTA ----------------
       tma_prefetch_map(&map_a);
       tma_prefetch_map(&map_b);
-      int kb = 0;
-      for (; kb < num_kb; ++kb) {
-        const int s = kb % STAGES;
-        const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, p.timeout_ns, p.status)) break;
-        mbar_arrive_expect_tx(full0 + 8 * s, S::a_bytes + S::b_bytes);
-        tma_load_2d(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, tm * kGemmBM, full0 + 8 * s);
-        tma_load_2d(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
+      uint32_t g = 0;  // slices issued so far
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        int tm, tn;
+        gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const uint32_t s = g % STAGES;
+          if (!mbar_wait(empty0 + 8 * s, ((g / STAGES) & 1u) ^ 1u, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * s, S::a_bytes + S::b_bytes);
+          tma_load_2d(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, tm * kGemmBM, full0 + 8 * s);
+          tma_load_2d(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, tn * BN, full0 + 8 * s);
+        }
       }
       // the copies of the last slices must have landed before the CTA may exit
-      for (int j = (kb > STAGES ? kb - STAGES : 0); j < kb; ++j)
-        mbar_wait(full0 + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u, p.timeout_ns, p.status);
+      for (uint32_t j = (g > (uint32_t)STAGES ? g - STAGES : 0u); j < g; ++j)
+        mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns, p.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % STAGES;
-        if (!mbar_wait(full0 + 8 * s, (uint32_t)(kb / STAGES) & 1u, p.timeout_ns, p.status)) break;
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x, i = 0; t < p.num_tiles && ok; t += gridDim.x, ++i) {
+        const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
+        // the epilogue has drained this accumulator's previous tile
+        if (!mbar_wait(acc_empty0 + 8 * acc, (use & 1u) ^ 1u, p.timeout_ns, p.status)) break;
         tc_fence_after();
-        const uint32_t a = a_base + s * S::a_bytes, b = b_base + s * S::b_bytes;
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const uint32_t s = g % STAGES;
+          if (!mbar_wait(full0 + 8 * s, (g / STAGES) & 1u, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = a_base + s * S::a_bytes, b = b_base + s * S::b_bytes;
 #pragma unroll
-        for (int k = 0; k < kGemmBK / kGemmUK; ++k)
-          umma_f16(tmem, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), IDESC,
-                   (kb | k) != 0);
-        umma_commit(empty0 + 8 * s);  // the slice is free once these MMAs have read it
+          for (int k = 0; k < kGemmBK / kGemmUK; ++k)
+            umma_f16(d, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), IDESC,
+                     (kb | k) != 0);
+          umma_commit(empty0 + 8 * s);  // the slice is free once these MMAs have read it
+        }
+        umma_commit(acc_full0 + 8 * acc);  // the tile's accumulators are final
       }
-      umma_commit(acc_full);  // the tile's accumulators are final
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..5), one tile behind the MMAs ----------------
     const int quarter = warp & 3;  // the TMEM lanes this warp may read: 32 * quarter ..
-    if (mbar_wait(acc_full, 0u, p.timeout_ns, p.status)) {
+    for (int t = blockIdx.x, i = 0; t < p.num_tiles; t += gridDim.x, ++i) {
+      const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
+      if (!mbar_wait(acc_full0 + 8 * acc, use & 1u, p.timeout_ns, p.status)) break;
       tc_fence_after();
+      int tm, tn;
+      gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
       const int64_t row = (int64_t)tm * kGemmBM + quarter * 32 + lane;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, r);
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * BN + (uint32_t)c, r);
         tmem_ld_wait(r);
         const int col0 = tn * BN + c;
         if (col0 < p.N) gemm_store32(p, row, col0, r);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty0 + 8 * acc);  // this quarter of the accumulator is free
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -326,7 +372,7 @@ GemmPlan plan_gemm(const GemmCall& c, int sms) {
     if (tiles <= INT32_MAX) {
       g.kind = 0;
       g.bn = bn;
-      g.grid = (int)tiles;
+      g.grid = (int)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
       g.block = kGemmThreads;
       g.smem = bn == 256 ? GemmShape<256>::smem_bytes : bn == 128 ? GemmShape<128>::smem_bytes
                                                                    : GemmShape<64>::smem_bytes;
@@ -381,6 +427,9 @@ int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t
   p.K = (int32_t)K;
   p.out_f32 = out_dtype == FAR_F32;
   p.tiles_m = (int32_t)((M + kGemmBM - 1) / kGemmBM);
+  p.tiles_n = g.kind == 0 ? (int32_t)((N + g.bn - 1) / g.bn) : 0;
+  p.num_tiles = p.tiles_m * p.tiles_n;
+  p.group_m = 8;
   p.status = status;
   p.timeout_ns = kWaitTimeoutNs;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
