@@ -46,12 +46,14 @@ OP_METRIC = {
     "layernorm": "achieved HBM GB/s and tokens/s of fused add+LayerNorm at 1 GB300 (% of HBM peak)",
     "rmsnorm_int8": "achieved HBM GB/s and tokens/s of fused add+RMSNorm with int8 per-token output at 1 GB300",
     "rmsnorm_fp8": "achieved HBM GB/s and tokens/s of fused add+RMSNorm with FP8 E4M3 per-token output at 1 GB300",
+    "gemm": "achieved TFLOP/s of the fp16-storage / fp32-compute GEMM y = fp16(x @ wt^T) + bias at 1 GB300",
 }
 OP_STEP = {
     "rmsnorm": "fused_add_rmsnorm then rmsnorm on the same x",
     "layernorm": "fused_add_layernorm then layernorm on the same x",
     "rmsnorm_int8": "fused_add_rmsnorm_quant then rmsnorm_quant (int8) on the same x",
     "rmsnorm_fp8": "fused_add_rmsnorm_quant then rmsnorm_quant (FP8 E4M3) on the same x",
+    "gemm": "gemm_f16_f32acc with an fp16 bias and fp16 output",
 }
 WORKLOAD = "c5"
 CSRC = os.path.join(ROOT, "mixed_precision_residual_gb300", "csrc")
@@ -72,6 +74,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=sorted(OP_METRIC), default="rmsnorm")
+    ap.add_argument("--gemm-shape", default="8192x8192x8192", help="M x N x K of the GEMM op")
     return ap.parse_args()
 
 
@@ -279,8 +282,159 @@ def run_reference(args):
     return 0
 
 
+def gemm_shape(args):
+    M, N, K = (int(v) for v in args.gemm_shape.lower().split("x"))
+    return M, N, K
+
+
+def gemm_oracle_sample(d, seconds, threads=None):
+    """The GEMM oracle, as it stands, on the first rows of x (all of N and K): TFLOP/s."""
+    import oracle
+
+    threads = threads or oracle.default_threads()
+    N, K = d["N"], d["K"]
+    rows, t0 = 0, time.perf_counter()
+    step = max(1, threads)
+    while time.perf_counter() - t0 < seconds and rows < d["M"]:
+        oracle.gemm_f16(d["x"][rows:rows + step], d["wt"], d["bias"], "f16", threads=threads)
+        rows += step
+    el = time.perf_counter() - t0
+    return rows, el, threads
+
+
+def run_gemm_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import far_gen
+
+    M, N, K = gemm_shape(args)
+    d = far_gen.gemm_inputs(M, N, K, seed=0)
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        gemm_oracle_sample(d, per_step)
+    total_rows, total_s, threads = 0, 0.0, 1
+    for _ in range(args.steps):
+        rows, el, threads = gemm_oracle_sample(d, per_step)
+        total_rows, total_s = total_rows + rows, total_s + el
+    value = 2.0 * total_rows * N * K / total_s / 1e12
+    sample = f"the first rows of x (all {N} columns, K = {K}) per step, about {per_step:.1f} s each, oracle on {threads} host threads"
+    line = {"impl": "reference", "metric": OP_METRIC["gemm"], "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+            "data": "synthetic (seeded Philox4x32-10 generator)",
+            "config": {"workload": f"gemm {M}x{N}x{K}", "M": M, "N": N, "K": K, "op": "gemm"},
+            "cpu_baseline": {"value": round(value, 8), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gemm_bench(args):
+    """--op gemm: one GEMM launch per step on resident fp16 operands."""
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group(backend="nccl", device_id=torch.device("cuda", local))
+    else:
+        dist = None
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import far_gen
+    import mixed_precision_residual_gb300 as far
+
+    M, N, K = gemm_shape(args)
+    d = far_gen.gemm_inputs(M, N, K, seed=rank)
+    dev = torch.device("cuda", local)
+    x, wt, b = d["x"].to(dev), d["wt"].to(dev), d["bias"].to(dev)
+    out = torch.empty((M, N), dtype=torch.float16, device=dev)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    L = far.lib
+    xp, wp, bp, op = x.data_ptr(), wt.data_ptr(), b.data_ptr(), out.data_ptr()
+    # operands and output are larger than the 129 MB L2 from 4096^3 up; smaller shapes are
+    # flushed by a read sweep of a 512 MB buffer before each step (outside the kernel's events)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    needs_flush = (M * K + N * K + M * N) * 2 < 3 * (129 << 20)
+
+    def step():
+        if L.gemm_f16_f32acc(xp, wp, bp, op, M, N, K, 1, sh):
+            raise RuntimeError("gemm launch failed")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert far.device_status() == 0
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        if needs_flush:
+            flush.sum()
+        ev0[k].record(stream)
+        step()
+        ev1[k].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    if far.device_status() != 0:
+        raise RuntimeError("device status after the timed region")
+    kernel_ms = sum(a.elapsed_time(c) for a, c in zip(ev0, ev1)) / args.steps
+    kernel_ms = max_over_ranks(kernel_ms, dist, dev)
+    flops = 2.0 * M * N * K
+    value = flops * world / (kernel_ms * 1e-3) / 1e12
+    peaks = {}
+    if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")):
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    plan = far.plan_gemm_for_sms(M, N, K, True, torch.float16, torch.cuda.get_device_properties(dev).multi_processor_count)
+    line = {
+        "metric": OP_METRIC["gemm"], "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(kernel_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded Philox4x32-10 generator)",
+        "config": {"workload": f"gemm {M}x{N}x{K}", "M": M, "N": N, "K": K, "op": "gemm",
+                   "l2": "flushed by a read sweep before each step" if needs_flush else
+                         "no flush: operands and output exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "tensor", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / peak, 4), "traffic": None,
+                     "kernel": "tc_gemm_kernel", "peak_source": "measured bf16_tflops (fp16 runs at the bf16 tensor rate)",
+                     "algorithmic_flops_per_launch": flops, "avg_launch_ms": round(kernel_ms, 5), "launch_plan": plan},
+        "clocks": clk,
+        "e2e": None,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        rows, el, threads = gemm_oracle_sample(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(2.0 * rows * N * K / el / 1e12, 8), "unit": "TFLOP/s", "cores": threads,
+                                "kind": "oracle", "seconds": round(el, 2),
+                                "sample": f"the first {rows} rows of x (all {N} columns, K = {K}), oracle on {threads} host threads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.op == "gemm":
+        return run_gemm_reference(args) if args.impl == "reference" else run_gemm_bench(args)
     if args.impl == "reference":
         return run_reference(args)
     rank, world, local = dist_env()

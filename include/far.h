@@ -187,10 +187,12 @@ int gemm_f16_f32acc(const void* x, const void* wt, const void* bias, void* out, 
                     int out_dtype, void* stream);
 
 /* the GEMM's plan for a device with `sms` SMs (host logic only, aligned operands):
-   out6 = {kind (0 tensor cores, 1 plain), tile width, grid, threads, dynamic shared bytes, stages} */
+   out6 = {kind (0 tensor cores, 1 plain, 2 tensor cores over CTA pairs), tile width, grid, threads,
+   dynamic shared bytes, stages} */
 int far_plan_gemm_for_sms(int64_t m, int64_t n, int64_t k, int has_bias, int out_dtype, int sms, int* out6);
 /* process-wide override of the GEMM plan, for measurements and tests: kind -1 automatic,
-   0 tensor cores where feasible, 1 the plain kernel; bn 0 automatic, else 64, 128 or 256 */
+   0 tensor cores, one CTA a tile, where feasible; 1 the plain kernel; 2 tensor cores over CTA
+   pairs (256 x 256 tiles) where feasible; bn 0 automatic, else 64, 128 or 256 (kind 0) */
 int far_set_gemm_override(int kind, int bn);
 
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */

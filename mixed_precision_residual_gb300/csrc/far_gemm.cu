@@ -252,6 +252,156 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// CTA pairs: 256 x 256 output tiles over a cluster of 2.  Each CTA holds its 128 rows of
+// A and half (128 rows) of B per K-slice; one thread of the even CTA issues
+// tcgen05.mma.cta_group::2 (256 x 256 x 16) over both CTAs' tensor cores, each CTA's TMEM
+// receiving its 128 rows of the tile.  Per SM a slice is 32 KB for the same MMA time as
+// the single-CTA 128 x 256 tile's 48 KB.
+//   - both producers wait on their own "empty" barriers (the MMA's commit is multicast to
+//     both CTAs) and load into their own shared memory, counting the bytes on the even
+//     CTA's "full" barrier, which expects both CTAs' bytes;
+//   - "acc_full" commits are multicast; both CTAs' epilogues free the accumulator on the
+//     even CTA's "acc_empty" (8 arrivals: 4 warps x 2 CTAs).
+// ---------------------------------------------------------------------------
+struct PairShape {
+  static constexpr int BM = 256, BN = 256;             // the pair's output tile
+  static constexpr uint32_t a_bytes = 128 * kGemmBK * 2;  // this CTA's rows of A
+  static constexpr uint32_t b_bytes = 128 * kGemmBK * 2;  // this CTA's half of B
+  static constexpr int stages = 6;
+  static constexpr uint32_t ring_bytes = stages * (a_bytes + b_bytes);
+  static constexpr size_t smem_bytes = ring_bytes + (2 * stages + 4) * 8 + 16 + 1024;
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                    const GemmParams p) {
+  using S = PairShape;
+  constexpr int STAGES = S::stages;
+  constexpr uint32_t IDESC = umma_idesc_f16_f32(S::BM, S::BN);
+  constexpr uint32_t TMEM_COLS = 2 * S::BN;  // two accumulators of 256 columns
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);  // the same offset in both CTAs
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t a_base = sbase, b_base = sbase + STAGES * S::a_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::ring_bytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  const uint32_t full0 = smem_addr(&bars[0]), empty0 = smem_addr(&bars[STAGES]);
+  const uint32_t acc_full0 = smem_addr(&bars[2 * STAGES]), acc_empty0 = smem_addr(&bars[2 * STAGES + 2]);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_cta_rank();
+  const int pair = (int)(blockIdx.x >> 1), num_pairs = (int)(gridDim.x >> 1);
+  const int num_kb = (p.K + kGemmBK - 1) / kGemmBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);   // even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(empty0 + 8 * s, 1);  // one multicast commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full0 + 8 * a, 1);   // one multicast commit
+      mbar_init(acc_empty0 + 8 * a, 8);  // even CTA: 4 epilogue warps in each CTA
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_addr(tmem_slot), TMEM_COLS);  // one warp in each CTA, the same columns
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or copy
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = pair; t < p.num_tiles && ok; t += num_pairs) {
+        int tm, tn;
+        gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const uint32_t s = g % STAGES;
+          if (!mbar_wait(empty0 + 8 * s, ((g / STAGES) & 1u) ^ 1u, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * (S::a_bytes + S::b_bytes));
+          const uint32_t full_even = map_to_cta(full0 + 8 * s, 0);
+          tma_load_2d_pair(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, tm * S::BM + (int)rank * 128, full_even);
+          tma_load_2d_pair(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, tn * S::BN + (int)rank * 128, full_even);
+        }
+      }
+      if (rank == 0) {  // the pair's copies of the last slices must have landed before exit
+        for (uint32_t j = (g > (uint32_t)STAGES ? g - STAGES : 0u); j < g; ++j)
+          mbar_wait(full0 + 8 * (j % STAGES), (j / STAGES) & 1u, p.timeout_ns, p.status);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA) ----------------
+      uint32_t g = 0;
+      bool ok = true;
+      for (int t = pair, i = 0; t < p.num_tiles && ok; t += num_pairs, ++i) {
+        const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
+        if (!mbar_wait_cluster(acc_empty0 + 8 * acc, (use & 1u) ^ 1u, p.timeout_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * S::BN;
+        for (int kb = 0; kb < num_kb; ++kb, ++g) {
+          const uint32_t s = g % STAGES;
+          if (!mbar_wait(full0 + 8 * s, (g / STAGES) & 1u, p.timeout_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = a_base + s * S::a_bytes, b = b_base + s * S::b_bytes;
+#pragma unroll
+          for (int k = 0; k < kGemmBK / kGemmUK; ++k)
+            umma_f16_pair(d, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), IDESC,
+                          (kb | k) != 0);
+          umma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs' slots are free once read
+        }
+        umma_commit_pair(acc_full0 + 8 * acc, 0x3);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
+    const int quarter = warp & 3;
+    for (int t = pair, i = 0; t < p.num_tiles; t += num_pairs, ++i) {
+      const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
+      if (!mbar_wait(acc_full0 + 8 * acc, use & 1u, p.timeout_ns, p.status)) break;
+      tc_fence_after();
+      int tm, tn;
+      gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      const int64_t row = (int64_t)tm * S::BM + (int)rank * 128 + quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < S::BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * S::BN + (uint32_t)c, r);
+        tmem_ld_wait(r);
+        const int col0 = tn * S::BN + c;
+        if (col0 < p.N) gemm_store32(p, row, col0, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(acc_empty0 + 8 * acc, 0));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, TMEM_COLS);
+  }
+}
+
 // any shape, any alignment: out[m, n] = sum_k x[m, k] * wt[n, k] in binary32 (each product
 // of two fp16 values is exact), then the cast and the fp16 bias add
 __global__ void __launch_bounds__(256) generic_gemm_kernel(const GemmParams p) {
@@ -345,21 +495,35 @@ int validate_gemm(const GemmCall& c) {
 }
 
 struct GemmPlan {
-  int kind;   // 0 tensor cores, 1 generic
+  int kind;   // 0 tensor cores (one CTA a tile), 1 generic, 2 tensor cores over CTA pairs
   int bn;     // tile width
   int grid, block;
   size_t smem;
 };
 
 // tensor cores when TMA can read both operands (16-byte aligned rows and bases) and the
-// vector epilogue can write (N a multiple of 8, 16-byte aligned out and bias); the tile
-// width is the widest that still gives at least one tile per SM, else 64
-GemmPlan plan_gemm(const GemmCall& c, int sms) {
+// vector epilogue can write (N a multiple of 8, 16-byte aligned out and bias).  256 x 256
+// tiles over CTA pairs when there are enough of them to occupy every pair of SMs
+// (`max_pairs` clusters resident at once); else one CTA a tile, the widest tile width that
+// still gives a tile per SM, else 64.
+GemmPlan plan_gemm(const GemmCall& c, int sms, int max_pairs) {
   GemmPlan g{1, 0, 1, 256, 0};
   const bool tc = c.K > 0 && c.K % 8 == 0 && c.N % 8 == 0 && al16(c.x) && al16(c.wt) && al16(c.out) &&
                   (!c.bias || al16(c.bias));
   const int64_t tiles_m = (c.M + kGemmBM - 1) / kGemmBM;
-  if (tc && g_gemm_force_kind.load() != 1) {
+  const int force = g_gemm_force_kind.load();
+  if (tc && max_pairs > 0 && (force == 2 || (force == -1 && g_gemm_force_bn.load() == 0))) {
+    const int64_t pair_tiles = ((c.M + PairShape::BM - 1) / PairShape::BM) * ((c.N + PairShape::BN - 1) / PairShape::BN);
+    if (pair_tiles <= INT32_MAX && (force == 2 || pair_tiles >= max_pairs)) {
+      g.kind = 2;
+      g.bn = PairShape::BN;
+      g.grid = 2 * (int)(pair_tiles < max_pairs ? pair_tiles : max_pairs);
+      g.block = kGemmThreads;
+      g.smem = PairShape::smem_bytes;
+      return g;
+    }
+  }
+  if (tc && force != 1) {
     int bn = 64;
     for (int cand : {256, 128}) {
       if (tiles_m * ((c.N + cand - 1) / cand) >= sms) {
@@ -383,6 +547,39 @@ GemmPlan plan_gemm(const GemmCall& c, int sms) {
   const int64_t blocks = (total + 255) / 256;
   g.grid = (int)(blocks < (int64_t)sms * 16 ? blocks : (int64_t)sms * 16);
   return g;
+}
+
+// clusters of two pair CTAs that fit on the device at once (0 if none)
+int max_active_pairs() {
+  static std::mutex mu;
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached_dev != dev) {
+    cached = 0;
+    if (cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PairShape::smem_bytes) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(kGemmThreads, 1, 1);
+      cfg.dynamicSmemBytes = PairShape::smem_bytes;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 2;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc2_gemm_kernel, &cfg) == cudaSuccess) cached = n;
+      else cudaGetLastError();  // leave no sticky error behind
+    } else {
+      cudaGetLastError();
+    }
+    cached_dev = dev;
+  }
+  return cached;
 }
 
 template <int BN>
@@ -416,7 +613,7 @@ int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t
   int sms = 0;
   st = device_info(&status, &sms);
   if (st != FAR_OK) return st;
-  const GemmPlan g = plan_gemm(c, sms);
+  const GemmPlan g = plan_gemm(c, sms, max_active_pairs());
   GemmParams p{};
   p.out = out;
   p.bias = static_cast<const __half*>(bias);
@@ -426,8 +623,9 @@ int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t
   p.N = (int32_t)N;
   p.K = (int32_t)K;
   p.out_f32 = out_dtype == FAR_F32;
-  p.tiles_m = (int32_t)((M + kGemmBM - 1) / kGemmBM);
-  p.tiles_n = g.kind == 0 ? (int32_t)((N + g.bn - 1) / g.bn) : 0;
+  const int tile_rows = g.kind == 2 ? PairShape::BM : kGemmBM;
+  p.tiles_m = (int32_t)((M + tile_rows - 1) / tile_rows);
+  p.tiles_n = g.kind != 1 ? (int32_t)((N + g.bn - 1) / g.bn) : 0;
   p.num_tiles = p.tiles_m * p.tiles_n;
   p.group_m = 8;
   p.status = status;
@@ -442,6 +640,13 @@ int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t
     e = g.bn == 256 ? launch_tc<256>(ma, mb, p, g, s)
         : g.bn == 128 ? launch_tc<128>(ma, mb, p, g, s)
                       : launch_tc<64>(ma, mb, p, g, s);
+  } else if (g.kind == 2) {
+    CUtensorMap ma, mb;  // each CTA of a pair loads 128 rows of A and 128 rows (half the tile) of B
+    st = encode_kmajor(&ma, x, M, K, 128);
+    if (st == FAR_OK) st = encode_kmajor(&mb, wt, N, K, 128);
+    if (st != FAR_OK) return st;
+    tc2_gemm_kernel<<<g.grid, g.block, g.smem, s>>>(ma, mb, p);  // the attribute was set by max_active_pairs
+    e = cudaGetLastError();
   } else {
     generic_gemm_kernel<<<g.grid, g.block, 0, s>>>(p);
     e = cudaGetLastError();
@@ -457,8 +662,9 @@ int plan_gemm_for_sms(int64_t M, int64_t N, int64_t K, int has_bias, int out_dty
   int st = validate_gemm(c);
   if (st != FAR_OK) return st;
   if (M == 0 || N == 0 || sms < 1) return FAR_ERR_SHAPE;
-  const GemmPlan g = plan_gemm(c, sms);
-  int v[6] = {g.kind, g.bn, g.grid, g.block, (int)g.smem, g.kind == 0 ? (g.bn == 256 ? 4 : g.bn == 128 ? 6 : 8) : 0};
+  const GemmPlan g = plan_gemm(c, sms, sms / 2);  // host logic: every SM pair can hold a cluster
+  int v[6] = {g.kind, g.bn, g.grid, g.block, (int)g.smem,
+              g.kind == 2 ? PairShape::stages : g.kind == 0 ? (g.bn == 256 ? 4 : g.bn == 128 ? 6 : 8) : 0};
   for (int i = 0; i < 6; ++i) out6[i] = v[i];
   return FAR_OK;
 }
@@ -473,7 +679,7 @@ int gemm_f16_f32acc(const void* x, const void* wt, const void* bias, void* out, 
 }
 
 int far_set_gemm_override(int kind, int bn) {
-  if (kind < -1 || kind > 1 || (bn != 0 && bn != 64 && bn != 128 && bn != 256)) return FAR_ERR_SHAPE;
+  if (kind < -1 || kind > 2 || (bn != 0 && bn != 64 && bn != 128 && bn != 256)) return FAR_ERR_SHAPE;
   far::g_gemm_force_kind = kind;
   far::g_gemm_force_bn = bn;
   return FAR_OK;

@@ -294,11 +294,12 @@ def test_gemm_plans(far):
     p = far.plan_gemm_for_sms(1024, 1024, 768, True, T16, 152)
     assert p["kind"] == 0 and p["bn"] == 64 and p["grid"] == 8 * 16
     p = far.plan_gemm_for_sms(8192, 8192, 8192, False, F32, 152)
-    assert p["kind"] == 0 and p["bn"] == 256 and p["grid"] == 152  # persistent: one CTA per SM
+    assert p["kind"] == 2 and p["bn"] == 256 and p["grid"] == 152  # CTA pairs, one CTA per SM
     assert far.plan_gemm_for_sms(4096, 2048, 4096, True, T16, 152)["bn"] == 256
     assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["bn"] == 128  # 8 x 16 tiles of 256 < 152
     for m, n, k in [(100, 8, 8), (1, 8, 4096), (5000, 1000, 64)]:
         p = far.plan_gemm_for_sms(m, n, k, True, T16, 152)
-        assert p["kind"] == 0 and p["smem"] <= 227 * 1024 and p["threads"] == 192
+        assert p["kind"] in (0, 2) and p["smem"] <= 227 * 1024 and p["threads"] == 192
+        assert p["grid"] % 2 == 0 or p["kind"] == 0  # pairs launch whole clusters
     for m, n, k in [(64, 12, 64), (64, 64, 12), (64, 64, 0), (3, 5, 7)]:
         assert far.plan_gemm_for_sms(m, n, k, True, T16, 152)["kind"] == 1

@@ -110,14 +110,25 @@ def test_page_shape(far):
     check_all(far, far_gen.gemm_inputs(1024, 1024, 768, seed=1), "1024x1024x768")
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 136), (257, 520, 1000), (1, 8, 8), (128, 64, 4096)])
+def force(far, bn):
+    """The plan under test: a single-CTA tile width, "pair" (256 x 256 over CTA pairs) or "plain"."""
+    if bn == "pair":
+        far.set_gemm_override(2, 0)
+    elif bn == "plain":
+        far.set_gemm_override(1, 0)
+    else:
+        far.set_gemm_override(0, bn)
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256, "pair"])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 200, 136), (257, 520, 1000), (1, 8, 8), (128, 64, 4096),
+                                   (768, 768, 512)])
 def test_tiles_and_tails(far, bn, M, N, K):
     """Every tile width on full tiles and ragged tails in M, N and K, a single row and
-    a long K (the slice ring wraps many times)."""
+    a long K (the slice ring wraps many times); several tiles per CTA."""
     d = far_gen.gemm_inputs(M, N, K, seed=M + N + K)
     try:
-        far.set_gemm_override(0, bn)
+        force(far, bn)
         check_all(far, d, f"bn={bn} {M}x{N}x{K}")
     finally:
         far.set_gemm_override()
@@ -195,13 +206,14 @@ def check_exact(far, d, where):
         assert torch.equal(got.view(ib), ref.view(ib)), f"{where} bias={bias} {dt}: not bit for bit"
 
 
-@pytest.mark.parametrize("bn", [64, 128, 256, "plain"])
-@pytest.mark.parametrize("M,N,K", [(1024, 1024, 768), (300, 200, 136), (257, 520, 1000), (129, 72, 8)])
+@pytest.mark.parametrize("bn", [64, 128, 256, "pair", "plain"])
+@pytest.mark.parametrize("M,N,K", [(1024, 1024, 768), (300, 200, 136), (257, 520, 1000), (129, 72, 8),
+                                   (2048, 1536, 256)])
 def test_dyadic_bit_exact(far, bn, M, N, K):
     """Exact sums: the cast, the bias after the cast, the indexing and every tail bit for bit."""
     d = far_gen.gemm_dyadic_inputs(M, N, K, seed=M * 7 + K)
     try:
-        far.set_gemm_override(1, 0) if bn == "plain" else far.set_gemm_override(0, bn)
+        force(far, bn)
         check_exact(far, d, f"dyadic bn={bn} {M}x{N}x{K}")
     finally:
         far.set_gemm_override()
@@ -218,3 +230,10 @@ def test_bias_after_cast_fixture(far):
     d = {"x": x, "wt": wt, "bias": torch.full((64,), 2.0 ** -11, dtype=torch.float16), "M": 128, "N": 64, "K": K}
     y = run_gemm(far, d, bias=True)
     assert bool((y == 1.0).all()), "the bias must be added after the fp16 cast"
+
+
+def test_default_plan_uses_pairs_when_tiles_abound(far):
+    """A large GEMM takes the CTA-pair path by default (the device holds pairs) and matches."""
+    assert far.plan_gemm_for_sms(4096, 4096, 512, True, torch.float16, 152)["kind"] == 2
+    d = far_gen.gemm_dyadic_inputs(4096, 4096, 512, seed=9)
+    check_exact(far, d, "default plan 4096x4096x512")
