@@ -1,6 +1,6 @@
 """The large workloads at full size, in the launch configuration the bench times.
 
-The fp16 65536 x 8192 workload is compared with the oracle on sampled rows
+The fp16 65536 x 8192 workload (RMSNorm and LayerNorm) is compared with the oracle on sampled rows
 (first, last and spread rows) and its residual_out on every element (a
 property that holds at any size: RNE_act(fl32(x + r)), rebuilt with torch's
 binary32 add and RNE cast); the bf16 16384 x 5120 workload is compared with
@@ -63,3 +63,45 @@ def test_f16_65536x8192_sampled_rows(far):
     ref_out, ref_res = oracle.fused_add_rmsnorm(x, r, d["w"], d["eps"], "f16", "f16")
     gate(out[idx], ref_out, res[idx], ref_res, "c5 fused (sampled rows)")
     gate(nout[idx], oracle.rmsnorm(x, d["w"], d["eps"], "f16", "f16"), where="c5 rmsnorm (sampled rows)")
+
+
+def test_layernorm_f16_65536x8192_sampled_rows(far):
+    """LayerNorm on the same workload in the bench's launch plans, sampled rows."""
+    d = far_gen.make_inputs("c5")
+    b = far_gen.ln_beta(d)
+    x, r, w, bb = d["x"].cuda(), d["r"].cuda(), d["w"].cuda(), b.cuda()
+    out, res = far.fused_add_layernorm(x, r, w, bb, d["eps"])
+    nout = far.layernorm(x, w, bb, d["eps"])
+    assert far.device_status() == 0
+    out, res, nout = out.cpu(), res.cpu(), nout.cpu()
+    rng = np.random.default_rng(1)
+    rows = np.unique(np.concatenate([np.arange(0, 32), np.arange(d["tokens"] - 32, d["tokens"]),
+                                     rng.choice(d["tokens"], 960, replace=False)]))
+    idx = torch.from_numpy(rows)
+    xs, rs = d["x"][idx].contiguous(), d["r"][idx].contiguous()
+    ref_out, ref_res = oracle.fused_add_layernorm(xs, rs, d["w"], b, d["eps"], "f16", "f16")
+    gate(out[idx], ref_out, res[idx], ref_res, "c5 layernorm fused (sampled rows)")
+    gate(nout[idx], oracle.layernorm(xs, d["w"], b, d["eps"], "f16", "f16"), where="c5 layernorm (sampled rows)")
+
+
+def test_gemm_8192_cubed_sampled_rows(far):
+    """The GEMM at the bench's shape and plan (256 x 256 tiles over CTA pairs): on dyadic
+    operands (every binary32 sum exact) sampled rows bit for bit; on random operands the
+    page's tolerance."""
+    M = N = K = 8192
+    far.set_gemm_override()
+    assert far.plan_gemm_for_sms(M, N, K, True, torch.float16, 152)["kind"] == 2
+    rng = np.random.default_rng(2)
+    rows = np.unique(np.concatenate([[0, 127, 128, 255, 256, M - 1], rng.choice(M, 26, replace=False)]))
+    idx = torch.from_numpy(rows)
+    g = far_gen.gemm_dyadic_inputs(M, N, K, seed=3)
+    y = far.gemm_f16_f32acc(g["x"].cuda(), g["wt"].cuda(), g["bias"].cuda())
+    assert far.device_status() == 0
+    ref = oracle.gemm_f16(g["x"][idx].contiguous(), g["wt"], g["bias"], "f16")
+    assert torch.equal(y.cpu()[idx].view(torch.int16), ref.view(torch.int16)), "dyadic rows differ"
+    g = far_gen.gemm_inputs(M, N, K, seed=4)
+    y = far.gemm_f16_f32acc(g["x"].cuda(), g["wt"].cuda(), g["bias"].cuda())
+    assert far.device_status() == 0
+    ref = oracle.gemm_f16(g["x"][idx[:8]].contiguous(), g["wt"], g["bias"], "f16").double().numpy()
+    got = y.cpu()[idx[:8]].double().numpy()
+    assert np.isfinite(got).all() and (np.abs(got - ref) <= 2e-4 + 2e-3 * np.abs(ref)).all()
