@@ -253,7 +253,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// CTA pairs: 256 x 256 output tiles over a cluster of 2.  Each CTA holds its 128 rows of
+// CTA pairs: 256 x 256 output tiles over a cluster of 2 (the last, partial wave in
+// 256 x 128 halves).  Each CTA holds its 128 rows of
 // A and half (128 rows) of B per K-slice; one thread of the even CTA issues
 // tcgen05.mma.cta_group::2 (256 x 256 x 16) over both CTAs' tensor cores, each CTA's TMEM
 // receiving its 128 rows of the tile.  Per SM a slice is 32 KB for the same MMA time as
@@ -273,12 +274,40 @@ struct PairShape {
   static constexpr size_t smem_bytes = ring_bytes + (2 * stages + 4) * 8 + 16 + 1024;
 };
 
+// A pair's k-th work item: whole 256 x 256 tiles for the full waves, then the tiles of the
+// last, partial wave split into two 256 x 128 halves, so that wave costs half as long.
+// False past the end of the pair's list.
+struct PairWork {
+  int tm, tn;
+  int col0;   // first output column
+  int ncols;  // 256, or 128 for a half tile
+};
+__device__ __forceinline__ bool pair_work(const GemmParams& p, int pair, int num_pairs, int k, PairWork& w) {
+  const int waves = p.num_tiles / num_pairs;
+  const int rest = p.num_tiles - waves * num_pairs;
+  int t, hsel = 0;
+  if (k < waves) {
+    t = pair + k * num_pairs;
+    w.ncols = PairShape::BN;
+  } else {
+    const int h = pair + (k - waves) * num_pairs;
+    if (h >= 2 * rest) return false;
+    t = waves * num_pairs + (h >> 1);
+    hsel = h & 1;
+    w.ncols = PairShape::BN / 2;
+  }
+  gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, w.tm, w.tn);
+  w.col0 = w.tn * PairShape::BN + hsel * (PairShape::BN / 2);
+  return true;
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                     const GemmParams p) {
   using S = PairShape;
   constexpr int STAGES = S::stages;
   constexpr uint32_t IDESC = umma_idesc_f16_f32(S::BM, S::BN);
+  constexpr uint32_t IDESC_HALF = umma_idesc_f16_f32(S::BM, S::BN / 2);
   constexpr uint32_t TMEM_COLS = 2 * S::BN;  // two accumulators of 256 columns
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -323,9 +352,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       tma_prefetch_map(&map_b);
       uint32_t g = 0;
       bool ok = true;
-      for (int t = pair; t < p.num_tiles && ok; t += num_pairs) {
-        int tm, tn;
-        gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      PairWork w;
+      for (int item = 0; ok && pair_work(p, pair, num_pairs, item, w); ++item) {
+        // this CTA's rows of B: its half of the tile's columns (a 128-row box; a half tile
+        // uses the first 64 rows of it)
+        const int b_row = w.col0 + (int)rank * (w.ncols / 2);
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const uint32_t s = g % STAGES;
           if (!mbar_wait(empty0 + 8 * s, ((g / STAGES) & 1u) ^ 1u, p.timeout_ns, p.status)) {
@@ -334,8 +365,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * (S::a_bytes + S::b_bytes));
           const uint32_t full_even = map_to_cta(full0 + 8 * s, 0);
-          tma_load_2d_pair(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, tm * S::BM + (int)rank * 128, full_even);
-          tma_load_2d_pair(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, tn * S::BN + (int)rank * 128, full_even);
+          tma_load_2d_pair(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, w.tm * S::BM + (int)rank * 128, full_even);
+          tma_load_2d_pair(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, b_row, full_even);
         }
       }
       if (rank == 0) {  // the pair's copies of the last slices must have landed before exit
@@ -348,11 +379,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // ---------------- MMA issuer (even CTA) ----------------
       uint32_t g = 0;
       bool ok = true;
-      for (int t = pair, i = 0; t < p.num_tiles && ok; t += num_pairs, ++i) {
+      PairWork w;
+      for (int i = 0; ok && pair_work(p, pair, num_pairs, i, w); ++i) {
         const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
         if (!mbar_wait_cluster(acc_empty0 + 8 * acc, (use & 1u) ^ 1u, p.timeout_ns, p.status)) break;
         tc_fence_after();
         const uint32_t d = tmem + acc * S::BN;
+        const uint32_t idesc = w.ncols == S::BN ? IDESC : IDESC_HALF;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const uint32_t s = g % STAGES;
           if (!mbar_wait(full0 + 8 * s, (g / STAGES) & 1u, p.timeout_ns, p.status)) {
@@ -363,7 +396,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t a = a_base + s * S::a_bytes, b = b_base + s * S::b_bytes;
 #pragma unroll
           for (int k = 0; k < kGemmBK / kGemmUK; ++k)
-            umma_f16_pair(d, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), IDESC,
+            umma_f16_pair(d, sw128_kmajor_desc(a + k * kGemmUK * 2), sw128_kmajor_desc(b + k * kGemmUK * 2), idesc,
                           (kb | k) != 0);
           umma_commit_pair(empty0 + 8 * s, 0x3);  // both CTAs' slots are free once read
         }
@@ -373,19 +406,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   } else {
     // ---------------- epilogue (warps 2..5 of both CTAs) ----------------
     const int quarter = warp & 3;
-    for (int t = pair, i = 0; t < p.num_tiles; t += num_pairs, ++i) {
+    PairWork w;
+    for (int i = 0; pair_work(p, pair, num_pairs, i, w); ++i) {
       const uint32_t acc = (uint32_t)i & 1u, use = (uint32_t)i >> 1;
       if (!mbar_wait(acc_full0 + 8 * acc, use & 1u, p.timeout_ns, p.status)) break;
       tc_fence_after();
-      int tm, tn;
-      gemm_tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-      const int64_t row = (int64_t)tm * S::BM + (int)rank * 128 + quarter * 32 + lane;
+      const int64_t row = (int64_t)w.tm * S::BM + (int)rank * 128 + quarter * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < S::BN; c += 32) {
+      for (int c = 0; c < w.ncols; c += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + acc * S::BN + (uint32_t)c, r);
         tmem_ld_wait(r);
-        const int col0 = tn * S::BN + c;
+        const int col0 = w.col0 + c;
         if (col0 < p.N) gemm_store32(p, row, col0, r);
       }
       tc_fence_before();
