@@ -71,6 +71,7 @@ def parse_args():
     ap.add_argument("--tokens", type=int, default=0,
                     help="time only the first N rows of the workload (profiling captures)")
     ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-chunk", type=int, default=4096, help="rows per chunk of the host-buffer pipeline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=sorted(OP_METRIC), default="rmsnorm")
@@ -544,7 +545,7 @@ def main():
         oh = torch.empty(x.shape, dtype=od, pin_memory=True)
         roh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
         o2h = torch.empty(x.shape, dtype=od, pin_memory=True)
-        chunk = 4096
+        chunk = args.e2e_chunk
         ws = torch.empty(far.host_workspace_bytes(chunk, H, x.dtype, wt.dtype, True), dtype=torch.uint8, device=dev)
         wsb = ws.numel()
         def e2e_step():
@@ -570,7 +571,7 @@ def main():
         e2e = {"value": round(job_rate(fb + nb, world, e2e_ms) / 1e9, 3), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                "tokens_per_s": round(job_rate(T, world, e2e_ms), 1),
-               "path": "fused_add_rmsnorm_host + rmsnorm_host (pinned host buffers, 4096-row chunks, "
+               "path": f"fused_add_rmsnorm_host + rmsnorm_host (pinned host buffers, {chunk}-row chunks, "
                        "two internal streams)"}
         assert far.device_status() == 0
 
