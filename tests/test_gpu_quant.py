@@ -120,3 +120,40 @@ def test_quant_rejections(far):
     st = far.lib.rmsnorm_quant(x.data_ptr(), w.data_ptr(), 1e-6, x.data_ptr(), scale.data_ptr(), 4, 64,
                                far.dtypes(x.dtype, w.dtype), 1, torch.cuda.current_stream().cuda_stream)
     assert st == 5  # q over x
+
+
+def _quantise_given_out(out, qtype, L):
+    """The quantisation step alone, applied to given out values the way the oracle takes
+    it: amax per row, scale = fl32(amax / QMAX), inv = fl32(QMAX / amax) (0 for a zero
+    row), codes = Q(fl32(out * inv)) by the oracle's pinned converters; binary32 steps
+    by numpy's IEEE float32 arithmetic."""
+    o = out.float().numpy()
+    qmax = np.float32(127.0 if qtype == "int8" else 448.0)
+    amax = np.max(np.abs(o), axis=1).astype(np.float32)
+    scale = (amax / qmax).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        inv = np.where(amax == 0, np.float32(0), qmax / amax).astype(np.float32)
+    v = (o * inv[:, None]).astype(np.float32)
+    conv = L.oracle_f32_to_int8 if qtype == "int8" else L.oracle_f32_to_e4m3
+    codes = np.array([conv(float(t)) for t in v.ravel()], dtype=np.int64).reshape(v.shape)
+    return codes, scale
+
+
+@pytest.mark.parametrize("act,wd,hidden", [("bf16", "bf16", 4096), ("f16", "f16", 8192), ("f32", "f32", 2048),
+                                           ("bf16", "f32", 5120), ("f16", "f16", 1000)])
+def test_quantisation_bit_exact_given_out(far, act, wd, hidden):
+    """Where floating point decides the integer codes, both sides decide from the same
+    values: the GPU's own out (from the plain kernel, same arithmetic) quantised by the
+    oracle's steps must equal the quantised kernel's codes and scales bit for bit."""
+    L = oracle.lib()
+    d = far_gen.custom_inputs(act, wd, 48, hidden, seed=hidden + 3, scale_lo=1e-2, scale_hi=50)
+    x, r, w = d["x"].cuda(), d["r"].cuda(), d["w"].cuda()
+    for residual in (True, False):
+        out = far.fused_add_rmsnorm(x, r, w, d["eps"])[0] if residual else far.rmsnorm(x, w, d["eps"])
+        assert far.device_status() == 0
+        for qtype in ("int8", "fp8"):
+            q, scale, _ = run_quant(far, d, qtype, residual)
+            codes, want_scale = _quantise_given_out(out.cpu(), qtype, L)
+            got = q.numpy().astype(np.int64) if qtype == "int8" else q.view(torch.uint8).numpy().astype(np.int64)
+            assert np.array_equal(scale.numpy().view(np.uint32), want_scale.view(np.uint32)), (qtype, residual)
+            assert np.array_equal(got, codes), f"{act}/{wd} H={hidden} {qtype} residual={residual}: codes differ"
