@@ -195,6 +195,28 @@ int far_plan_gemm_for_sms(int64_t m, int64_t n, int64_t k, int has_bias, int out
    pairs (256 x 256 tiles) where feasible; bn 0 automatic, else 64, 128 or 256 (kind 0) */
 int far_set_gemm_override(int kind, int bn);
 
+/*
+ * Strided forms of LayerNorm and of the quantised output: as fused_add_rmsnorm_strided,
+ * each activation tensor has its own row stride in elements (>= hidden; elements within a
+ * row contiguous); an output may be exactly its input, no other byte may be shared.  q
+ * and scale stay contiguous ([tokens, hidden] bytes and [tokens] binary32).
+ */
+int fused_add_layernorm_strided(const void* x, int64_t x_row_stride, const void* residual,
+                                int64_t residual_row_stride, const void* gamma, const void* beta, float eps, void* out,
+                                int64_t out_row_stride, void* residual_out, int64_t residual_out_row_stride,
+                                int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+int layernorm_strided(const void* x, int64_t x_row_stride, const void* gamma, const void* beta, float eps, void* out,
+                      int64_t out_row_stride, int64_t tokens, int64_t hidden, int dtype, void* stream);
+
+int fused_add_rmsnorm_quant_strided(const void* x, int64_t x_row_stride, const void* residual,
+                                    int64_t residual_row_stride, const void* weight, float eps, void* q, float* scale,
+                                    void* residual_out, int64_t residual_out_row_stride, int64_t tokens,
+                                    int64_t hidden, int dtype, int qtype, void* stream);
+
+int rmsnorm_quant_strided(const void* x, int64_t x_row_stride, const void* weight, float eps, void* q, float* scale,
+                          int64_t tokens, int64_t hidden, int dtype, int qtype, void* stream);
+
 /* the output dtype od of FAR_DTYPES(act, wd), or -status when the pair is rejected */
 int far_output_dtype(int dtype);
 

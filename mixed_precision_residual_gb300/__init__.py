@@ -57,6 +57,16 @@ lib.layernorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
 lib.layernorm.restype = _int
 lib.far_plan_ln_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
 lib.far_plan_ln_for_sms.restype = _int
+lib.fused_add_layernorm_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _f32, _vp, _i64, _vp, _i64, _i64, _i64,
+                                            _int, _vp]
+lib.fused_add_layernorm_strided.restype = _int
+lib.layernorm_strided.argtypes = [_vp, _i64, _vp, _vp, _f32, _vp, _i64, _i64, _i64, _int, _vp]
+lib.layernorm_strided.restype = _int
+lib.fused_add_rmsnorm_quant_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _i64,
+                                                _int, _int, _vp]
+lib.fused_add_rmsnorm_quant_strided.restype = _int
+lib.rmsnorm_quant_strided.argtypes = [_vp, _i64, _vp, _f32, _vp, _vp, _i64, _i64, _int, _int, _vp]
+lib.rmsnorm_quant_strided.restype = _int
 lib.gemm_f16_f32acc.argtypes = [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp]
 lib.gemm_f16_f32acc.restype = _int
 lib.far_plan_gemm_for_sms.argtypes = [_i64, _i64, _i64, _int, _int, _int, _vp]
@@ -251,33 +261,53 @@ def fused_add_rmsnorm_quant(x: torch.Tensor, residual: torch.Tensor, weight: tor
     q is int8 for "int8" and uint8 E4M3 codes for "fp8" (view as torch.float8_e4m3fn);
     dequantise as q * scale[:, None].
     """
-    if not (x.is_contiguous() and residual.is_contiguous() and weight.is_contiguous()):
-        raise ValueError("x, residual and weight must be contiguous")
+    if not weight.is_contiguous():
+        raise ValueError("weight must be contiguous")
     tokens, hidden = _rows(x)
     if q is None:
         q = torch.empty(x.shape, dtype=torch.int8 if qtype == "int8" else torch.uint8, device=x.device)
     if scale is None:
         scale = torch.empty(tokens, dtype=torch.float32, device=x.device)
     if residual_out is None:
-        residual_out = torch.empty_like(x)
-    _check(lib.fused_add_rmsnorm_quant(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(q), _ptr(scale),
-                                       _ptr(residual_out), tokens, hidden, dtypes(x.dtype, weight.dtype),
-                                       QUANT[qtype], _stream_handle(stream)))
+        residual_out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    if not (q.is_contiguous() and scale.is_contiguous()):
+        raise ValueError("q and scale must be contiguous")
+    code = dtypes(x.dtype, weight.dtype)
+    ts = (x, residual, residual_out)
+    if all(t.is_contiguous() for t in ts):
+        _check(lib.fused_add_rmsnorm_quant(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(q), _ptr(scale),
+                                           _ptr(residual_out), tokens, hidden, code, QUANT[qtype],
+                                           _stream_handle(stream)))
+    else:
+        st = [_row_stride(t) for t in ts]
+        if None in st:
+            raise ValueError("non-contiguous tensors must be 2-D with contiguous rows")
+        _check(lib.fused_add_rmsnorm_quant_strided(_ptr(x), st[0], _ptr(residual), st[1], _ptr(weight), eps, _ptr(q),
+                                                   _ptr(scale), _ptr(residual_out), st[2], tokens, hidden, code,
+                                                   QUANT[qtype], _stream_handle(stream)))
     return q, scale, residual_out
 
 
 def rmsnorm_quant(x: torch.Tensor, weight: torch.Tensor, eps: float, qtype: str = "int8",
                   q: torch.Tensor | None = None, scale: torch.Tensor | None = None, stream=None):
     """(q, scale): the no-residual variant with a per-token quantised output."""
-    if not (x.is_contiguous() and weight.is_contiguous()):
-        raise ValueError("x and weight must be contiguous")
+    if not weight.is_contiguous():
+        raise ValueError("weight must be contiguous")
     tokens, hidden = _rows(x)
     if q is None:
         q = torch.empty(x.shape, dtype=torch.int8 if qtype == "int8" else torch.uint8, device=x.device)
     if scale is None:
         scale = torch.empty(tokens, dtype=torch.float32, device=x.device)
-    _check(lib.rmsnorm_quant(_ptr(x), _ptr(weight), eps, _ptr(q), _ptr(scale), tokens, hidden,
-                             dtypes(x.dtype, weight.dtype), QUANT[qtype], _stream_handle(stream)))
+    code = dtypes(x.dtype, weight.dtype)
+    if x.is_contiguous():
+        _check(lib.rmsnorm_quant(_ptr(x), _ptr(weight), eps, _ptr(q), _ptr(scale), tokens, hidden, code,
+                                 QUANT[qtype], _stream_handle(stream)))
+    else:
+        sx = _row_stride(x)
+        if sx is None:
+            raise ValueError("a non-contiguous x must be 2-D with contiguous rows")
+        _check(lib.rmsnorm_quant_strided(_ptr(x), sx, _ptr(weight), eps, _ptr(q), _ptr(scale), tokens, hidden, code,
+                                         QUANT[qtype], _stream_handle(stream)))
     return q, scale
 
 
@@ -294,11 +324,12 @@ def fused_add_layernorm(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Te
                         stream=None):
     """out, residual_out = LayerNorm(x + residual) * gamma + beta under the rounding contract.
 
-    x, residual: contiguous [..., hidden] CUDA tensors of one dtype; gamma, beta:
-    contiguous [hidden] in the weight dtype.  Outputs are allocated when not given.
+    x, residual: [..., hidden] CUDA tensors of one dtype, contiguous or 2-D with contiguous
+    rows and any row stride; gamma, beta: contiguous [hidden] in the weight dtype.
+    Outputs are allocated when not given.
     """
-    if not all(t.is_contiguous() for t in (x, residual, gamma, beta)):
-        raise ValueError("x, residual, gamma and beta must be contiguous")
+    if not (gamma.is_contiguous() and beta.is_contiguous()):
+        raise ValueError("gamma and beta must be contiguous")
     if residual.dtype != x.dtype or beta.dtype != gamma.dtype:
         raise ValueError("x and residual, gamma and beta must share a dtype")
     code = dtypes(x.dtype, gamma.dtype)
@@ -308,28 +339,44 @@ def fused_add_layernorm(x: torch.Tensor, residual: torch.Tensor, gamma: torch.Te
         residual_out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
     tokens, hidden = _rows(x)
     if (gamma.numel() != hidden or beta.numel() != hidden or residual.shape != x.shape or out.shape != x.shape
-            or residual_out.shape != x.shape or not out.is_contiguous() or not residual_out.is_contiguous()):
-        raise ValueError("shape mismatch or non-contiguous output")
-    _check(lib.fused_add_layernorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), eps, _ptr(out),
-                                   _ptr(residual_out), tokens, hidden, code, _stream_handle(stream)))
+            or residual_out.shape != x.shape):
+        raise ValueError("shape mismatch")
+    ts = (x, residual, out, residual_out)
+    if all(t.is_contiguous() for t in ts):
+        _check(lib.fused_add_layernorm(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), eps, _ptr(out),
+                                       _ptr(residual_out), tokens, hidden, code, _stream_handle(stream)))
+    else:
+        st = [_row_stride(t) for t in ts]
+        if None in st:
+            raise ValueError("non-contiguous tensors must be 2-D with contiguous rows")
+        _check(lib.fused_add_layernorm_strided(_ptr(x), st[0], _ptr(residual), st[1], _ptr(gamma), _ptr(beta), eps,
+                                               _ptr(out), st[2], _ptr(residual_out), st[3], tokens, hidden, code,
+                                               _stream_handle(stream)))
     return out, residual_out
 
 
 def layernorm(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor, eps: float,
               out: torch.Tensor | None = None, stream=None):
     """out = LayerNorm(x) * gamma + beta under the rounding contract (no residual)."""
-    if not all(t.is_contiguous() for t in (x, gamma, beta)):
-        raise ValueError("x, gamma and beta must be contiguous")
+    if not (gamma.is_contiguous() and beta.is_contiguous()):
+        raise ValueError("gamma and beta must be contiguous")
     if beta.dtype != gamma.dtype:
         raise ValueError("gamma and beta must share a dtype")
     code = dtypes(x.dtype, gamma.dtype)
     if out is None:
         out = torch.empty(x.shape, dtype=output_dtype(x.dtype, gamma.dtype), device=x.device)
     tokens, hidden = _rows(x)
-    if gamma.numel() != hidden or beta.numel() != hidden or out.shape != x.shape or not out.is_contiguous():
-        raise ValueError("shape mismatch or non-contiguous output")
-    _check(lib.layernorm(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(out), tokens, hidden, code,
-                         _stream_handle(stream)))
+    if gamma.numel() != hidden or beta.numel() != hidden or out.shape != x.shape:
+        raise ValueError("shape mismatch")
+    if x.is_contiguous() and out.is_contiguous():
+        _check(lib.layernorm(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(out), tokens, hidden, code,
+                             _stream_handle(stream)))
+    else:
+        sx, so = _row_stride(x), _row_stride(out)
+        if sx is None or so is None:
+            raise ValueError("non-contiguous tensors must be 2-D with contiguous rows")
+        _check(lib.layernorm_strided(_ptr(x), sx, _ptr(gamma), _ptr(beta), eps, _ptr(out), so, tokens, hidden, code,
+                                     _stream_handle(stream)))
     return out
 
 

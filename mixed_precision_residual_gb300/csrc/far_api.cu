@@ -186,34 +186,40 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
 
 // the LayerNorm entry points: gamma in the weight's place, plus beta
 int validate_ln(const void* x, const void* r, const void* gamma, const void* beta, float eps, void* out,
-                void* res_out, int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c) {
+                void* res_out, int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c,
+                const Strides* strides = nullptr) {
   c.ln = true;
   c.beta = beta;
-  return validate(x, r, gamma, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  return validate(x, r, gamma, eps, out, res_out, tokens, hidden, dtype, residual, c, strides);
 }
 
 // the quantised entry points: q and scale replace out and must share no byte with anything
 int validate_quant(const void* x, const void* r, const void* w, float eps, void* q, float* scale, void* res_out,
-                   int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, Call& c) {
+                   int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, Call& c,
+                   const Strides* strides = nullptr) {
   if (qtype != kQuantInt8 && qtype != kQuantFp8) return FAR_ERR_DTYPE;
   c.quant = qtype;
   c.q = q;
   c.scale = scale;
+  // q is always contiguous ([tokens, hidden] bytes); x, the residual and residual_out may
+  // have row strides
+  Strides sd = strides ? *strides : Strides{hidden, hidden, hidden, hidden};
+  sd.out = hidden;
   // validate the rest with q standing in for out (the out checks then cover q's bytes too)
-  int st = validate(x, r, w, eps, q, res_out, tokens, hidden, dtype, residual, c);
+  int st = validate(x, r, w, eps, q, res_out, tokens, hidden, dtype, residual, c, &sd);
   if (st != FAR_OK || tokens == 0) return st;
   if (!scale) return FAR_ERR_NULL;
   const int64_t sa = dsize(c.act);
   const Region Q = region(q, tokens, hidden, hidden);
   const Region S = region(scale, 1, tokens * 4, tokens * 4);
-  const Region X = region(x, tokens, hidden * sa, hidden * sa);
+  const Region X = region(x, tokens, hidden * sa, sd.x * sa);
   const Region W = region(w, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
   // q: one byte an element, never an exact alias of an input
   if (regions_overlap(Q, X) || regions_overlap(S, X) || regions_overlap(S, Q) || regions_overlap(S, W))
     return FAR_ERR_ALIAS;
   if (residual) {
-    const Region R = region(r, tokens, hidden * sa, hidden * sa);
-    const Region RO = region(res_out, tokens, hidden * sa, hidden * sa);
+    const Region R = region(r, tokens, hidden * sa, sd.r * sa);
+    const Region RO = region(res_out, tokens, hidden * sa, sd.res * sa);
     if (regions_overlap(Q, R) || regions_overlap(S, R) || regions_overlap(S, RO)) return FAR_ERR_ALIAS;
   }
   c.out = nullptr;
@@ -450,9 +456,10 @@ int run(const void* x, const void* r, const void* w, float eps, void* out, void*
 }
 
 int run_quant(const void* x, const void* r, const void* w, float eps, void* q, float* scale, void* res_out,
-              int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, void* stream) {
+              int64_t tokens, int64_t hidden, int dtype, int qtype, bool residual, void* stream,
+              const Strides* strides = nullptr) {
   Call c;
-  int st = validate_quant(x, r, w, eps, q, scale, res_out, tokens, hidden, dtype, qtype, residual, c);
+  int st = validate_quant(x, r, w, eps, q, scale, res_out, tokens, hidden, dtype, qtype, residual, c, strides);
   if (st != FAR_OK || tokens == 0) return st;
   DeviceState* dev = nullptr;
   st = current_device(dev);
@@ -461,9 +468,9 @@ int run_quant(const void* x, const void* r, const void* w, float eps, void* q, f
 }
 
 int run_ln(const void* x, const void* r, const void* gamma, const void* beta, float eps, void* out, void* res_out,
-           int64_t tokens, int64_t hidden, int dtype, bool residual, void* stream) {
+           int64_t tokens, int64_t hidden, int dtype, bool residual, void* stream, const Strides* strides = nullptr) {
   Call c;
-  int st = validate_ln(x, r, gamma, beta, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  int st = validate_ln(x, r, gamma, beta, eps, out, res_out, tokens, hidden, dtype, residual, c, strides);
   if (st != FAR_OK || tokens == 0) return st;
   DeviceState* dev = nullptr;
   st = current_device(dev);
@@ -710,6 +717,34 @@ int fused_add_layernorm(const void* x, const void* residual, const void* gamma, 
 int layernorm(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
               int64_t hidden, int dtype, void* stream) {
   return run_ln(x, nullptr, gamma, beta, eps, out, nullptr, tokens, hidden, dtype, false, stream);
+}
+
+int fused_add_layernorm_strided(const void* x, int64_t x_row_stride, const void* residual,
+                                int64_t residual_row_stride, const void* gamma, const void* beta, float eps, void* out,
+                                int64_t out_row_stride, void* residual_out, int64_t residual_out_row_stride,
+                                int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  const Strides sd{x_row_stride, residual_row_stride, out_row_stride, residual_out_row_stride};
+  return run_ln(x, residual, gamma, beta, eps, out, residual_out, tokens, hidden, dtype, true, stream, &sd);
+}
+
+int layernorm_strided(const void* x, int64_t x_row_stride, const void* gamma, const void* beta, float eps, void* out,
+                      int64_t out_row_stride, int64_t tokens, int64_t hidden, int dtype, void* stream) {
+  const Strides sd{x_row_stride, hidden, out_row_stride, hidden};
+  return run_ln(x, nullptr, gamma, beta, eps, out, nullptr, tokens, hidden, dtype, false, stream, &sd);
+}
+
+int fused_add_rmsnorm_quant_strided(const void* x, int64_t x_row_stride, const void* residual,
+                                    int64_t residual_row_stride, const void* weight, float eps, void* q, float* scale,
+                                    void* residual_out, int64_t residual_out_row_stride, int64_t tokens,
+                                    int64_t hidden, int dtype, int qtype, void* stream) {
+  const Strides sd{x_row_stride, residual_row_stride, hidden, residual_out_row_stride};
+  return run_quant(x, residual, weight, eps, q, scale, residual_out, tokens, hidden, dtype, qtype, true, stream, &sd);
+}
+
+int rmsnorm_quant_strided(const void* x, int64_t x_row_stride, const void* weight, float eps, void* q, float* scale,
+                          int64_t tokens, int64_t hidden, int dtype, int qtype, void* stream) {
+  const Strides sd{x_row_stride, hidden, hidden, hidden};
+  return run_quant(x, nullptr, weight, eps, q, scale, nullptr, tokens, hidden, dtype, qtype, false, stream, &sd);
 }
 
 int far_output_dtype(int dtype) {

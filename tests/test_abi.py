@@ -303,3 +303,26 @@ def test_gemm_plans(far):
         assert p["grid"] % 2 == 0 or p["kind"] == 0  # pairs launch whole clusters
     for m, n, k in [(64, 12, 64), (64, 64, 12), (64, 64, 0), (3, 5, 7)]:
         assert far.plan_gemm_for_sms(m, n, k, True, T16, 152)["kind"] == 1
+
+
+def test_strided_layernorm_and_quant_validation(far):
+    """The strided LayerNorm and quantised entry points reject before any CUDA call: a
+    stride below hidden, a missing beta or scale, an output over beta or over x."""
+    L = far.lib
+    B = FAKE + (8 << 30)
+    g, b = FAKE + (2 << 30), FAKE + (5 << 30)
+    bf = code("bf16", "bf16")
+    assert L.fused_add_layernorm_strided(B, 32, B + 128, 256, g, b, 1e-5, B + 256, 256, B + 384, 256, 4, 64, bf,
+                                         None) == 4   # x stride below hidden
+    assert L.fused_add_layernorm_strided(B, 256, B + 128, 256, g, None, 1e-5, B + 256, 256, B + 384, 256, 4, 64, bf,
+                                         None) == 3   # no beta
+    assert L.layernorm_strided(B, 256, g, b, 1e-5, B + 64, 256, 4, 64, bf, None) == 5      # out shares x's columns
+    assert L.layernorm_strided(B, 256, g, b, 1e-5, b, 256, 4, 64, bf, None) == 5           # out over beta
+    q, sc = FAKE + (3 << 30), FAKE + (6 << 30)
+    assert L.rmsnorm_quant_strided(B, 63, g, 1e-6, q, sc, 4, 64, bf, 1, None) == 4
+    assert L.rmsnorm_quant_strided(B, 256, g, 1e-6, q, None, 4, 64, bf, 1, None) == 3
+    assert L.rmsnorm_quant_strided(B, 256, g, 1e-6, B + 16, sc, 4, 64, bf, 1, None) == 5   # q inside x's rows
+    assert L.fused_add_rmsnorm_quant_strided(B, 256, B + 128, 256, g, 1e-6, q, sc, B + 130, 256, 4, 64, bf, 2,
+                                             None) == 5  # residual_out overlaps the residual partially
+    assert L.fused_add_rmsnorm_quant_strided(B, 256, B + 128, 256, g, 1e-6, q, sc, B + 256, 256, 4, 64, bf, 3,
+                                             None) == 2  # unknown quantised type

@@ -218,3 +218,29 @@ def test_rounded_squares_are_summed(far):
 
 def oracle_sums_of_squares(dev):
     return np.array([oracle.exact_sum((row * row).astype(np.float32)) for row in dev], np.float32)
+
+
+@pytest.mark.parametrize("act,wd,hidden", [("bf16", "bf16", 4096), ("f16", "f32", 1000), ("f32", "f32", 2048)])
+def test_strided_rows(far, act, wd, hidden):
+    """Column slices of wider buffers (x, residual, out, residual_out interleaved): bit for
+    bit the contiguous result, and the oracle's gate."""
+    d = with_beta(far_gen.custom_inputs(act, wd, 48, hidden, seed=hidden + 9))
+    T, H = 48, hidden
+    x_c, r_c, w, b = d["x"].cuda(), d["r"].cuda(), d["w"].cuda(), d["b"].cuda()
+    od = far.output_dtype(x_c.dtype, w.dtype)
+    wide = torch.zeros((T, 4 * H), dtype=x_c.dtype, device="cuda")
+    x, r = wide[:, 0:H], wide[:, 2 * H:3 * H]
+    x.copy_(x_c)
+    r.copy_(r_c)
+    res = wide[:, 3 * H:4 * H]
+    outw = torch.zeros((T, 2 * H), dtype=od, device="cuda")
+    out = outw[:, H:2 * H]
+    far.fused_add_layernorm(x, r, w, b, d["eps"], out=out, residual_out=res)
+    ref_out, ref_res = far.fused_add_layernorm(x_c, r_c, w, b, d["eps"])
+    assert far.device_status() == 0
+    assert bits_equal(out.cpu(), ref_out.cpu()) and bits_equal(res.cpu(), ref_res.cpu())
+    ro, rr = oracle.fused_add_layernorm(d["x"], d["r"], d["w"], d["b"], d["eps"], d["act"], d["wd"])
+    gate(out.cpu(), ro, res.cpu(), rr, where=f"strided fused {act}/{wd}")
+    nout = far.layernorm(x, w, b, d["eps"], out=outw[:, 0:H])
+    assert far.device_status() == 0
+    assert bits_equal(nout.cpu(), far.layernorm(x_c, w, b, d["eps"]).cpu())

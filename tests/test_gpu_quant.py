@@ -157,3 +157,25 @@ def test_quantisation_bit_exact_given_out(far, act, wd, hidden):
             got = q.numpy().astype(np.int64) if qtype == "int8" else q.view(torch.uint8).numpy().astype(np.int64)
             assert np.array_equal(scale.numpy().view(np.uint32), want_scale.view(np.uint32)), (qtype, residual)
             assert np.array_equal(got, codes), f"{act}/{wd} H={hidden} {qtype} residual={residual}: codes differ"
+
+
+@pytest.mark.parametrize("act,wd,hidden", [("bf16", "bf16", 4096), ("f16", "f16", 1000), ("f32", "f32", 2048)])
+def test_strided_inputs(far, act, wd, hidden):
+    """x, the residual and residual_out as column slices: codes, scales and residual_out bit
+    for bit the contiguous call's (q and scale stay contiguous)."""
+    d = far_gen.custom_inputs(act, wd, 40, hidden, seed=hidden + 2)
+    T, H = 40, hidden
+    x_c, r_c, w = d["x"].cuda(), d["r"].cuda(), d["w"].cuda()
+    wide = torch.zeros((T, 3 * H), dtype=x_c.dtype, device="cuda")
+    x, r, res = wide[:, 0:H], wide[:, H:2 * H], wide[:, 2 * H:3 * H]
+    x.copy_(x_c)
+    r.copy_(r_c)
+    for qtype in ("int8", "fp8"):
+        q, s, res_o = far.fused_add_rmsnorm_quant(x, r, w, d["eps"], qtype, residual_out=res)
+        q_c, s_c, res_c = far.fused_add_rmsnorm_quant(x_c, r_c, w, d["eps"], qtype)
+        assert far.device_status() == 0
+        assert torch.equal(q.cpu(), q_c.cpu()) and bits_equal(s.cpu(), s_c.cpu()) and bits_equal(res.cpu(), res_c.cpu())
+        q, s = far.rmsnorm_quant(x, w, d["eps"], qtype)
+        q_c, s_c = far.rmsnorm_quant(x_c, w, d["eps"], qtype)
+        assert far.device_status() == 0
+        assert torch.equal(q.cpu(), q_c.cpu()) and bits_equal(s.cpu(), s_c.cpu())
