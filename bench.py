@@ -19,7 +19,7 @@ region, and the CPU oracle timed on the host cores as a baseline.
 Under torchrun each rank runs its own replica (weak scaling, no collective on
 the data path); rank 0 prints one JSON line.  --op measures one of the other
 operations of the library the same way (its fused form, then its no-residual
-variant); the end-to-end leg exists for RMSNorm only (the host-buffer entry points).
+variant), the end-to-end leg through that op's host-buffer entry points.
 """
 from __future__ import annotations
 
@@ -540,18 +540,49 @@ def main():
 
     # end to end through the host-buffer entry points: copies inside the timed region
     e2e = None
-    if args.e2e_steps > 0 and args.op == "rmsnorm":
-        xh, rh, wh = d["x"].pin_memory(), d["r"].pin_memory(), d["w"].pin_memory()
-        oh = torch.empty(x.shape, dtype=od, pin_memory=True)
+    if args.e2e_steps > 0:
+        xh, rh, wh, bh = (t.pin_memory() for t in (d["x"], d["r"], d["w"], d["b"]))
         roh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
-        o2h = torch.empty(x.shape, dtype=od, pin_memory=True)
         chunk = args.e2e_chunk
-        ws = torch.empty(far.host_workspace_bytes(chunk, H, x.dtype, wt.dtype, True), dtype=torch.uint8, device=dev)
+        host_op = {"rmsnorm": "rmsnorm", "layernorm": "layernorm"}.get(args.op, "quant")
+        ws = torch.empty(far.host_workspace_bytes_op(chunk, H, x.dtype, wt.dtype, True, host_op), dtype=torch.uint8,
+                         device=dev)
         wsb = ws.numel()
+        if quant:
+            oh = torch.empty(x.shape, dtype=torch.uint8, pin_memory=True)
+            o2h = torch.empty(x.shape, dtype=torch.uint8, pin_memory=True)
+            s1h = torch.empty(T, dtype=torch.float32, pin_memory=True)
+            s2h = torch.empty(T, dtype=torch.float32, pin_memory=True)
+        else:
+            oh = torch.empty(x.shape, dtype=od, pin_memory=True)
+            o2h = torch.empty(x.shape, dtype=od, pin_memory=True)
+        hp = {n: t.data_ptr() for n, t in (("x", xh), ("r", rh), ("w", wh), ("b", bh), ("o", oh), ("ro", roh),
+                                             ("o2", o2h), ("ws", ws))}
+        if args.op == "rmsnorm":
+            path = "fused_add_rmsnorm_host + rmsnorm_host"
+
+            def e2e_calls():
+                return (L.fused_add_rmsnorm_host(hp["x"], hp["r"], hp["w"], eps, hp["o"], hp["ro"], T, H, code,
+                                                 hp["ws"], wsb, sh),
+                        L.rmsnorm_host(hp["x"], hp["w"], eps, hp["o2"], T, H, code, hp["ws"], wsb, sh))
+        elif args.op == "layernorm":
+            path = "fused_add_layernorm_host + layernorm_host"
+
+            def e2e_calls():
+                return (L.fused_add_layernorm_host(hp["x"], hp["r"], hp["w"], hp["b"], eps, hp["o"], hp["ro"], T, H,
+                                                   code, hp["ws"], wsb, sh),
+                        L.layernorm_host(hp["x"], hp["w"], hp["b"], eps, hp["o2"], T, H, code, hp["ws"], wsb, sh))
+        else:
+            path = "fused_add_rmsnorm_quant_host + rmsnorm_quant_host"
+
+            def e2e_calls():
+                return (L.fused_add_rmsnorm_quant_host(hp["x"], hp["r"], hp["w"], eps, hp["o"], s1h.data_ptr(),
+                                                       hp["ro"], T, H, code, qt, hp["ws"], wsb, sh),
+                        L.rmsnorm_quant_host(hp["x"], hp["w"], eps, hp["o2"], s2h.data_ptr(), T, H, code, qt,
+                                             hp["ws"], wsb, sh))
+
         def e2e_step():
-            s1 = L.fused_add_rmsnorm_host(xh.data_ptr(), rh.data_ptr(), wh.data_ptr(), eps, oh.data_ptr(),
-                                          roh.data_ptr(), T, H, code, ws.data_ptr(), wsb, sh)
-            s2 = L.rmsnorm_host(xh.data_ptr(), wh.data_ptr(), eps, o2h.data_ptr(), T, H, code, ws.data_ptr(), wsb, sh)
+            s1, s2 = e2e_calls()
             if s1 or s2:
                 raise RuntimeError(f"host-buffer launch failed: {s1} {s2}")
         e2e_step()
@@ -565,14 +596,15 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dist, dev)
-        sa, sw, so = DSIZE[x.dtype], DSIZE[wt.dtype], DSIZE[od]
-        h2d = T * H * sa * 2 + H * sw + T * H * sa + H * sw
-        d2h = T * H * so + T * H * sa + T * H * so
+        sa, sw = DSIZE[x.dtype], DSIZE[wt.dtype]
+        so = 1 if quant else DSIZE[od]
+        nw = 2 if args.op == "layernorm" else 1  # weight rows copied per call (LayerNorm: gamma and beta)
+        h2d = T * H * sa * 2 + nw * H * sw + T * H * sa + nw * H * sw
+        d2h = T * H * so + T * H * sa + T * H * so + (2 * T * 4 if quant else 0)
         e2e = {"value": round(job_rate(fb + nb, world, e2e_ms) / 1e9, 3), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3),
                "tokens_per_s": round(job_rate(T, world, e2e_ms), 1),
-               "path": f"fused_add_rmsnorm_host + rmsnorm_host (pinned host buffers, {chunk}-row chunks, "
-                       "two internal streams)"}
+               "path": f"{path} (pinned host buffers, {chunk}-row chunks, two internal streams)"}
         assert far.device_status() == 0
 
     peak, peak_kind = measured_peaks()

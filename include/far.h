@@ -253,6 +253,30 @@ int rmsnorm_host(const void* x, const void* weight, float eps, void* out, int64_
                  int64_t hidden, int dtype, void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * The same host-buffer pipeline for LayerNorm and for the quantised outputs (arguments as
+ * their device forms, every buffer on the host).  far_host_workspace_bytes_op sizes the
+ * workspace for `chunk_tokens` rows of an op: 0 RMSNorm (as far_host_workspace_bytes),
+ * 1 LayerNorm (gamma and beta kept once), 2 a quantised output (q and the per-row scales
+ * in place of out).  Negative -status on bad arguments.
+ */
+int64_t far_host_workspace_bytes_op(int64_t chunk_tokens, int64_t hidden, int dtype, int has_residual, int op);
+
+int fused_add_layernorm_host(const void* x, const void* residual, const void* gamma, const void* beta, float eps,
+                             void* out, void* residual_out, int64_t tokens, int64_t hidden, int dtype,
+                             void* workspace, int64_t workspace_bytes, void* stream);
+
+int layernorm_host(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
+                   int64_t hidden, int dtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+int fused_add_rmsnorm_quant_host(const void* x, const void* residual, const void* weight, float eps, void* q,
+                                 float* scale, void* residual_out, int64_t tokens, int64_t hidden, int dtype,
+                                 int qtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+int rmsnorm_quant_host(const void* x, const void* weight, float eps, void* q, float* scale, int64_t tokens,
+                       int64_t hidden, int dtype, int qtype, void* workspace, int64_t workspace_bytes,
+                       void* stream);
+
+/*
  * fused_add_rmsnorm_host on host buffers WITHOUT any allocation: no workspace
  * argument, no cudaMalloc or cudaFree, no stream or event creation.  (The pages
  * describe no such entry point: it is an addition of this library.)

@@ -57,6 +57,17 @@ lib.layernorm.argtypes = [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp]
 lib.layernorm.restype = _int
 lib.far_plan_ln_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
 lib.far_plan_ln_for_sms.restype = _int
+lib.far_host_workspace_bytes_op.argtypes = [_i64, _i64, _int, _int, _int]
+lib.far_host_workspace_bytes_op.restype = _i64
+lib.fused_add_layernorm_host.argtypes = [_vp, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _vp, _i64, _vp]
+lib.fused_add_layernorm_host.restype = _int
+lib.layernorm_host.argtypes = [_vp, _vp, _vp, _f32, _vp, _i64, _i64, _int, _vp, _i64, _vp]
+lib.layernorm_host.restype = _int
+lib.fused_add_rmsnorm_quant_host.argtypes = [_vp, _vp, _vp, _f32, _vp, _vp, _vp, _i64, _i64, _int, _int, _vp, _i64,
+                                             _vp]
+lib.fused_add_rmsnorm_quant_host.restype = _int
+lib.rmsnorm_quant_host.argtypes = [_vp, _vp, _f32, _vp, _vp, _i64, _i64, _int, _int, _vp, _i64, _vp]
+lib.rmsnorm_quant_host.restype = _int
 lib.fused_add_layernorm_strided.argtypes = [_vp, _i64, _vp, _i64, _vp, _vp, _f32, _vp, _i64, _vp, _i64, _i64, _i64,
                                             _int, _vp]
 lib.fused_add_layernorm_strided.restype = _int
@@ -422,3 +433,48 @@ def plan_gemm_for_sms(m: int, n: int, k: int, bias: bool, out_dtype: torch.dtype
 
 def set_gemm_override(kind: int = -1, bn: int = 0) -> None:
     _check(lib.far_set_gemm_override(kind, bn))
+
+
+HOST_OP = {"rmsnorm": 0, "layernorm": 1, "quant": 2}
+
+
+def host_workspace_bytes_op(chunk_tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool,
+                            op: str) -> int:
+    """Workspace bytes of the host-buffer pipeline for `op` ("rmsnorm", "layernorm", "quant")."""
+    n = lib.far_host_workspace_bytes_op(chunk_tokens, hidden, dtypes(act, wd), int(residual), HOST_OP[op])
+    if n < 0:
+        raise FarError(-n)
+    return n
+
+
+def _wsb(workspace: torch.Tensor) -> int:
+    return workspace.numel() * workspace.element_size()
+
+
+def fused_add_layernorm_host(x, residual, gamma, beta, eps, out, residual_out, workspace, stream=None) -> None:
+    """End-to-end LayerNorm on host (ideally pinned) tensors through a device workspace."""
+    tokens, hidden = _rows(x)
+    _check(lib.fused_add_layernorm_host(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(beta), eps, _ptr(out),
+                                        _ptr(residual_out), tokens, hidden, dtypes(x.dtype, gamma.dtype),
+                                        _ptr(workspace), _wsb(workspace), _stream_handle(stream)))
+
+
+def layernorm_host(x, gamma, beta, eps, out, workspace, stream=None) -> None:
+    tokens, hidden = _rows(x)
+    _check(lib.layernorm_host(_ptr(x), _ptr(gamma), _ptr(beta), eps, _ptr(out), tokens, hidden,
+                              dtypes(x.dtype, gamma.dtype), _ptr(workspace), _wsb(workspace), _stream_handle(stream)))
+
+
+def fused_add_rmsnorm_quant_host(x, residual, weight, eps, qtype, q, scale, residual_out, workspace,
+                                 stream=None) -> None:
+    tokens, hidden = _rows(x)
+    _check(lib.fused_add_rmsnorm_quant_host(_ptr(x), _ptr(residual), _ptr(weight), eps, _ptr(q), _ptr(scale),
+                                            _ptr(residual_out), tokens, hidden, dtypes(x.dtype, weight.dtype),
+                                            QUANT[qtype], _ptr(workspace), _wsb(workspace), _stream_handle(stream)))
+
+
+def rmsnorm_quant_host(x, weight, eps, qtype, q, scale, workspace, stream=None) -> None:
+    tokens, hidden = _rows(x)
+    _check(lib.rmsnorm_quant_host(_ptr(x), _ptr(weight), eps, _ptr(q), _ptr(scale), tokens, hidden,
+                                  dtypes(x.dtype, weight.dtype), QUANT[qtype], _ptr(workspace), _wsb(workspace),
+                                  _stream_handle(stream)))

@@ -489,11 +489,14 @@ struct HostLayout {
   int64_t total;
 };
 
-HostLayout host_layout(int64_t rows, int64_t hidden, int act, int wd, int od, bool residual) {
+enum HostOp { kHostRms = 0, kHostLn = 1, kHostQuant = 2 };
+
+HostLayout host_layout(int64_t rows, int64_t hidden, int act, int wd, int od, bool residual, int op = kHostRms) {
   HostLayout h;
-  h.w_bytes = align256(hidden * dsize(wd));
+  h.w_bytes = align256(hidden * dsize(wd)) * (op == kHostLn ? 2 : 1);  // the weight (LayerNorm: gamma, beta)
   h.x_bytes = align256(rows * hidden * dsize(act));
-  h.o_bytes = align256(rows * hidden * dsize(od));
+  // out, or for a quantised output q (one byte an element) and the per-row scales
+  h.o_bytes = op == kHostQuant ? align256(rows * hidden) + align256(rows * 4) : align256(rows * hidden * dsize(od));
   // per slot: x, (residual, residual_out), out
   int64_t slot = h.x_bytes * (residual ? 3 : 1) + h.o_bytes;
   h.total = h.w_bytes + 2 * slot;
@@ -516,40 +519,46 @@ int ensure_pipe(DeviceState& d) {
   return FAR_OK;
 }
 
-int run_host(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
-             int64_t hidden, int dtype, bool residual, void* workspace, int64_t ws_bytes, void* stream) {
-  Call c;
-  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
-  if (st != FAR_OK || tokens == 0) return st;
+// The host-buffer pipeline for a validated call `c` whose pointers are host buffers:
+// row chunks stream through the two slots of `workspace` on two internal streams (copy in,
+// kernel, copy out), after the weight (and LayerNorm's beta) is copied once.
+int run_host_call(const Call& c, void* workspace, int64_t ws_bytes, void* stream) {
+  if (c.tokens == 0) return FAR_OK;
   if (!workspace) return FAR_ERR_NULL;
   if (!aligned16(workspace)) return FAR_ERR_WORKSPACE;
+  const int op = c.ln ? kHostLn : c.quant ? kHostQuant : kHostRms;
+  const int64_t tokens = c.tokens, hidden = c.hidden;
+  const bool residual = c.residual;
   // the largest chunk of rows whose two slots fit the workspace (the layout grows with rows)
-  if (host_layout(1, hidden, c.act, c.wd, c.od, residual).total > ws_bytes) return FAR_ERR_WORKSPACE;
+  if (host_layout(1, hidden, c.act, c.wd, c.od, residual, op).total > ws_bytes) return FAR_ERR_WORKSPACE;
   int64_t lo = 1, hi = tokens;
   while (lo < hi) {
     const int64_t mid = lo + (hi - lo + 1) / 2;
-    if (host_layout(mid, hidden, c.act, c.wd, c.od, residual).total <= ws_bytes) lo = mid;
+    if (host_layout(mid, hidden, c.act, c.wd, c.od, residual, op).total <= ws_bytes) lo = mid;
     else hi = mid - 1;
   }
   const int64_t rows = lo;
   DeviceState* dev = nullptr;
-  st = current_device(dev);
+  int st = current_device(dev);
   if (st != FAR_OK) return st;
   std::lock_guard<std::mutex> lk(dev->pipe_mu);
   st = ensure_pipe(*dev);
   if (st != FAR_OK) return st;
 
-  const HostLayout lay = host_layout(rows, hidden, c.act, c.wd, c.od, residual);
+  const HostLayout lay = host_layout(rows, hidden, c.act, c.wd, c.od, residual, op);
   char* base = static_cast<char*>(workspace);
   char* w_dev = base;
+  char* beta_dev = base + align256(hidden * dsize(c.wd));
   char* slot_base[2] = {base + lay.w_bytes, base + lay.w_bytes + (lay.total - lay.w_bytes) / 2};
-  const int64_t sa = dsize(c.act), so = dsize(c.od);
+  const int64_t sa = dsize(c.act), so = op == kHostQuant ? 1 : dsize(c.od);
   cudaStream_t caller = static_cast<cudaStream_t>(stream);
 
   cudaError_t e = cudaEventRecord(dev->fork, caller);
   for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(dev->pipe[i], dev->fork, 0);
   if (e == cudaSuccess)
-    e = cudaMemcpyAsync(w_dev, w, hidden * dsize(c.wd), cudaMemcpyHostToDevice, dev->pipe[0]);
+    e = cudaMemcpyAsync(w_dev, c.w, hidden * dsize(c.wd), cudaMemcpyHostToDevice, dev->pipe[0]);
+  if (e == cudaSuccess && op == kHostLn)
+    e = cudaMemcpyAsync(beta_dev, c.beta, hidden * dsize(c.wd), cudaMemcpyHostToDevice, dev->pipe[0]);
   if (e == cudaSuccess) e = cudaEventRecord(dev->wready, dev->pipe[0]);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(dev->pipe[1], dev->wready, 0);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -560,27 +569,34 @@ int run_host(const void* x, const void* r, const void* w, float eps, void* out, 
     const int s = (int)(chunk & 1);
     cudaStream_t ps = dev->pipe[s];
     char* xd = slot_base[s];
-    char* od = xd + lay.x_bytes;
+    char* od = xd + lay.x_bytes;                         // out, or q then the scales
+    char* scd = od + align256(rows * hidden);            // the scales (quantised output)
     char* rd = od + lay.o_bytes;
     char* rod = rd + lay.x_bytes;
     const int64_t in_off = t0 * hidden * sa, out_off = t0 * hidden * so;
-    e = cudaMemcpyAsync(xd, static_cast<const char*>(x) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
+    e = cudaMemcpyAsync(xd, static_cast<const char*>(c.x) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
     if (e == cudaSuccess && residual)
-      e = cudaMemcpyAsync(rd, static_cast<const char*>(r) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
+      e = cudaMemcpyAsync(rd, static_cast<const char*>(c.r) + in_off, n * hidden * sa, cudaMemcpyHostToDevice, ps);
     if (e != cudaSuccess) return cuda_fail(e);
     Call cc = c;
     cc.x = xd;
     cc.r = residual ? rd : nullptr;
     cc.w = w_dev;
-    cc.out = od;
+    cc.beta = op == kHostLn ? beta_dev : nullptr;
+    cc.out = op == kHostQuant ? nullptr : od;
+    cc.q = op == kHostQuant ? od : nullptr;
+    cc.scale = op == kHostQuant ? reinterpret_cast<float*>(scd) : nullptr;
     cc.res_out = residual ? rod : nullptr;
     cc.tokens = n;
     cc.st = Strides{hidden, hidden, hidden, hidden};  // the workspace slots are contiguous
     st = launch(cc, *dev, ps);
     if (st != FAR_OK) return st;
-    e = cudaMemcpyAsync(static_cast<char*>(out) + out_off, od, n * hidden * so, cudaMemcpyDeviceToHost, ps);
+    void* out_host = op == kHostQuant ? c.q : c.out;
+    e = cudaMemcpyAsync(static_cast<char*>(out_host) + out_off, od, n * hidden * so, cudaMemcpyDeviceToHost, ps);
+    if (e == cudaSuccess && op == kHostQuant)
+      e = cudaMemcpyAsync(c.scale + t0, scd, n * 4, cudaMemcpyDeviceToHost, ps);
     if (e == cudaSuccess && residual)
-      e = cudaMemcpyAsync(static_cast<char*>(res_out) + in_off, rod, n * hidden * sa, cudaMemcpyDeviceToHost, ps);
+      e = cudaMemcpyAsync(static_cast<char*>(c.res_out) + in_off, rod, n * hidden * sa, cudaMemcpyDeviceToHost, ps);
     if (e != cudaSuccess) return cuda_fail(e);
   }
   for (int i = 0; i < 2; ++i) {
@@ -589,6 +605,14 @@ int run_host(const void* x, const void* r, const void* w, float eps, void* out, 
     if (e != cudaSuccess) return cuda_fail(e);
   }
   return FAR_OK;
+}
+
+int run_host(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
+             int64_t hidden, int dtype, bool residual, void* workspace, int64_t ws_bytes, void* stream) {
+  Call c;
+  int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c);
+  if (st != FAR_OK || tokens == 0) return st;
+  return run_host_call(c, workspace, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -796,6 +820,45 @@ int64_t far_host_workspace_bytes(int64_t chunk_tokens, int64_t hidden, int dtype
   if (st != FAR_OK) return -st;
   if (chunk_tokens <= 0 || hidden <= 0 || hidden > kMaxHidden) return -FAR_ERR_SHAPE;
   return host_layout(chunk_tokens, hidden, act, wd, od, has_residual != 0).total;
+}
+
+int64_t far_host_workspace_bytes_op(int64_t chunk_tokens, int64_t hidden, int dtype, int has_residual, int op) {
+  int act, wd, od;
+  int st = decode(dtype, act, wd, od);
+  if (st != FAR_OK) return -st;
+  if (chunk_tokens <= 0 || hidden <= 0 || hidden > kMaxHidden || op < 0 || op > 2) return -FAR_ERR_SHAPE;
+  return host_layout(chunk_tokens, hidden, act, wd, od, has_residual != 0, op).total;
+}
+
+int fused_add_layernorm_host(const void* x, const void* residual, const void* gamma, const void* beta, float eps,
+                             void* out, void* residual_out, int64_t tokens, int64_t hidden, int dtype,
+                             void* workspace, int64_t workspace_bytes, void* stream) {
+  Call c;
+  int st = validate_ln(x, residual, gamma, beta, eps, out, residual_out, tokens, hidden, dtype, true, c);
+  return (st != FAR_OK || tokens == 0) ? st : run_host_call(c, workspace, workspace_bytes, stream);
+}
+
+int layernorm_host(const void* x, const void* gamma, const void* beta, float eps, void* out, int64_t tokens,
+                   int64_t hidden, int dtype, void* workspace, int64_t workspace_bytes, void* stream) {
+  Call c;
+  int st = validate_ln(x, nullptr, gamma, beta, eps, out, nullptr, tokens, hidden, dtype, false, c);
+  return (st != FAR_OK || tokens == 0) ? st : run_host_call(c, workspace, workspace_bytes, stream);
+}
+
+int fused_add_rmsnorm_quant_host(const void* x, const void* residual, const void* weight, float eps, void* q,
+                                 float* scale, void* residual_out, int64_t tokens, int64_t hidden, int dtype,
+                                 int qtype, void* workspace, int64_t workspace_bytes, void* stream) {
+  Call c;
+  int st = validate_quant(x, residual, weight, eps, q, scale, residual_out, tokens, hidden, dtype, qtype, true, c);
+  return (st != FAR_OK || tokens == 0) ? st : run_host_call(c, workspace, workspace_bytes, stream);
+}
+
+int rmsnorm_quant_host(const void* x, const void* weight, float eps, void* q, float* scale, int64_t tokens,
+                       int64_t hidden, int dtype, int qtype, void* workspace, int64_t workspace_bytes,
+                       void* stream) {
+  Call c;
+  int st = validate_quant(x, nullptr, weight, eps, q, scale, nullptr, tokens, hidden, dtype, qtype, false, c);
+  return (st != FAR_OK || tokens == 0) ? st : run_host_call(c, workspace, workspace_bytes, stream);
 }
 
 int fused_add_rmsnorm_host(const void* x, const void* residual, const void* weight, float eps, void* out,

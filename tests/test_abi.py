@@ -326,3 +326,14 @@ def test_strided_layernorm_and_quant_validation(far):
                                              None) == 5  # residual_out overlaps the residual partially
     assert L.fused_add_rmsnorm_quant_strided(B, 256, B + 128, 256, g, 1e-6, q, sc, B + 256, 256, 4, 64, bf, 3,
                                              None) == 2  # unknown quantised type
+
+
+def test_host_workspace_size_per_op(far):
+    """RMSNorm's layout is unchanged; LayerNorm keeps beta beside gamma; a quantised output
+    holds q (one byte an element) and the per-row scales in place of out."""
+    T, H, bf = 8, 4096, code("bf16", "f32")
+    a256 = lambda n: -(-n // 256) * 256
+    assert far.lib.far_host_workspace_bytes_op(T, H, bf, 1, 0) == far.lib.far_host_workspace_bytes(T, H, bf, 1)
+    assert far.lib.far_host_workspace_bytes_op(T, H, bf, 1, 1) == 2 * a256(H * 4) + 2 * (3 * a256(T * H * 2) + a256(T * H * 4))
+    assert far.lib.far_host_workspace_bytes_op(T, H, bf, 0, 2) == a256(H * 4) + 2 * (a256(T * H * 2) + a256(T * H) + a256(T * 4))
+    assert far.lib.far_host_workspace_bytes_op(T, H, bf, 1, 3) == -4

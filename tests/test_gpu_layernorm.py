@@ -244,3 +244,23 @@ def test_strided_rows(far, act, wd, hidden):
     nout = far.layernorm(x, w, b, d["eps"], out=outw[:, 0:H])
     assert far.device_status() == 0
     assert bits_equal(nout.cpu(), far.layernorm(x_c, w, b, d["eps"]).cpu())
+
+
+def test_host_buffers(far):
+    """The host-buffer pipeline (several chunks through a small workspace) gives the device
+    path's bits."""
+    d = with_beta(far_gen.custom_inputs("bf16", "f32", 300, 2048, seed=41))
+    od = far.output_dtype(d["x"].dtype, d["w"].dtype)
+    ws = torch.empty(far.host_workspace_bytes_op(64, 2048, d["x"].dtype, d["w"].dtype, True, "layernorm"),
+                     dtype=torch.uint8, device="cuda")
+    xh, rh, wh, bh = (t.pin_memory() for t in (d["x"], d["r"], d["w"], d["b"]))
+    out = torch.empty((300, 2048), dtype=od).pin_memory()
+    res = torch.empty_like(d["x"]).pin_memory()
+    far.fused_add_layernorm_host(xh, rh, wh, bh, d["eps"], out, res, ws)
+    nout = torch.empty((300, 2048), dtype=od).pin_memory()
+    far.layernorm_host(xh, wh, bh, d["eps"], nout, ws)
+    torch.cuda.synchronize()
+    assert far.device_status() == 0
+    ref_out, ref_res = far.fused_add_layernorm(d["x"].cuda(), d["r"].cuda(), d["w"].cuda(), d["b"].cuda(), d["eps"])
+    assert bits_equal(out, ref_out.cpu()) and bits_equal(res, ref_res.cpu())
+    assert bits_equal(nout, far.layernorm(d["x"].cuda(), d["w"].cuda(), d["b"].cuda(), d["eps"]).cpu())

@@ -179,3 +179,26 @@ def test_strided_inputs(far, act, wd, hidden):
         q_c, s_c = far.rmsnorm_quant(x_c, w, d["eps"], qtype)
         assert far.device_status() == 0
         assert torch.equal(q.cpu(), q_c.cpu()) and bits_equal(s.cpu(), s_c.cpu())
+
+
+def test_host_buffers(far):
+    """The host-buffer pipeline for the quantised outputs gives the device path's bits."""
+    d = far_gen.custom_inputs("f16", "f16", 300, 4096, seed=43)
+    xh, rh, wh = (t.pin_memory() for t in (d["x"], d["r"], d["w"]))
+    for qtype in ("int8", "fp8"):
+        ws = torch.empty(far.host_workspace_bytes_op(64, 4096, d["x"].dtype, d["w"].dtype, True, "quant"),
+                         dtype=torch.uint8, device="cuda")
+        qdt = torch.int8 if qtype == "int8" else torch.uint8
+        q = torch.empty((300, 4096), dtype=qdt).pin_memory()
+        sc = torch.empty(300, dtype=torch.float32).pin_memory()
+        res = torch.empty_like(d["x"]).pin_memory()
+        far.fused_add_rmsnorm_quant_host(xh, rh, wh, d["eps"], qtype, q, sc, res, ws)
+        q2 = torch.empty((300, 4096), dtype=qdt).pin_memory()
+        sc2 = torch.empty(300, dtype=torch.float32).pin_memory()
+        far.rmsnorm_quant_host(xh, wh, d["eps"], qtype, q2, sc2, ws)
+        torch.cuda.synchronize()
+        assert far.device_status() == 0
+        rq, rs, rr = far.fused_add_rmsnorm_quant(d["x"].cuda(), d["r"].cuda(), d["w"].cuda(), d["eps"], qtype)
+        assert torch.equal(q, rq.cpu()) and bits_equal(sc, rs.cpu()) and bits_equal(res, rr.cpu())
+        rq2, rs2 = far.rmsnorm_quant(d["x"].cuda(), d["w"].cuda(), d["eps"], qtype)
+        assert torch.equal(q2, rq2.cpu()) and bits_equal(sc2, rs2.cpu())
