@@ -303,7 +303,7 @@ __device__ __forceinline__ bool pair_work(const GemmParams& p, int pair, int num
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     tc2_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                    const GemmParams p) {
+                    const __grid_constant__ CUtensorMap map_b_half, const GemmParams p) {
   using S = PairShape;
   constexpr int STAGES = S::stages;
   constexpr uint32_t IDESC = umma_idesc_f16_f32(S::BM, S::BN);
@@ -350,23 +350,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       // ---------------- TMA producer (both CTAs) ----------------
       tma_prefetch_map(&map_a);
       tma_prefetch_map(&map_b);
+      tma_prefetch_map(&map_b_half);
       uint32_t g = 0;
       bool ok = true;
       PairWork w;
       for (int item = 0; ok && pair_work(p, pair, num_pairs, item, w); ++item) {
-        // this CTA's rows of B: its half of the tile's columns (a 128-row box; a half tile
-        // uses the first 64 rows of it)
+        // this CTA's rows of B: its half of the tile's columns (128 rows, or 64 for a half tile)
+        const bool half = w.ncols != S::BN;
         const int b_row = w.col0 + (int)rank * (w.ncols / 2);
+        const uint32_t b_bytes = half ? S::b_bytes / 2 : S::b_bytes;
         for (int kb = 0; kb < num_kb; ++kb, ++g) {
           const uint32_t s = g % STAGES;
           if (!mbar_wait(empty0 + 8 * s, ((g / STAGES) & 1u) ^ 1u, p.timeout_ns, p.status)) {
             ok = false;
             break;
           }
-          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * (S::a_bytes + S::b_bytes));
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * (S::a_bytes + b_bytes));
           const uint32_t full_even = map_to_cta(full0 + 8 * s, 0);
           tma_load_2d_pair(a_base + s * S::a_bytes, &map_a, kb * kGemmBK, w.tm * S::BM + (int)rank * 128, full_even);
-          tma_load_2d_pair(b_base + s * S::b_bytes, &map_b, kb * kGemmBK, b_row, full_even);
+          tma_load_2d_pair(b_base + s * S::b_bytes, half ? &map_b_half : &map_b, kb * kGemmBK, b_row, full_even);
         }
       }
       if (rank == 0) {  // the pair's copies of the last slices must have landed before exit
@@ -536,8 +538,9 @@ struct GemmPlan {
 // tensor cores when TMA can read both operands (16-byte aligned rows and bases) and the
 // vector epilogue can write (N a multiple of 8, 16-byte aligned out and bias).  256 x 256
 // tiles over CTA pairs when there are enough of them to occupy every pair of SMs
-// (`max_pairs` clusters resident at once); else one CTA a tile, the widest tile width that
-// still gives a tile per SM, else 64.
+// (`max_pairs` clusters resident at once) and their waves are estimated no slower than
+// single-CTA 128 x 256 tiles'; else one CTA a tile, the widest tile width that still gives
+// a tile per SM, else 64.
 GemmPlan plan_gemm(const GemmCall& c, int sms, int max_pairs) {
   GemmPlan g{1, 0, 1, 256, 0};
   const bool tc = c.K > 0 && c.K % 8 == 0 && c.N % 8 == 0 && al16(c.x) && al16(c.wt) && al16(c.out) &&
@@ -546,7 +549,15 @@ GemmPlan plan_gemm(const GemmCall& c, int sms, int max_pairs) {
   const int force = g_gemm_force_kind.load();
   if (tc && max_pairs > 0 && (force == 2 || (force == -1 && g_gemm_force_bn.load() == 0))) {
     const int64_t pair_tiles = ((c.M + PairShape::BM - 1) / PairShape::BM) * ((c.N + PairShape::BN - 1) / PairShape::BN);
-    if (pair_tiles <= INT32_MAX && (force == 2 || pair_tiles >= max_pairs)) {
+    // estimated time in waves of whole pair tiles: the pairs' full waves plus the last
+    // wave's half tiles (each wave of them ~0.75 of a full wave, measured), against waves
+    // of single-CTA 128 x 256 tiles (the same work per SM at ~1.12x the time, measured:
+    // ~85 % vs ~95 % of the tensor peak in steady state)
+    const int64_t waves = pair_tiles / max_pairs, rest = pair_tiles % max_pairs;
+    const double pair_cost = (double)waves + (rest ? 0.75 * (double)((2 * rest + max_pairs - 1) / max_pairs) : 0.0);
+    const int64_t single_tiles = tiles_m * ((c.N + 255) / 256);
+    const double single_cost = 1.12 * (double)((single_tiles + sms - 1) / sms);
+    if (pair_tiles <= INT32_MAX && (force == 2 || (pair_tiles >= max_pairs && pair_cost <= single_cost))) {
       g.kind = 2;
       g.bn = PairShape::BN;
       g.grid = 2 * (int)(pair_tiles < max_pairs ? pair_tiles : max_pairs);
@@ -673,11 +684,14 @@ int run_gemm(const void* x, const void* wt, const void* bias, void* out, int64_t
         : g.bn == 128 ? launch_tc<128>(ma, mb, p, g, s)
                       : launch_tc<64>(ma, mb, p, g, s);
   } else if (g.kind == 2) {
-    CUtensorMap ma, mb;  // each CTA of a pair loads 128 rows of A and 128 rows (half the tile) of B
+    // each CTA of a pair loads 128 rows of A and its half of B's rows: 128, or 64 for the
+    // half tiles of the last wave
+    CUtensorMap ma, mb, mbh;
     st = encode_kmajor(&ma, x, M, K, 128);
     if (st == FAR_OK) st = encode_kmajor(&mb, wt, N, K, 128);
+    if (st == FAR_OK) st = encode_kmajor(&mbh, wt, N, K, 64);
     if (st != FAR_OK) return st;
-    tc2_gemm_kernel<<<g.grid, g.block, g.smem, s>>>(ma, mb, p);  // the attribute was set by max_active_pairs
+    tc2_gemm_kernel<<<g.grid, g.block, g.smem, s>>>(ma, mb, mbh, p);  // the attribute was set by max_active_pairs
     e = cudaGetLastError();
   } else {
     generic_gemm_kernel<<<g.grid, g.block, 0, s>>>(p);
