@@ -254,11 +254,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ---------------------------------------------------------------------------
 // CTA pairs: 256 x 256 output tiles over a cluster of 2 (the last, partial wave in
-// 256 x 128 halves).  Each CTA holds its 128 rows of
-// A and half (128 rows) of B per K-slice; one thread of the even CTA issues
-// tcgen05.mma.cta_group::2 (256 x 256 x 16) over both CTAs' tensor cores, each CTA's TMEM
-// receiving its 128 rows of the tile.  Per SM a slice is 32 KB for the same MMA time as
-// the single-CTA 128 x 256 tile's 48 KB.
+// 256 x 128 halves).  Each CTA holds its 128 rows of A and half (128 rows) of B per
+// K-slice; one thread of the even CTA issues tcgen05.mma.cta_group::2 (256 x 256 x 16)
+// over both CTAs' tensor cores, each CTA's TMEM receiving its 128 rows of the tile.  Per
+// SM a slice is 32 KB for the same MMA time as the single-CTA 128 x 256 tile's 48 KB.
 //   - both producers wait on their own "empty" barriers (the MMA's commit is multicast to
 //     both CTAs) and load into their own shared memory, counting the bytes on the even
 //     CTA's "full" barrier, which expects both CTAs' bytes;
@@ -275,8 +274,9 @@ struct PairShape {
 };
 
 // A pair's k-th work item: whole 256 x 256 tiles for the full waves, then the tiles of the
-// last, partial wave split into two 256 x 128 halves, so that wave costs half as long.
-// False past the end of the pair's list.
+// last, partial wave split into two 256 x 128 halves, so that wave finishes sooner (each
+// half-tile wave takes ~0.6-0.75 of a full one, measured).  False past the end of the
+// pair's list.
 struct PairWork {
   int tm, tn;
   int col0;   // first output column
