@@ -548,6 +548,22 @@ cudaError_t launch_typed(const Launch& L) {
       case 9: k = staged_kernel<ACT, WD, RES, 4, true, Q, LN>; break;
       case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q, LN>; break;
       case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q, LN>; break;
+      // 5 or 6 chunks a thread, only where they cover a row exactly (hidden 5120 or 2560 in
+      // 16-bit with 4 or 2 warps a row, 3072 with 2): plain RMSNorm only
+      case 11:
+        if constexpr (Q == kQuantNone && !LN) {
+          k = staged_kernel<ACT, WD, RES, 5, true, Q, LN>;
+          break;
+        } else {
+          return cudaErrorInvalidValue;
+        }
+      case 13:
+        if constexpr (Q == kQuantNone && !LN) {
+          k = staged_kernel<ACT, WD, RES, 6, true, Q, LN>;
+          break;
+        } else {
+          return cudaErrorInvalidValue;
+        }
       default: return cudaErrorInvalidValue;
     }
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);

@@ -134,13 +134,14 @@ def test_launch_plans_are_consistent(far):
     the rows, and a row is covered by its group's warps."""
     T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
     overrides = [(-1, 0, 0, 0), (0, 4, 1, 2), (0, 4, 2, 3), (0, 8, 1, 0), (0, 8, 4, 0), (0, 2, 0, 0),
-                 (0, 4, 2, 0), (0, 8, 3, 0), (0, 4, 2, 4), (0, 8, 2, 4), (0, 1, 0, 0), (0, 4, 16, 5)]
+                 (0, 4, 2, 0), (0, 8, 3, 0), (0, 4, 2, 4), (0, 8, 2, 4), (0, 1, 0, 0), (0, 4, 16, 5), (0, 5, 0, 0),
+                 (0, 6, 3, 6)]
     try:
         for kind, nch, groups, stages in overrides:
             far.set_launch_override(kind, nch, groups, stages)
             for (act, wd), hidden, tokens, res, sms in itertools.product(
                     [(T16, T16), (B16, B16), (B16, F32), (F32, F32), (F32, B16)],
-                    [1, 8, 64, 1000, 2048, 4096, 5120, 8192, 12288, 16384, 24576, 32768],
+                    [1, 8, 64, 1000, 2048, 2560, 3072, 4096, 5120, 8192, 12288, 16384, 24576, 32768],
                     [1, 8, 151, 152, 4096, 65536], (True, False), (152, 148, 1)):
                 p = far.plan_for_sms(tokens, hidden, act, wd, res, sms)
                 if p["kind"] == 1:  # generic kernel
@@ -149,7 +150,9 @@ def test_launch_plans_are_consistent(far):
                 sa = 4 if act == F32 else 2
                 chunks = hidden * sa // 16
                 G, g, st = p["warps_per_row"], p["groups"], p["stages"]
-                assert p["nch"] in (1, 2, 4, 8)
+                assert p["nch"] in (1, 2, 4, 5, 6, 8)
+                if p["nch"] in (5, 6):  # only as exact plans
+                    assert hidden * (4 if act == F32 else 2) // 16 == p["nch"] * p["warps_per_row"] * 32, p
                 assert st >= 2 and st % g == 0, p
                 packed = not res and act != F32  # the no-residual variant keeps 16-bit x packed
                 assert g * G <= (12 if p["nch"] == 8 and not packed else 16), p

@@ -123,6 +123,37 @@ def test_every_plan_gives_the_same_bits(far):
         assert bits_equal(out, results[0][0]) and bits_equal(nout, results[0][1])
 
 
+def test_exact_five_and_six_chunk_plans(far):
+    """Rows that 5 or 6 chunks a thread cover exactly (hidden 2560 and 3072 in 16-bit, 1280
+    and 1536 in binary32) get those plans by default; they must pass the gate and give the
+    same bits as the 8-chunk plan with idle lanes and as the generic kernel."""
+    cases = [("bf16", "bf16", 2560, 5), ("f16", "f16", 3072, 6), ("f32", "f32", 1280, 5),
+             ("f32", "bf16", 1536, 6), ("bf16", "f32", 2560, 5)]
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for act, wd, hidden, nch in cases:
+        for tokens in (1, 37, 1234):
+            plan = far.plan_for_sms(tokens, hidden, dt[act], dt[wd], True, sms)
+            if tokens >= sms:
+                assert plan["nch"] == nch, (act, hidden, tokens, plan)
+            d = far_gen.custom_inputs(act, wd, tokens, hidden, seed=tokens + hidden)
+            ref_out, ref_res = oracle_fused(d)
+            ref_norm = oracle_norm(d)
+            results = []
+            try:
+                for ov in [(-1, 0, 0, 0), (0, 8, 2, 0), (1, 0, 0, 0), (0, nch, 3, 3)]:
+                    far.set_launch_override(*ov)
+                    out, res = far_fused(far, d)
+                    nout = far_norm(far, d)
+                    gate(out, ref_out, res, ref_res, f"{act}/{wd} {hidden}x{tokens} plan {ov}")
+                    gate(nout, ref_norm, where=f"{act}/{wd} {hidden}x{tokens} plan {ov} rmsnorm")
+                    results.append((out, nout))
+            finally:
+                far.set_launch_override()
+            for out, nout in results[1:]:
+                assert bits_equal(out, results[0][0]) and bits_equal(nout, results[0][1])
+
+
 def test_special_values(far):
     """inf / NaN / huge / subnormal inputs: NaN spreads through its row only."""
     for act in ("f16", "bf16", "f32"):
