@@ -356,6 +356,16 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     // A row that 8 chunks a thread cover with idle lanes but 6 or 5 chunks cover exactly with
     // the same number of warps (hidden 2560 or 3072 in 16-bit) takes the exact plan: measured
     // 3-8 % faster (at most 6 groups fused, 7 for the variant); plain RMSNorm only.
+    // The packed variant on rows of 640 chunks (hidden 5120 in 16-bit), which 8 chunks cover
+    // with 3 warps and idle lanes, runs 10 chunks on 2 warps: measured 6-10 % faster from
+    // 2048 to 24576 tokens and as fast above, with 7 groups of one slot (9 up to 128 rows
+    // an SM, where the rows split evenly: 16384 tokens run 3.6 % faster still).
+    if (nch == 8 && packed && C == 640 && c.od != FAR_F32 && !one_group) {
+      nch = 10;
+      G = 2;
+      group_cap = rows_per_sm <= 128 ? 9 : 7;
+      slots_per_group = 1;
+    }
     if (nch == 8 && !c.quant && !c.ln && C % 256 != 0 && !one_group) {
       for (int cand : {6, 5}) {
         if (C % (32LL * cand) == 0 && C / (32LL * cand) == G) {
@@ -374,8 +384,14 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     staged = G <= max_consumer_warps(nch, packed);
     // 5 or 6 chunks a thread exist only as exact plain-RMSNorm kernels
     if ((nch == 5 || nch == 6) && (C != 32LL * nch * G || c.quant || c.ln)) staged = false;
+    // 10 chunks a thread exist only as exact kernels of the packed no-residual variant
+    if (nch == 10 && (C != 320LL * G || !packed)) staged = false;
     if (staged) {
-      groups = one_group ? 1 : max_consumer_warps(nch, packed) / G;
+      // the default plans keep to 16 consumer warps but for the 10-chunk one; more are
+      // reachable through overrides
+      const int cap_warps = max_consumer_warps(nch, packed);
+      const int plan_warps = (nch == 10 || cap_warps < kMaxConsumerWarps) ? cap_warps : kMaxConsumerWarps;
+      groups = one_group ? 1 : plan_warps / G;
       if (groups > group_cap) groups = group_cap;
       if (groups > rows_per_sm) groups = (int)(rows_per_sm > 0 ? rows_per_sm : 1);
       if (g_force_groups.load() > 0 && g_force_groups.load() * G <= max_consumer_warps(nch, packed))
@@ -899,9 +915,10 @@ int far_selftest_wait_timeout(uint32_t timeout_us, void* stream) {
 }
 
 int far_set_launch_override(int kind, int nch, int groups, int stages) {
-  if (kind < -1 || kind > 1 || (nch != 0 && nch != 1 && nch != 2 && nch != 4 && nch != 5 && nch != 6 && nch != 8) ||
+  if (kind < -1 || kind > 1 || (nch != 0 && nch != 1 && nch != 2 && nch != 4 && nch != 5 && nch != 6 && nch != 8 &&
+                                   nch != 10) ||
       groups < 0 ||
-      groups > kMaxConsumerWarps || stages < 0 || stages > 32)
+      groups > kMaxPackedWarps || stages < 0 || stages > 32)
     return FAR_ERR_SHAPE;
   g_force_kind = kind;
   g_force_nch = nch;

@@ -564,6 +564,15 @@ cudaError_t launch_typed(const Launch& L) {
         } else {
           return cudaErrorInvalidValue;
         }
+      // 10 chunks a thread: the no-residual variant on 16-bit rows that 2 warps cover
+      // exactly at 10 (hidden 5120 with x kept packed)
+      case 21:
+        if constexpr (Q == kQuantNone && !LN && packed_rows(RES, ACT)) {
+          k = staged_kernel<ACT, WD, RES, 10, true, Q, LN>;
+          break;
+        } else {
+          return cudaErrorInvalidValue;
+        }
       default: return cudaErrorInvalidValue;
     }
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);

@@ -14,8 +14,13 @@ namespace far {
 // registers, so it keeps 16 warps at 8 chunks a thread.
 constexpr int kMaxConsumerWarps = 16;
 __host__ __device__ constexpr bool packed_rows(bool residual, int act) { return !residual && act != 0; }
+// Consumer warps a CTA may hold: 12 at 8 chunks a thread (up to 128 registers), 16 below.
+// A packed no-residual row needs at most 96 registers a thread (up to 10 chunks): 19
+// consumer warps and the producer put at most 5 warps on each of the SM's four register
+// file quarters (16384 registers each), which leaves 96 a thread.
+constexpr int kMaxPackedWarps = 19;
 __host__ __device__ constexpr int max_consumer_warps(int nch, bool packed = false) {
-  return (nch >= 8 && !packed) ? 12 : 16;
+  return packed ? kMaxPackedWarps : (nch >= 8 ? 12 : 16);
 }
 __host__ __device__ constexpr int max_threads(int nch, bool packed = false) {
   return (max_consumer_warps(nch, packed) + 1) * 32;

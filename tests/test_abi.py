@@ -135,7 +135,7 @@ def test_launch_plans_are_consistent(far):
     T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
     overrides = [(-1, 0, 0, 0), (0, 4, 1, 2), (0, 4, 2, 3), (0, 8, 1, 0), (0, 8, 4, 0), (0, 2, 0, 0),
                  (0, 4, 2, 0), (0, 8, 3, 0), (0, 4, 2, 4), (0, 8, 2, 4), (0, 1, 0, 0), (0, 4, 16, 5), (0, 5, 0, 0),
-                 (0, 6, 3, 6)]
+                 (0, 6, 3, 6), (0, 10, 0, 0), (0, 10, 9, 18), (0, 8, 6, 12)]
     try:
         for kind, nch, groups, stages in overrides:
             far.set_launch_override(kind, nch, groups, stages)
@@ -150,12 +150,17 @@ def test_launch_plans_are_consistent(far):
                 sa = 4 if act == F32 else 2
                 chunks = hidden * sa // 16
                 G, g, st = p["warps_per_row"], p["groups"], p["stages"]
-                assert p["nch"] in (1, 2, 4, 5, 6, 8)
-                if p["nch"] in (5, 6):  # only as exact plans
+                assert p["nch"] in (1, 2, 4, 5, 6, 8, 10)
+                if p["nch"] in (5, 6, 10):  # only as exact plans
                     assert hidden * (4 if act == F32 else 2) // 16 == p["nch"] * p["warps_per_row"] * 32, p
                 assert st >= 2 and st % g == 0, p
                 packed = not res and act != F32  # the no-residual variant keeps 16-bit x packed
-                assert g * G <= (12 if p["nch"] == 8 and not packed else 16), p
+                if p["nch"] == 10:
+                    assert packed, p
+                # 19 consumer warps for packed rows (96 registers a thread), else 12 or 16
+                assert g * G <= (19 if packed else 12 if p["nch"] == 8 else 16), p
+                if kind == -1 and packed and p["nch"] != 10:
+                    assert g * G <= 16, p  # the default plans keep to 16 but for 10 chunks
                 assert p["threads"] == (1 + g * G) * 32
                 assert p["smem"] <= 227 * 1024
                 # the group's warps cover the row, and one warp fewer would not

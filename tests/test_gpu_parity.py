@@ -154,6 +154,28 @@ def test_exact_five_and_six_chunk_plans(far):
                 assert bits_equal(out, results[0][0]) and bits_equal(nout, results[0][1])
 
 
+def test_ten_chunk_variant(far):
+    """The no-residual variant on 16-bit rows that 2 warps cover exactly at 10 chunks a thread
+    (hidden 5120): every plan, including 10 chunks with 1 to 9 groups, gives the same bits
+    and passes the gate; the fused op asked for 10 chunks runs the generic kernel."""
+    for act, wd in [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f16", "f32")]:
+        d = far_gen.custom_inputs(act, wd, 999, 5120, seed=77)
+        ref_norm = oracle_norm(d)
+        ref_out, ref_res = oracle_fused(d)
+        results = []
+        try:
+            for ov in [(-1, 0, 0, 0), (0, 10, 1, 2), (0, 10, 6, 12), (0, 10, 9, 18), (0, 8, 6, 12), (1, 0, 0, 0)]:
+                far.set_launch_override(*ov)
+                nout = far_norm(far, d)
+                gate(nout, ref_norm, where=f"{act}/{wd} 5120 plan {ov} rmsnorm")
+                out, res = far_fused(far, d)
+                gate(out, ref_out, res, ref_res, f"{act}/{wd} 5120 plan {ov}")
+                results.append(nout)
+        finally:
+            far.set_launch_override()
+        assert all(bits_equal(r, results[0]) for r in results[1:])
+
+
 def test_special_values(far):
     """inf / NaN / huge / subnormal inputs: NaN spreads through its row only."""
     for act in ("f16", "bf16", "f32"):
