@@ -154,14 +154,22 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_from_profile(workload: str, op: str = "rmsnorm"):
-    """DRAM bytes per fused launch from a committed ncu summary, if the kernel sources still match."""
+PLAN_KEYS = ("kind", "nch", "warps_per_row", "groups", "stages")
+
+
+def traffic_from_profile(workload: str, op: str = "rmsnorm", plan: dict | None = None, tokens: int | None = None):
+    """DRAM bytes per fused launch from a committed ncu summary, if the kernel sources, the
+    launch plan and the token count are still the captured ones."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
     with open(TRAFFIC_FILE) as f:
         d = json.load(f)
     e = d.get(workload if op == "rmsnorm" else f"{workload}:{op}")
     if not e or e.get("source_hash") != source_hash():
+        return None
+    if plan is not None and e.get("launch_plan") != [plan[k] for k in PLAN_KEYS]:
+        return None
+    if tokens is not None and e.get("captured_tokens") != tokens:
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -609,7 +617,6 @@ def main():
 
     peak, peak_kind = measured_peaks()
     achieved = fb / (fused_ms * 1e-3) / 1e9
-    traffic = traffic_from_profile(args.workload, args.op)
     if args.op == "rmsnorm":
         plan = far.describe_launch(T, H, x.dtype, wt.dtype, True)
     elif args.op == "layernorm":
@@ -617,6 +624,7 @@ def main():
     else:
         plan = far.plan_quant_for_sms(T, H, x.dtype, wt.dtype, True, args.op.split("_")[1],
                                       torch.cuda.get_device_properties(dev).multi_processor_count)
+    traffic = traffic_from_profile(args.workload, args.op, plan, T)
     kernel_name = {"rmsnorm": "fused add+RMSNorm", "layernorm": "fused add+LayerNorm",
                    "rmsnorm_int8": "fused add+RMSNorm, int8 output",
                    "rmsnorm_fp8": "fused add+RMSNorm, FP8 output"}[args.op]

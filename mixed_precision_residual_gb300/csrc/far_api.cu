@@ -338,6 +338,15 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       const int64_t want = (budget + row_total / 2) / row_total;
       group_cap = (int)(want < 1 ? 1 : want);
       slots_per_group = 1;
+    } else if (c.residual && C > 128 && G <= max_consumer_warps(nch, false)) {
+      // fused rows at 8 chunks a thread: measured best with about 70 KB of rows (x and
+      // the residual) in flight per SM, one ring slot per group, and a slot more where an
+      // SM has at most 32 rows (hidden 2048 to 8192, 512 to 65536 tokens)
+      const int64_t slot = 2 * ((row_bytes + 127) / 128 * 128);
+      const int64_t target = 70 * 1024 + (rows_per_sm <= 32 ? slot : 0);
+      const int64_t want = (target + slot / 2) / slot;
+      group_cap = (int)(want < 1 ? 1 : want);
+      slots_per_group = 1;
     } else if (G >= 4) {
       if (c.residual) {
         nch = 1;

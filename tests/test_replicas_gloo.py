@@ -55,3 +55,31 @@ def test_two_gloo_ranks():
 def test_single_process_path():
     assert bench.max_over_ranks(3.25, None, None) == 3.25
     assert bench.job_rate(10.0, 1, 2.0) == 5000.0
+
+
+def test_traffic_record_matches_the_current_plans():
+    """The DRAM bytes the bench reports as `traffic` come from committed ncu captures; each
+    record names the kernel-source hash and the launch plan it was taken with. The record
+    must match the sources and the plan the planner picks today on a 152-SM GB300, and the
+    lookup must refuse another plan or token count."""
+    import json
+
+    import mixed_precision_residual_gb300 as far
+
+    with open(bench.TRAFFIC_FILE) as f:
+        d = json.load(f)
+    dt = {"f16": torch.float16, "bf16": torch.bfloat16}
+    cases = {"c5": ("f16", 8192, far.plan_for_sms), "c5:layernorm": ("f16", 8192, far.plan_ln_for_sms),
+             "c4": ("bf16", 5120, far.plan_for_sms)}
+    for key, (act, hidden, planner) in cases.items():
+        e = d[key]
+        assert e["source_hash"] == bench.source_hash(), key
+        p = planner(e["captured_tokens"], hidden, dt[act], dt[act], True, 152)
+        assert e["launch_plan"] == [p[k] for k in bench.PLAN_KEYS], (key, p)
+        assert e["dram_bytes_per_launch"] == e["captured_read_bytes"] + e["captured_write_bytes"]
+        workload, _, op = key.partition(":")
+        op = op or "rmsnorm"
+        assert bench.traffic_from_profile(workload, op, p, e["captured_tokens"]) == e["dram_bytes_per_launch"]
+        other = dict(p, groups=p["groups"] + 1)
+        assert bench.traffic_from_profile(workload, op, other, e["captured_tokens"]) is None
+        assert bench.traffic_from_profile(workload, op, p, e["captured_tokens"] // 2) is None
