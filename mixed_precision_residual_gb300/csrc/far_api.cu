@@ -347,6 +347,22 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       const int64_t want = (target + slot / 2) / slot;
       group_cap = (int)(want < 1 ? 1 : want);
       slots_per_group = 1;
+    } else if (packed && c.od != FAR_F32) {
+      // the no-residual variant on 16-bit rows (x kept packed), from a sweep of every plan
+      // on 59 shapes (hidden 1024 to 16384, 512 to 65536 tokens): rows of up to 192 chunks
+      // 7 groups of 2 slots; one warp a row 7 groups of 3 slots (1 below 100 rows an SM);
+      // two warps 8 groups of one slot; three 6; four 4; more, 16 warps in groups of 2 slots
+      if (C <= 192) {
+        group_cap = 7;
+        slots_per_group = 2;
+      } else if (G <= 4) {
+        const int caps[5] = {0, 7, 8, 6, 4};
+        group_cap = caps[G];
+        slots_per_group = (G == 1 && rows_per_sm >= 100) ? 3 : 1;
+      } else {
+        group_cap = kMaxConsumerWarps / G;
+        slots_per_group = 2;
+      }
     } else if (G >= 4) {
       if (c.residual) {
         nch = 1;
@@ -381,10 +397,13 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
           nch = cand;
           const int cap = c.residual ? 6 : 7;  // measured best: 6 groups (fused), 7 (variant)
           if (group_cap > cap) group_cap = cap;
+          if (packed) slots_per_group = 2;  // the variant: 2 slots a group
           break;
         }
       }
     }
+    // a variant batch of at most 16 rows an SM is latency-bound: one slot a group
+    if (packed && c.od != FAR_F32 && rows_per_sm <= 16 && G > 1) slots_per_group = 1;
     if (g_force_nch.load() > 0) {
       nch = g_force_nch.load();
       G = (int)((C + 32LL * nch - 1) / (32LL * nch));
@@ -396,10 +415,11 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     // 10 chunks a thread exist only as exact kernels of the packed no-residual variant
     if (nch == 10 && (C != 320LL * G || !packed)) staged = false;
     if (staged) {
-      // the default plans keep to 16 consumer warps but for the 10-chunk one; more are
-      // reachable through overrides
+      // the default plans keep to 16 consumer warps but for the packed variant with a 16-bit
+      // output (19); more are reachable through overrides
       const int cap_warps = max_consumer_warps(nch, packed);
-      const int plan_warps = (nch == 10 || cap_warps < kMaxConsumerWarps) ? cap_warps : kMaxConsumerWarps;
+      const int plan_warps =
+          ((packed && c.od != FAR_F32) || cap_warps < kMaxConsumerWarps) ? cap_warps : kMaxConsumerWarps;
       groups = one_group ? 1 : plan_warps / G;
       if (groups > group_cap) groups = group_cap;
       if (groups > rows_per_sm) groups = (int)(rows_per_sm > 0 ? rows_per_sm : 1);

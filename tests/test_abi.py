@@ -141,7 +141,7 @@ def test_launch_plans_are_consistent(far):
             far.set_launch_override(kind, nch, groups, stages)
             for (act, wd), hidden, tokens, res, sms in itertools.product(
                     [(T16, T16), (B16, B16), (B16, F32), (F32, F32), (F32, B16)],
-                    [1, 8, 64, 1000, 2048, 2560, 3072, 4096, 5120, 8192, 12288, 16384, 24576, 32768],
+                    [1, 8, 64, 1000, 1536, 2048, 2560, 3072, 4096, 5120, 6144, 8192, 12288, 16384, 24576, 32768],
                     [1, 8, 151, 152, 4096, 65536], (True, False), (152, 148, 1)):
                 p = far.plan_for_sms(tokens, hidden, act, wd, res, sms)
                 if p["kind"] == 1:  # generic kernel
@@ -159,8 +159,8 @@ def test_launch_plans_are_consistent(far):
                     assert packed, p
                 # 19 consumer warps for packed rows (96 registers a thread), else 12 or 16
                 assert g * G <= (19 if packed else 12 if p["nch"] == 8 else 16), p
-                if kind == -1 and packed and p["nch"] != 10:
-                    assert g * G <= 16, p  # the default plans keep to 16 but for 10 chunks
+                if kind == -1 and not (packed and wd != F32):
+                    assert g * G <= 16, p  # the default plans keep to 16 but for the 16-bit variant
                 assert p["threads"] == (1 + g * G) * 32
                 assert p["smem"] <= 227 * 1024
                 # the group's warps cover the row, and one warp fewer would not
