@@ -316,20 +316,37 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       if (c.residual) group_cap = G >= 4 ? (wide_out ? 3 : 2) : (G == 1 ? 10 : 5);
       else group_cap = wide_out ? 5 : kMaxConsumerWarps;
       slots_per_group = 1;
-    } else if (c.quant && C > 128) {
+    } else if (c.ln) {
+      // LayerNorm on rows of one warp at up to 4 chunks a thread (hidden up to 1024 in
+      // 16-bit): 7 groups of one slot (measured 5-50 % faster than a rows-per-group cap)
+      group_cap = 7;
+      slots_per_group = 1;
+    } else if (c.quant) {
       // quantised output (a second per-row reduction, the row maximum, lengthens each
-      // row's critical path, so several groups must overlap it): measured best were
-      // 4 chunks a thread for the fused op and 8 for the variant when that still gives
-      // 4+ warps a row, 3 groups at most, one ring slot per group (two for rows of 8+ warps)
-      const bool eight = !c.residual && (C + 255) / 256 >= 4;
-      nch = eight ? 8 : 4;
-      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
-      if (G > kMaxConsumerWarps) {
-        nch = 8;
-        G = (int)((C + 255) / 256);
+      // row's critical path, so as many groups as possible must overlap it), from a sweep
+      // of every plan on 20 shapes per op (hidden 1024 to 8192, 512 to 32768 tokens; mean
+      // 0.6-0.9 % above the best plan of each, against 14-16 % for the previous table):
+      // 8 chunks a thread where they cover the row exactly (the non-exact quantised kernels
+      // spill registers) and need at most 12 warps but not 3, else 4 chunks; as many
+      // groups of one slot as the warps hold, but at most 11 (fused) or 12 (variant) on
+      // one-warp rows and 7 (fused) or 10 (variant) on rows of up to 128 chunks. The fused
+      // op on rows of 2+ warps at 8 chunks keeps to 8 warps: with 12 it is 5-10 % faster
+      // after an L2 flush but 3-10 % slower when the previous launch's output is still
+      // being written back (back-to-back launches, as in the bench)
+      if (C > 128) {
+        nch = (C % 256 == 0 && C / 256 <= 12 && C / 256 != 3) ? 8 : 4;
+        G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+        if (G > kMaxConsumerWarps) {
+          nch = 8;
+          G = (int)((C + 255) / 256);
+        }
+        if (G == 1) group_cap = c.residual ? 11 : 12;
+        else if (c.residual && nch == 8) group_cap = 8 / G > 0 ? 8 / G : 1;
+        else group_cap = 1 << 30;
+      } else {
+        group_cap = c.residual ? 7 : 10;
       }
-      group_cap = 3;
-      slots_per_group = (c.residual && G >= 8) ? 2 : 1;
+      slots_per_group = 1;
     } else if (c.od == FAR_F32 && !c.quant) {
       // fp32 output (or fp32 activations): rows are long in bytes; keep about 128 KB
       // (fused) or 120 KB (variant) of rows in progress per SM, one ring slot per group
