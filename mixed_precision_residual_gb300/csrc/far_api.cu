@@ -356,11 +356,29 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       group_cap = (int)(want < 1 ? 1 : want);
       slots_per_group = 1;
     } else if (c.residual && C > 128 && G <= max_consumer_warps(nch, false)) {
-      // fused rows at 8 chunks a thread: measured best with about 70 KB of rows (x and
-      // the residual) in flight per SM, one ring slot per group, and a slot more where an
-      // SM has at most 32 rows (hidden 2048 to 8192, 512 to 65536 tokens)
+      // fused rows, one ring slot per group, from sweeps of every plan timed both after an
+      // L2 flush and back to back (where each launch writes back the previous one's output
+      // still in L2, as in a stream of launches): rows that 8 chunks a thread cover exactly
+      // (and one-warp rows) at 8 chunks with about 70 KB of x and residual in flight per
+      // SM, a slot more where an SM has at most 32 rows; longer rows that 8 chunks would
+      // cover with idle lanes at 5 or 6 chunks where they cover the row exactly, else 4,
+      // with about 64 KB in flight (96 KB at most 32 rows an SM)
+      if (C > 256 && C % 256 != 0) {
+        int n = 0;
+        for (int cand : {5, 6, 4})
+          if (C % (32LL * cand) == 0 && C / (32LL * cand) <= kMaxConsumerWarps) {
+            n = cand;
+            break;
+          }
+        if (n == 0 && (C + 127) / 128 <= kMaxConsumerWarps) n = 4;
+        if (n != 0) {
+          nch = n;
+          G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+        }
+      }
       const int64_t slot = 2 * ((row_bytes + 127) / 128 * 128);
-      const int64_t target = 70 * 1024 + (rows_per_sm <= 32 ? slot : 0);
+      const int64_t target = nch != 8 ? (rows_per_sm <= 32 ? 96 : 64) * 1024
+                                      : 70 * 1024 + (rows_per_sm <= 32 ? slot : 0);
       const int64_t want = (target + slot / 2) / slot;
       group_cap = (int)(want < 1 ? 1 : want);
       slots_per_group = 1;
