@@ -387,6 +387,7 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       // on 59 shapes (hidden 1024 to 16384, 512 to 65536 tokens): rows of up to 192 chunks
       // 7 groups of 2 slots; one warp a row 7 groups of 3 slots (1 below 100 rows an SM);
       // two warps 8 groups of one slot; three 6; four 4; more, 16 warps in groups of 2 slots
+      // (of one slot at 8+ warps a row, measured back to back)
       if (C <= 192) {
         group_cap = 7;
         slots_per_group = 2;
@@ -396,7 +397,7 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
         slots_per_group = (G == 1 && rows_per_sm >= 100) ? 3 : 1;
       } else {
         group_cap = kMaxConsumerWarps / G;
-        slots_per_group = 2;
+        slots_per_group = G >= 8 ? 1 : 2;
       }
     } else if (G >= 4) {
       if (c.residual) {
@@ -418,13 +419,14 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     // 3-8 % faster (at most 6 groups fused, 7 for the variant); plain RMSNorm only.
     // The packed variant on rows of 640 chunks (hidden 5120 in 16-bit), which 8 chunks cover
     // with 3 warps and idle lanes, runs 10 chunks on 2 warps: measured 6-10 % faster from
-    // 2048 to 24576 tokens and as fast above, with 7 groups of one slot (9 up to 128 rows
-    // an SM, where the rows split evenly: 16384 tokens run 3.6 % faster still).
+    // 2048 to 24576 tokens and as fast above, with 7 groups of one slot above 128 rows an
+    // SM, 5 groups of 2 slots from 65 to 128 (the best mean of timings after an L2 flush
+    // and back to back at 16384 tokens) and 9 of one slot below.
     if (nch == 8 && packed && C == 640 && c.od != FAR_F32 && !one_group) {
       nch = 10;
       G = 2;
-      group_cap = rows_per_sm <= 128 ? 9 : 7;
-      slots_per_group = 1;
+      group_cap = rows_per_sm > 128 ? 7 : (rows_per_sm > 64 ? 5 : 9);
+      slots_per_group = (rows_per_sm > 64 && rows_per_sm <= 128) ? 2 : 1;
     }
     if (nch == 8 && !c.quant && !c.ln && C % 256 != 0 && !one_group) {
       for (int cand : {6, 5}) {
