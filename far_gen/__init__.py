@@ -253,7 +253,8 @@ def gemm_inputs(M: int, N: int, K: int, seed: int = 0, bias: bool = True) -> dic
 def gemm_dyadic_inputs(M: int, N: int, K: int, seed: int = 0) -> dict:
     """GEMM operands on a dyadic grid: x, wt in {k/8 : -8 <= k <= 8}, bias in {k/16 : -16
     <= k <= 16}.  Every product is a multiple of 2^-6 of magnitude <= 1, so every partial
-    sum of up to 2^10 products is exact in binary32 whatever the order of the additions."""
+    sum of up to 2^18 products (at most 2^18 in magnitude, on a 2^-6 grid: 24 bits) is
+    exact in binary32 whatever the order of the additions."""
     def grid(stream, n, half, scale):
         u = uniform(seed, stream, 0, n)
         return torch.from_numpy((np.floor(u * (2 * half + 1)) - half) / scale).to(torch.float16)
