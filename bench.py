@@ -277,7 +277,8 @@ def run_reference(args):
     value = (fb + nb) * args.steps / el / 1e9
     sample = (f"{rows} of {w.tokens} rows of the {w.name} batch per step ({OP_STEP[args.op]}), "
               f"oracle on {threads} host threads")
-    line = {"impl": "reference", "metric": OP_METRIC[args.op], "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+    line = {"impl": "reference", "metric": OP_METRIC[args.op], "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "compute": "host cores (the oracle; no GPU work)",
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.act,
             "data": "synthetic (seeded Philox4x32-10 generator)",
@@ -328,7 +329,8 @@ def run_gemm_reference(args):
         total_rows, total_s = total_rows + rows, total_s + el
     value = 2.0 * total_rows * N * K / total_s / 1e12
     sample = f"the first rows of x (all {N} columns, K = {K}) per step, about {per_step:.1f} s each, oracle on {threads} host threads"
-    line = {"impl": "reference", "metric": OP_METRIC["gemm"], "value": round(value, 8), "unit": "TFLOP/s", "n_gpus": 0,
+    line = {"impl": "reference", "metric": OP_METRIC["gemm"], "value": round(value, 8), "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "compute": "host cores (the oracle; no GPU work)",
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_s / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
             "data": "synthetic (seeded Philox4x32-10 generator)",
