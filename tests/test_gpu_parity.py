@@ -65,6 +65,17 @@ def test_dtype_pairs_and_hidden_sizes(far, act, wd, hidden):
     check_both(far, d, f"{act}/{wd} H={hidden}")
 
 
+@pytest.mark.parametrize("act,wd", [("bf16", "bf16"), ("f16", "f16"), ("bf16", "f32"), ("f32", "f32")])
+@pytest.mark.parametrize("hidden", [768, 1536, 2560, 3000, 3072, 6144, 7168, 10240, 12288])
+@pytest.mark.parametrize("tokens", [600, 2500])
+def test_default_plans_across_widths(far, act, wd, hidden, tokens):
+    """The launch table's rules at 4 and 17 rows an SM (more groups, exact 5, 6 or 10
+    chunks, 4 chunks on rows with idle lanes at 8, up to 19 warps for the variant):
+    the default plans of both ops against the oracle."""
+    d = far_gen.custom_inputs(act, wd, tokens, hidden, seed=hidden + tokens, scale_lo=1e-2, scale_hi=50.0)
+    check_both(far, d, f"{act}/{wd} {tokens}x{hidden}")
+
+
 @pytest.mark.parametrize("hidden", [16384, 24576, 32768, 65536, 100003])
 def test_large_hidden(far, hidden):
     d = far_gen.custom_inputs("bf16", "bf16", 5, hidden, seed=3)

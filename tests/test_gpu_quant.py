@@ -87,6 +87,16 @@ def test_dtype_pairs(far, act, wd, hidden):
     check_quant(far, d, f"{act}/{wd} H={hidden}")
 
 
+@pytest.mark.parametrize("act,wd", [("bf16", "bf16"), ("f16", "f16"), ("f32", "f32")])
+@pytest.mark.parametrize("hidden", [256, 1024, 2048, 3072, 4096, 6144, 7168, 12288])
+@pytest.mark.parametrize("tokens", [600, 2500])
+def test_default_plans_across_widths(far, act, wd, hidden, tokens):
+    """The default plans (8 chunks a thread on rows they cover exactly, else 4; up to 12
+    one-warp groups; 8 warps for fused rows of 2+ warps) at 4 and 17 rows an SM."""
+    d = far_gen.custom_inputs(act, wd, tokens, hidden, seed=hidden + tokens, scale_lo=1e-2, scale_hi=50.0)
+    check_quant(far, d, f"{act}/{wd} {tokens}x{hidden}")
+
+
 def test_generic_path_and_plans(far):
     d = far_gen.custom_inputs("f16", "f16", 200, 8192, seed=9)
     try:
