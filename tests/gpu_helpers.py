@@ -1,8 +1,8 @@
 """Helpers for the GPU parity tests: guarded device buffers, calls through the
 C ABI, and the parity gate.
 
-The gate (the north star of this path, after the case study "Aligning fused
-RMSNorm rounding across vLLM backends", section "Testing the contract"):
+The gate (after the case study "Aligning fused RMSNorm rounding across vLLM
+backends", section "Testing the contract"):
 residual_out bit for bit equal to the oracle's; out within 1 ULP of its dtype
 everywhere, with fewer than 1% of elements differing at all.
 """
