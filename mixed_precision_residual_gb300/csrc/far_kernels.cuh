@@ -52,7 +52,7 @@ __device__ __forceinline__ bool group_reduce(DW& v, float2* partials, uint64_t* 
 }
 
 template <int ACT, int WD, bool RES, int NCH, bool EXACT, int Q = kQuantNone, bool LN = false>
-__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && Q == kQuantNone && !LN), 1)
+__global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN), 1)
     staged_kernel(const Params p) {
   constexpr int SA = dtype_size<ACT>::value;
   constexpr int SW = dtype_size<WD>::value;

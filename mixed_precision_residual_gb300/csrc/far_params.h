@@ -15,7 +15,8 @@ namespace far {
 constexpr int kMaxConsumerWarps = 16;
 __host__ __device__ constexpr bool packed_rows(bool residual, int act) { return !residual && act != 0; }
 // Consumer warps a CTA may hold: 12 at 8 chunks a thread (up to 128 registers), 16 below.
-// A packed no-residual row needs at most 96 registers a thread (up to 10 chunks): 19
+// A packed no-residual row (RMSNorm, or RMSNorm with a quantised output, whose kept
+// outputs reuse the consumed x's registers) needs at most 96 registers a thread: 19
 // consumer warps and the producer put at most 5 warps on each of the SM's four register
 // file quarters (16384 registers each), which leaves 96 a thread.
 constexpr int kMaxPackedWarps = 19;

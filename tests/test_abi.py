@@ -202,7 +202,8 @@ def test_strided_validation(far):
 
 def test_quantised_launch_plans_are_consistent(far):
     """The planner's quantised plans: slots belong to one group, the CTA fits the 12-warp
-    (8 chunks) or 16-warp budget of the quantised kernels, shared memory fits, rows covered."""
+    (8 chunks) or 16-warp budget of the fused quantised kernels or the 19-warp budget of the
+    no-residual variant on 16-bit rows, shared memory fits, rows covered."""
     T16, B16, F32 = torch.float16, torch.bfloat16, torch.float32
     try:
         for override in [(-1, 0, 0, 0), (0, 8, 3, 0), (0, 4, 2, 3), (0, 2, 0, 0), (0, 8, 8, 8)]:
@@ -215,7 +216,8 @@ def test_quantised_launch_plans_are_consistent(far):
                     continue
                 G, g, st = p["warps_per_row"], p["groups"], p["stages"]
                 assert st >= 2 and st % g == 0, p
-                assert g * G <= (12 if p["nch"] == 8 else 16), p
+                packed = not res and act != F32  # x kept packed: 96 registers a thread
+                assert g * G <= (19 if packed else 12 if p["nch"] == 8 else 16), p
                 assert p["threads"] == (1 + g * G) * 32 and p["smem"] <= 227 * 1024
                 chunks = hidden * (4 if act == F32 else 2) // 16
                 assert (G - 1) * 32 * p["nch"] < chunks <= G * 32 * p["nch"], p
