@@ -423,7 +423,8 @@ def run_gemm_bench(args):
         "gpu_launches": args.steps,
         "roofline": {"bound": "tensor", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / peak, 4), "traffic": None,
-                     "kernel": "tc_gemm_kernel", "peak_source": "measured bf16_tflops (fp16 runs at the bf16 tensor rate)",
+                     "kernel": {0: "tc_gemm_kernel", 1: "generic_gemm_kernel", 2: "tc2_gemm_kernel"}.get(plan["kind"], "?"),
+                     "peak_source": "measured bf16_tflops (fp16 runs at the bf16 tensor rate)",
                      "algorithmic_flops_per_launch": flops, "avg_launch_ms": round(kernel_ms, 5), "launch_plan": plan},
         "clocks": clk,
         "e2e": None,

@@ -274,9 +274,10 @@ struct PairShape {
 };
 
 // A pair's k-th work item: whole 256 x 256 tiles for the full waves, then the tiles of the
-// last, partial wave split into two 256 x 128 halves, so that wave finishes sooner (each
-// half-tile wave takes ~0.6-0.75 of a full one, measured).  False past the end of the
-// pair's list.
+// last, partial wave split into two 256 x 128 halves where the halves fit in one round
+// (at most half the pairs have a tile left), so that wave finishes sooner (a half-tile
+// round takes ~0.6-0.75 of a full one, measured); else whole tiles (two rounds of halves
+// would take longer than one of whole tiles).  False past the end of the pair's list.
 struct PairWork {
   int tm, tn;
   int col0;   // first output column
@@ -286,10 +287,12 @@ __device__ __forceinline__ bool pair_work(const GemmParams& p, int pair, int num
   const int waves = p.num_tiles / num_pairs;
   const int rest = p.num_tiles - waves * num_pairs;
   int t, hsel = 0;
-  if (k < waves) {
+  if (k < waves || (k == waves && 2 * rest > num_pairs)) {
     t = pair + k * num_pairs;
+    if (t >= p.num_tiles) return false;
     w.ncols = PairShape::BN;
   } else {
+    if (2 * rest > num_pairs) return false;
     const int h = pair + (k - waves) * num_pairs;
     if (h >= 2 * rest) return false;
     t = waves * num_pairs + (h >> 1);
@@ -550,14 +553,16 @@ GemmPlan plan_gemm(const GemmCall& c, int sms, int max_pairs) {
   if (tc && max_pairs > 0 && (force == 2 || (force == -1 && g_gemm_force_bn.load() == 0))) {
     const int64_t pair_tiles = ((c.M + PairShape::BM - 1) / PairShape::BM) * ((c.N + PairShape::BN - 1) / PairShape::BN);
     // estimated time in waves of whole pair tiles: the pairs' full waves plus the last
-    // wave's half tiles (each wave of them ~0.75 of a full wave, measured), against waves
-    // of single-CTA 128 x 256 tiles (the same work per SM at ~1.12x the time, measured:
-    // ~85 % vs ~95 % of the tensor peak in steady state)
+    // wave, in half tiles where they fit one round (~0.75 of a full wave, measured), else
+    // whole tiles, against waves of single-CTA 128 x 256 tiles (the same work per SM at
+    // ~1.12x the time, measured: ~85 % vs ~95 % of the tensor peak in steady state).
+    // Pairs need tiles for at least half of them (fewer, as at 1024 x 1024, measured
+    // slower than single-CTA tiles)
     const int64_t waves = pair_tiles / max_pairs, rest = pair_tiles % max_pairs;
-    const double pair_cost = (double)waves + (rest ? 0.75 * (double)((2 * rest + max_pairs - 1) / max_pairs) : 0.0);
+    const double pair_cost = (double)waves + (rest == 0 ? 0.0 : 2 * rest <= max_pairs ? 0.75 : 1.0);
     const int64_t single_tiles = tiles_m * ((c.N + 255) / 256);
     const double single_cost = 1.12 * (double)((single_tiles + sms - 1) / sms);
-    if (pair_tiles <= INT32_MAX && (force == 2 || (pair_tiles >= max_pairs && pair_cost <= single_cost))) {
+    if (pair_tiles <= INT32_MAX && (force == 2 || (2 * pair_tiles >= max_pairs && pair_cost <= single_cost))) {
       g.kind = 2;
       g.bn = PairShape::BN;
       g.grid = 2 * (int)(pair_tiles < max_pairs ? pair_tiles : max_pairs);

@@ -306,7 +306,15 @@ def test_gemm_plans(far):
     p = far.plan_gemm_for_sms(8192, 8192, 8192, False, F32, 152)
     assert p["kind"] == 2 and p["bn"] == 256 and p["grid"] == 152  # CTA pairs, one CTA per SM
     assert far.plan_gemm_for_sms(4096, 2048, 4096, True, T16, 152)["bn"] == 256
-    assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["bn"] == 128  # 8 x 16 tiles of 256 < 152
+    # 64 pair tiles (half the pairs or more): pairs, whole tiles in one round
+    assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["kind"] == 2
+    assert far.plan_gemm_for_sms(2048, 2048, 8192, True, T16, 152)["kind"] == 2
+    assert far.plan_gemm_for_sms(1024, 1024, 4096, True, T16, 152)["kind"] == 0  # 16 pair tiles: one CTA a tile
+    try:
+        far.set_gemm_override(0, 0)  # one CTA a tile: the widest width that still gives a tile per SM
+        assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["bn"] == 128  # 8 x 16 tiles of 256 < 152
+    finally:
+        far.set_gemm_override()
     for m, n, k in [(100, 8, 8), (1, 8, 4096), (5000, 1000, 64)]:
         p = far.plan_gemm_for_sms(m, n, k, True, T16, 152)
         assert p["kind"] in (0, 2) and p["smem"] <= 227 * 1024 and p["threads"] == 192

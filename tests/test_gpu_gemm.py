@@ -237,3 +237,22 @@ def test_default_plan_uses_pairs_when_tiles_abound(far):
     assert far.plan_gemm_for_sms(4096, 4096, 512, True, torch.float16, 152)["kind"] == 2
     d = far_gen.gemm_dyadic_inputs(4096, 4096, 512, seed=9)
     check_exact(far, d, "default plan 4096x4096x512")
+
+
+def test_last_wave_in_whole_tiles(far):
+    """A last wave of tiles for more than half the pairs runs as whole 256 x 256 tiles (two
+    rounds of half tiles would take longer): 2048 x 2048 (64 tiles, one round) bit for bit
+    on dyadic operands and within the gates on random ones; 3072 x 3072 (a full wave, then
+    68 tiles) on sampled rows of every tile band."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert far.plan_gemm_for_sms(2048, 2048, 256, True, torch.float16, sms)["kind"] == 2
+    check_exact(far, far_gen.gemm_dyadic_inputs(2048, 2048, 256, seed=12), "dyadic 2048x2048x256 last wave whole")
+    check_all(far, far_gen.gemm_inputs(2048, 2048, 256, seed=13), "2048x2048x256 last wave whole")
+    M = N = 3072
+    K = 512
+    assert far.plan_gemm_for_sms(M, N, K, True, torch.float16, sms)["kind"] == 2
+    rows = sorted({r for band in range(0, M, 256) for r in (band, band + 129)} | {M - 1})
+    d = far_gen.gemm_dyadic_inputs(M, N, K, seed=14)
+    got = run_gemm(far, d, bias=True)
+    ref = oracle.gemm_f16(d["x"][rows], d["wt"], d["bias"], "f16")
+    assert torch.equal(got[rows].view(torch.int16), ref.view(torch.int16))
