@@ -307,21 +307,37 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     } else if (c.ln && C > 128) {
       // LayerNorm (two reductions a row, the mean's then the squared deviations', and
       // more arithmetic an element than RMSNorm): measured best were 8 chunks a thread
-      // and as many groups as 12 warps hold, one ring slot each, but only 2 groups for
-      // fused rows of 4+ warps (3 with an fp32 output of 16-bit activations), 5 for
-      // shorter fused rows (10 for one-warp rows), and 5 for the variant with an fp32
-      // output of 16-bit activations
+      // and as many groups as 12 warps hold, one ring slot each; with an fp32 output of
+      // 16-bit activations 3 groups for fused rows of 4+ warps, 5 for shorter fused rows
+      // (10 for one-warp rows) and 5 for the variant; the fused op otherwise as below
       nch = 8;
       G = (int)((C + 255) / 256);
       const bool wide_out = c.od == FAR_F32 && c.act != FAR_F32;
-      if (c.residual) group_cap = G >= 4 ? (wide_out ? 3 : 2) : (G == 1 ? 10 : 5);
-      else group_cap = wide_out ? 5 : kMaxConsumerWarps;
+      if (c.residual && !wide_out) {
+        // the fused op, from sweeps timed after an L2 flush and back to back: 4 chunks a
+        // thread where 8 would leave lanes idle and 4 cover the row exactly, and as many
+        // groups of one slot as keep about 64 KB of x and residual in flight per SM (a slot
+        // more where an SM has at most 32 rows), but at least 2 (bf16 32768 x 3072: 130 us
+        // against 156; 16384 x 7168: 160 against 177)
+        if (C % 256 != 0 && C % 128 == 0 && C / 128 <= kMaxConsumerWarps) {
+          nch = 4;
+          G = (int)(C / 128);
+        }
+        const int64_t slot = 2 * ((row_bytes + 127) / 128 * 128);
+        const int64_t want = (64 * 1024 + (rows_per_sm <= 32 ? slot : 0) + slot / 2) / slot;
+        group_cap = (int)(want < 2 ? 2 : want);
+      } else if (c.residual) {
+        group_cap = G >= 4 ? 3 : (G == 1 ? 10 : 5);
+      } else {
+        group_cap = wide_out ? 5 : kMaxConsumerWarps;
+      }
       slots_per_group = 1;
     } else if (c.ln) {
       // LayerNorm on rows of one warp at up to 4 chunks a thread (hidden up to 1024 in
-      // 16-bit): 7 groups of one slot (measured 5-50 % faster than a rows-per-group cap)
+      // 16-bit): 7 groups (measured 5-50 % faster than a rows-per-group cap), of two slots
+      // for the fused op (9 % faster back to back than one)
       group_cap = 7;
-      slots_per_group = 1;
+      slots_per_group = c.residual ? 2 : 1;
     } else if (c.quant) {
       // quantised output (a second per-row reduction, the row maximum, lengthens each
       // row's critical path, so as many groups as possible must overlap it), from a sweep
