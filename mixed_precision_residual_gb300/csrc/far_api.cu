@@ -270,17 +270,20 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   if (c.ln) w_bytes *= 2;  // gamma, then beta at the next 16-byte boundary
   size_t smem = 0;
   if (staged) {
-    // Launch table (measured on GB300 over nch x groups x slots, L2 flushed between launches):
-    //  - 8 chunks a thread (64 values for 16-bit data) keeps the per-row work (reductions,
-    //    IEEE divide and square root, waits) small against the per-element work;
-    //  - long rows (4 or more warps a row at 8 chunks) want few bytes in flight: the fused op
-    //    runs one group of up to 16 warps with 4 ring slots, the no-residual variant 4 groups
-    //    with one slot each;
-    //  - shorter rows take as many groups as the warp budget allows, but no more than keeps
-    //    5 (fused) or 8 (variant) rows per group per SM, with one (fused) or two (variant)
-    //    slots per group;
-    //  - with an fp32 output, the groups keep about 128 KB (fused) or 120 KB (variant) of
-    //    rows in progress per SM, one slot each.
+    // Launch table, from sweeps of chunks a thread x groups x ring slots on GB300, timed
+    // after an L2 flush and back to back (where each launch writes back its predecessor's
+    // output still in L2):
+    //  - at most 2 rows an SM: one group spreading each row over as many warps as it has chunks;
+    //  - otherwise 8 chunks a thread (64 values of 16-bit data) keeps the per-row work
+    //    (reductions, IEEE divide and square root, waits) small against the per-element
+    //    work, with 5, 6, 10 or 4 chunks where 8 would leave lanes idle;
+    //  - the groups keep a measured amount of rows in flight per SM: ~70 KB (fused RMSNorm),
+    //    ~64 KB (fused LayerNorm), 128 / 120 KB (fp32 output, fused / variant), a fitted
+    //    count for the no-residual RMSNorm variant; the quantised output as many groups as
+    //    the warps hold;
+    //  - the warp budget: 12 warps at 8 chunks (128 registers), 16 below, 19 for the
+    //    no-residual variant on 16-bit rows (x kept packed: 96 registers).
+    // Each branch below states its own rule and measurements.
     const int64_t C = row_bytes / 16;
     // packed x leaves room for 19 warps (96 registers a thread), also with a quantised
     // output, whose kept outputs take the registers of the consumed x; LayerNorm keeps the
@@ -418,20 +421,23 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
         group_cap = kMaxConsumerWarps / G;
         slots_per_group = G >= 8 ? 1 : 2;
       }
-    } else if (G >= 4) {
-      if (c.residual) {
-        nch = 1;
-        while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
-        G = (int)((C + 32LL * nch - 1) / (32LL * nch));
-        one_group = true;
-      } else {
-        group_cap = 4;
-        slots_per_group = 1;
-      }
+    } else if (c.residual && C <= 128) {
+      // fused rows of one warp at up to 4 chunks a thread (hidden up to 1024 in 16-bit):
+      // 7 groups of 2 slots (one slot at most 16 rows an SM), measured 7-10 % faster than
+      // a cap of 5 rows a group an SM, back to back and after a flush
+      group_cap = 7;
+      slots_per_group = rows_per_sm <= 16 ? 1 : 2;
+    } else if (c.residual) {
+      // fused rows longer than 12 warps at 8 chunks (hidden above 24576 in 16-bit): beyond
+      // the 12-warp budget of 8 chunks, so the check below sends them to the generic kernel
+      nch = 1;
+      while ((C + 32LL * nch - 1) / (32LL * nch) > kMaxConsumerWarps && nch < 8) nch *= 2;
+      G = (int)((C + 32LL * nch - 1) / (32LL * nch));
+      one_group = true;
     } else {
-      const int64_t per_group = c.residual ? 5 : 8;
-      const int64_t cap = rows_per_sm / per_group;
-      group_cap = (int)(cap < 1 ? 1 : cap);
+      // (every variant is taken above; kept as a safe default) 4 groups of one slot
+      group_cap = 4;
+      slots_per_group = 1;
     }
     // A row that 8 chunks a thread cover with idle lanes but 6 or 5 chunks cover exactly with
     // the same number of warps (hidden 2560 or 3072 in 16-bit) takes the exact plan: measured
