@@ -572,11 +572,18 @@ GemmPlan plan_gemm(const GemmCall& c, int sms, int max_pairs) {
     }
   }
   if (tc && force != 1) {
-    int bn = 64;
-    for (int cand : {256, 128}) {
-      if (tiles_m * ((c.N + cand - 1) / cand) >= sms) {
+    // the tile width with the least estimated time: its waves x the width x the width's
+    // cost a column (measured: 64-wide tiles ~1.5x a 128-wide tile's, 256-wide ~0.9x); at
+    // 1536 x 1536 x 4096, 144 tiles of 128 in one wave run 25 us, 288 of 64 in two 37 us
+    int bn = 256;
+    double best = 1e300;
+    for (int cand : {256, 128, 64}) {
+      const int64_t tiles = tiles_m * ((c.N + cand - 1) / cand);
+      const double eff = cand == 256 ? 0.9 : cand == 128 ? 1.0 : 1.5;
+      const double cost = (double)((tiles + sms - 1) / sms) * cand * eff;
+      if (cost < best) {
+        best = cost;
         bn = cand;
-        break;
       }
     }
     if (g_gemm_force_bn.load() > 0) bn = g_gemm_force_bn.load();

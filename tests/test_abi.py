@@ -310,9 +310,14 @@ def test_gemm_plans(far):
     assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["kind"] == 2
     assert far.plan_gemm_for_sms(2048, 2048, 8192, True, T16, 152)["kind"] == 2
     assert far.plan_gemm_for_sms(1024, 1024, 4096, True, T16, 152)["kind"] == 0  # 16 pair tiles: one CTA a tile
+    # one CTA a tile: the width of least estimated time (waves x width x the width's cost a
+    # column): 144 tiles of 128 in one wave rather than 288 of 64 in two
+    p = far.plan_gemm_for_sms(1536, 1536, 4096, True, T16, 152)
+    assert p["kind"] == 0 and p["bn"] == 128 and p["grid"] == 144
+    assert far.plan_gemm_for_sms(1024, 2048, 2048, True, T16, 152)["bn"] == 128
     try:
-        far.set_gemm_override(0, 0)  # one CTA a tile: the widest width that still gives a tile per SM
-        assert far.plan_gemm_for_sms(1024, 4096, 4096, True, T16, 152)["bn"] == 128  # 8 x 16 tiles of 256 < 152
+        far.set_gemm_override(0, 0)
+        assert far.plan_gemm_for_sms(4096, 2048, 4096, True, T16, 152)["bn"] == 256
     finally:
         far.set_gemm_override()
     for m, n, k in [(100, 8, 8), (1, 8, 4096), (5000, 1000, 64)]:
