@@ -128,6 +128,43 @@ def test_every_plan_gives_the_same_bits(far):
         far.set_launch_override()
 
 
+@pytest.mark.parametrize("act", ["f16", "f32"])
+def test_fp16_weight_extremes_every_plan(far, act):
+    """fp16 gamma and beta at the fp16 extremes (largest finite, smallest subnormal, signed
+    zeros, infinity): the generic kernel and staged plans of 1 to 8 chunks a thread give one
+    set of bits, fused and not, with fp16 and binary32 x, and pass the oracle's gate."""
+    d = with_beta(far_gen.custom_inputs(act, "f16", 96, 8192, seed=44, scale_lo=1e-2, scale_hi=60))
+    w, b = d["w"].clone(), d["b"].clone()
+    ext = torch.tensor([65504.0, -65504.0, 2.0 ** -24, -(2.0 ** -24), 2.0 ** -14, 0.0, -0.0, 1.0, 1024.5,
+                        float("inf")], dtype=torch.float16)
+    w[: 4 * len(ext)] = ext.repeat(4)
+    b[: 4 * len(ext)] = ext.flip(0).repeat(4)
+    b[100:140] = torch.tensor([65504.0, -(2.0 ** -24), -0.0, 3.0e-5], dtype=torch.float16).repeat(10)
+    d = dict(d, w=w, b=b)
+    for residual in (True, False):
+        ref = None
+        try:
+            for plan in [(1, 0, 0, 0), (0, 1, 0, 0), (0, 2, 0, 0), (0, 4, 1, 2), (0, 4, 3, 3), (0, 8, 1, 0),
+                         (0, 8, 2, 4)]:
+                far.set_launch_override(*plan)
+                got = run_ln(far, d, residual)
+                if ref is None:
+                    ref = got
+                    if residual:
+                        ro, rr = oracle.fused_add_layernorm(d["x"], d["r"], d["w"], d["b"], d["eps"], d["act"],
+                                                            d["wd"])
+                        gate(got[0], ro, got[1], rr, where=f"{act}/f16 extremes fused")
+                    else:
+                        gate(got[0], oracle.layernorm(d["x"], d["w"], d["b"], d["eps"], d["act"], d["wd"]),
+                             where=f"{act}/f16 extremes")
+                else:
+                    assert bits_equal(got[0], ref[0]), (residual, plan)
+                    if residual:
+                        assert bits_equal(got[1], ref[1]), (residual, plan)
+        finally:
+            far.set_launch_override()
+
+
 @pytest.mark.parametrize("offset", [1, 3])
 def test_misaligned_buffers(far, offset):
     d = with_beta(far_gen.custom_inputs("bf16", "bf16", 40, 1000, seed=offset))
