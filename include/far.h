@@ -344,6 +344,29 @@ int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_re
 int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int beta_offset, int sms,
                         int* out8);
 
+/*
+ * far_set_row_schedule: process-wide choice of how the staged kernel's CTAs share
+ * rows.  Each CTA first takes rows at a fixed stride (its own index, plus the grid size
+ * each time), as many as its shared-memory ring holds; after that it either keeps the
+ * stride or claims the next free rows, a few at a time, from a counter of the launch
+ * (library-owned device memory, 64 counters a device; a counter is handed to a new
+ * launch only after an event shows the previous launch that had it has finished, so
+ * launches running side by side never share one).  Claimed rows keep the CTAs that the
+ * memory system serves faster busy until the last rows, instead of idling them while
+ * slower ones finish.  A claim takes as many rows as keep the claims below ~150 M/s at
+ * the copy rate (one row where a row moves 45 KB or more).  mode 0 (default): claimed
+ * rows where a claim takes one or two rows, the rows left after the first ring-full of
+ * every CTA are at least as many again, the stream is not capturing a graph and a
+ * counter is free; 1: the fixed stride always; 2: claimed rows whenever there are rows
+ * left to claim (and a counter is free, and the stream is not capturing).  The results
+ * are the same bits in every mode (each row is computed the same way by whichever CTA
+ * takes it).  Returns FAR_ERR_SHAPE for another mode.
+ */
+int far_set_row_schedule(int mode);
+/* 1 if the calling thread's last kernel launch by this library claimed rows from a
+   counter, else 0 (fixed-stride rows, the generic kernel, or no launch) */
+int far_last_launch_claimed_rows(void);
+
 #ifdef __cplusplus
 }
 #endif

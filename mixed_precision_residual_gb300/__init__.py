@@ -102,6 +102,10 @@ lib.far_selftest_wait_timeout.argtypes = [_u32, _vp]
 lib.far_selftest_wait_timeout.restype = _int
 lib.far_set_launch_override.argtypes = [_int, _int, _int, _int]
 lib.far_set_launch_override.restype = _int
+lib.far_set_row_schedule.argtypes = [_int]
+lib.far_set_row_schedule.restype = _int
+lib.far_last_launch_claimed_rows.argtypes = []
+lib.far_last_launch_claimed_rows.restype = _int
 lib.far_describe_launch.argtypes = [_i64, _i64, _int, _int, _vp]
 lib.far_describe_launch.restype = _int
 lib.far_plan_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _vp]
@@ -246,6 +250,17 @@ def selftest_wait_timeout(timeout_us: int = 20000, stream=None) -> None:
 
 def set_launch_override(kind: int = -1, nch: int = 0, groups: int = 0, stages: int = 0) -> None:
     _check(lib.far_set_launch_override(kind, nch, groups, stages))
+
+
+def set_row_schedule(mode: int = 0) -> None:
+    """How the staged kernel's CTAs share rows: 0 automatic, 1 fixed stride, 2 claimed rows
+    whenever possible (the same bits in every mode)."""
+    _check(lib.far_set_row_schedule(mode))
+
+
+def last_launch_claimed_rows() -> bool:
+    """Whether this thread's last launch by the library claimed rows from a counter."""
+    return bool(lib.far_last_launch_claimed_rows())
 
 
 def describe_launch(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool = True) -> dict:

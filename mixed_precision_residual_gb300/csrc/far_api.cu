@@ -21,6 +21,11 @@ namespace far {
 // bounded wait.  Read and cleared by far_device_status.
 __device__ unsigned int g_status;
 
+// Row counters of the staged kernel's claimed rows: pairs {next claim, CTAs done}, zero
+// while free (each launch's last CTA zeroes its pair).
+constexpr int kSchedSlots = 64;
+__device__ unsigned long long g_sched[kSchedSlots][2];
+
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -39,6 +44,94 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// The counter pairs of a device, each handed to one launch at a time: a pair is given out
+// again only once the event recorded after its last launch has completed (that launch's
+// last CTA has zeroed it by then), so launches running side by side on different streams
+// never share one. No pair during stream capture (a captured event cannot be polled) or
+// when all are busy: the launch takes fixed-stride rows.
+struct SchedPool {
+  std::mutex mu;
+  bool ready = false, broken = false;
+  unsigned long long* pairs = nullptr;  // device address of g_sched on this device
+  cudaEvent_t ev[kSchedSlots] = {};
+  bool used[kSchedSlots] = {};     // launched at least once: wait for ev before reuse
+  bool pending[kSchedSlots] = {};  // handed out, its event not yet recorded
+  bool retired[kSchedSlots] = {};  // its event could not be recorded: never reused
+  int next = 0;
+};
+SchedPool g_sched_pool[kMaxDevices];
+
+// row schedule: 0 automatic, 1 fixed stride always, 2 claimed rows whenever a pair is free
+std::atomic<int> g_row_schedule{0};
+thread_local int g_last_claimed = 0;  // this thread's last staged launch claimed rows
+
+// a free counter pair for a launch on `stream`, or -1
+int sched_acquire(int dev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  if (cs != cudaStreamCaptureStatusNone) return -1;
+  SchedPool& sp = g_sched_pool[dev];
+  std::lock_guard<std::mutex> lk(sp.mu);
+  if (sp.broken) return -1;
+  // polling events is a call that a capture in global mode on another thread forbids:
+  // relax this thread's mode for the pool's own calls
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  int got = -1;
+  if (!sp.ready) {
+    void* addr = nullptr;
+    bool ok = cudaGetSymbolAddress(&addr, g_sched) == cudaSuccess;
+    for (int i = 0; ok && i < kSchedSlots; ++i)
+      ok = cudaEventCreateWithFlags(&sp.ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (ok) {
+      sp.pairs = static_cast<unsigned long long*>(addr);
+      sp.ready = true;
+    } else {
+      cudaGetLastError();
+      sp.broken = true;
+    }
+  }
+  for (int i = 0; sp.ready && i < kSchedSlots && got < 0; ++i) {
+    const int s = (sp.next + i) % kSchedSlots;
+    if (sp.pending[s] || sp.retired[s]) continue;
+    if (sp.used[s]) {
+      const cudaError_t e = cudaEventQuery(sp.ev[s]);
+      if (e != cudaSuccess) {
+        if (e != cudaErrorNotReady) cudaGetLastError();
+        continue;
+      }
+    }
+    got = s;
+  }
+  if (got >= 0) {
+    sp.pending[got] = true;
+    sp.next = (got + 1) % kSchedSlots;
+  }
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  return got;
+}
+
+// after the launch that used pair `s` (launched: the kernel was enqueued)
+void sched_release(int dev, int s, cudaStream_t stream, bool launched) {
+  SchedPool& sp = g_sched_pool[dev];
+  std::lock_guard<std::mutex> lk(sp.mu);
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  if (launched) {
+    if (cudaEventRecord(sp.ev[s], stream) == cudaSuccess) {
+      sp.used[s] = true;
+    } else {
+      cudaGetLastError();
+      sp.retired[s] = true;
+    }
+  }
+  sp.pending[s] = false;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+}
 
 thread_local char g_cuda_msg[256] = "CUDA error";
 
@@ -539,10 +632,29 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
 }
 
 int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
+  g_last_claimed = 0;
   if (c.tokens == 0) return FAR_OK;
   Launch L;
   int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
+  // Rows a claim: as few as keep the claims below ~150 M/s at the copy rate (~6.8 TB/s),
+  // well under the ~250 M/s that one counter's atomics were measured to sustain on GB300.
+  // Claimed rows by default where that is one or two rows (rows moving 23 KB or more) and
+  // at least as many rows are left after every CTA's first ring-full as those take: on
+  // shorter rows the fixed stride was as fast or faster; forced, wherever rows are left.
+  const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od)));
+  const int64_t run = (45333 + row_traffic - 1) / row_traffic;
+  const int mode = g_row_schedule.load();
+  const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
+  int pair = -1;
+  const int devno = (int)(&dev - g_dev);
+  if (L.kind == kStaged && mode != 1 && (mode == 2 ? c.tokens > r0 : (run <= 2 && c.tokens >= 2 * r0))) {
+    pair = sched_acquire(devno, stream);
+    if (pair >= 0) {
+      L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
+      L.p.sched_run = (int32_t)(run < (1 << 20) ? run : (1 << 20));
+    }
+  }
   cudaError_t e;
   if (c.ln) {
     switch (c.act) {
@@ -563,6 +675,8 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
       default: e = launch_act_f32(c.wd, c.residual, L); break;
     }
   }
+  if (pair >= 0) sched_release(devno, pair, stream, e == cudaSuccess);
+  g_last_claimed = pair >= 0 && e == cudaSuccess;
   return e == cudaSuccess ? FAR_OK : cuda_fail(e);
 }
 
@@ -1017,6 +1131,14 @@ int far_set_launch_override(int kind, int nch, int groups, int stages) {
   g_force_stages = stages;
   return FAR_OK;
 }
+
+int far_set_row_schedule(int mode) {
+  if (mode < 0 || mode > 2) return FAR_ERR_SHAPE;
+  g_row_schedule = mode;
+  return FAR_OK;
+}
+
+int far_last_launch_claimed_rows(void) { return g_last_claimed; }
 
 int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int sms, int* out8) {
   // kind, nch, warps per row, groups, stages, grid, threads per CTA, dynamic shared bytes

@@ -69,11 +69,14 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
 
   extern __shared__ __align__(128) unsigned char smem[];
   const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
-  // layout: full[stages] | empty[stages] | reduce[groups][NRED] | partials[groups][NRED][G] | w | ring
+  // layout: full[stages] | empty[stages] | reduce[groups][NRED] | partials[groups][NRED][G] |
+  //         slot_row[stages] | w | ring
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float2* partials = reinterpret_cast<float2*>(smem + (size_t)(2 * stages + NRED * groups) * 8);
+  int64_t* slot_row = reinterpret_cast<int64_t*>(partials + (size_t)groups * NRED * G);  // -1: no more rows
   const size_t head =
-      ((size_t)(2 * stages + NRED * groups) * 8 + (size_t)groups * NRED * G * 8 + 127) / 128 * 128;
+      ((size_t)(2 * stages + NRED * groups) * 8 + (size_t)groups * NRED * G * 8 + (size_t)stages * 8 + 127) /
+      128 * 128;
   unsigned char* wsm = smem + head;
   unsigned char* ring = wsm + (p.w_smem_bytes + 127) / 128 * 128;
   const uint32_t r_off = (p.row_bytes + 127u) & ~127u;  // residual row inside a slot
@@ -86,14 +89,22 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     if (threadIdx.x == 0) atomicOr(p.status, 1u << FAR_ERR_SHAPE);
     return;
   }
+  // Rows enter the ring in this order: first the CTA's fixed-stride rows b + k * nb (all of
+  // them; or, with a row counter, only those with k < stages), then runs of n rows R0 + c ..
+  // R0 + c + n - 1, R0 = nb * stages, n = sched_run, each claimed by one atomic add of n to
+  // the launch's counter (which returns c), until the claims pass the last row. The CTAs
+  // that are served faster take more rows, all finish within a run of each other, and at
+  // any time they all work in one window of neighbouring rows.
   const int64_t b = blockIdx.x, nb = gridDim.x;
-  const int64_t n_local = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
+  int64_t n_static = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
+  if (p.sched != nullptr && n_static > stages) n_static = stages;
   const uint32_t tx = RES ? 2u * p.row_bytes : p.row_bytes;
-  const int64_t first = n_local < stages ? n_local : stages;  // rows issued before the weight load
+  const int64_t first = n_static < stages ? n_static : stages;  // rows issued before the weight load
 
-  // producer: one bulk copy of row k's x (and residual) into ring slot k % stages
-  auto issue = [&](int64_t k, int slot) {
-    const int64_t row = b + k * nb;
+  // producer: the row number into slot_row[slot] (read by the slot's consumers after the
+  // full barrier), then one bulk copy of the row's x (and residual) into the slot
+  auto issue = [&](int64_t row, int slot) {
+    slot_row[slot] = row;
     const uint32_t full = smem_addr(&bars[slot]);
     const uint32_t dst = smem_addr(ring + (size_t)slot * p.stage_bytes);
     mbar_arrive_expect_tx(full, tx);
@@ -109,7 +120,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     for (int i = 0; i < NRED * groups; ++i) mbar_init(smem_addr(&bars[2 * stages + i]), G);
     fence_barrier_init();
     // the first `stages` rows need no free slot: start them now, under the weight load
-    for (int64_t k = 0; k < first; ++k) issue(k, (int)k);
+    for (int64_t k = 0; k < first; ++k) issue(b + k * nb, (int)k);
   }
   // LayerNorm's shift row sits right after the scale row in shared memory
   unsigned char* bsm = wsm + (size_t)((p.hidden * SW + 15) / 16 * 16);
@@ -131,19 +142,56 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
   if (warp == 0) {
     // ---------------- producer ----------------
     if (lane == 0) {
-      int64_t k = first;
+      int64_t k = first;  // ring positions filled: position k goes to slot k % stages
       int slot = (int)(first % stages);
       uint32_t phase = (uint32_t)(first / stages) & 1u;  // (k / stages) & 1
-      for (; k < n_local; ++k) {
-        // slot k % stages was last used by row k - stages: wait until its consumers released it
-        if (!mbar_wait(smem_addr(&bars[stages + slot]), phase ^ 1u, p.timeout_ns, p.status)) break;
-        issue(k, slot);
+      // fill position k with `row` (-1: the end marker of the group that owns position k)
+      auto put = [&](int64_t row) -> bool {
+        // slot k % stages last held position k - stages: wait until its consumers released it
+        if (k >= stages && !mbar_wait(smem_addr(&bars[stages + slot]), phase ^ 1u, p.timeout_ns, p.status))
+          return false;
+        if (row >= 0) {
+          issue(row, slot);
+        } else {
+          slot_row[slot] = -1;
+          mbar_arrive(smem_addr(&bars[slot]));  // completes the phase: no bytes to wait for
+        }
+        ++k;
         if (++slot == stages) {
           slot = 0;
           phase ^= 1u;
         }
+        return true;
+      };
+      bool ok = true;
+      for (int64_t i = first; ok && i < n_static; ++i) ok = put(b + i * nb);
+      if (p.sched != nullptr) {
+        const int64_t R0 = nb * stages;
+        const unsigned long long n = p.sched_run > 1 ? (unsigned long long)p.sched_run : 1ull;
+        // the next run is claimed while this one is issued (its atomic's latency hidden); a
+        // thread's adds to one address are ordered, so every run after a spent one is spent
+        unsigned long long c0 = atomicAdd(p.sched, n), c1 = atomicAdd(p.sched, n);
+        while (ok && R0 + (int64_t)c0 < p.tokens) {
+          int64_t end = R0 + (int64_t)(c0 + n);
+          if (end > p.tokens) end = p.tokens;
+          for (int64_t row = R0 + (int64_t)c0; ok && row < end; ++row) ok = put(row);
+          c0 = c1;
+          if (R0 + (int64_t)c0 >= p.tokens) break;
+          c1 = atomicAdd(p.sched, n);
+        }
+        // this CTA claims no more: count it done; the last one leaves the pair zero for the
+        // next launch that is given it (every claim of this launch precedes the reset)
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)nb - 1) {
+          atomicExch(p.sched, 0ull);
+          atomicExch(p.sched + 1, 0ull);
+        }
       }
-      // the copies of the last (at most `stages`) rows must have landed before the CTA may exit
+      // an end marker at each group's next position (positions k .. k + groups - 1 belong
+      // to distinct groups: stages is a multiple of groups)
+      for (int i = 0; ok && i < groups; ++i) ok = put(-1);
+      // the copies of the last (at most `stages`) positions must have landed before the CTA
+      // may exit
       for (int64_t j = (k > stages ? k - stages : 0); j < k; ++j)
         mbar_wait(smem_addr(&bars[j % stages]), (uint32_t)(j / stages) & 1u, p.timeout_ns, p.status);
     }
@@ -156,11 +204,13 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
   const int C = p.chunks;
   int G8 = 1;  // G rounded up to a power of two (<= 16): the lanes of the cross-warp butterfly
   while (G8 < G) G8 <<= 1;
-  int slot = g;          // k % stages (g < groups <= stages)
+  int slot = g;          // k % stages for this group's positions k = g, g + groups, ...
   uint32_t phase = 0;    // (k / stages) & 1
   uint32_t it = 0;       // this group's row count, for the reduction buffers
-  for (int64_t k = g; k < n_local; k += groups, ++it) {
+  for (;; ++it) {
     if (!mbar_wait(smem_addr(&bars[slot]), phase, p.timeout_ns, p.status)) return;
+    const int64_t row = slot_row[slot];  // read before the slot is released
+    if (row < 0) return;                 // the group's end marker
     const unsigned char* xs = ring + (size_t)slot * p.stage_bytes;
 
     // pass 1 (from shared memory): s = fl32(x + r) into registers, squares into the accumulator
@@ -224,7 +274,6 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       phase ^= 1u;
     }
 
-    const int64_t row = b + k * nb;
     float rstd;
     if constexpr (LN) {
       // LayerNorm: mean from the exact-per-addition signed sum; then d = s - mean in place,

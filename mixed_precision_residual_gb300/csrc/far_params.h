@@ -56,6 +56,10 @@ struct Params {
   float* scale;          // per-row scale [tokens] (quantised variants)
   unsigned int* status;  // device error word
   uint64_t timeout_ns;
+  // staged kernel: this launch's row counter pair {next row claim, CTAs done}, zero at
+  // launch and left zero by the launch's last CTA; null: every CTA takes a fixed stride
+  unsigned long long* sched;
+  int32_t sched_run;     // rows taken per claim from sched (>= 1)
 };
 
 enum Kind { kStaged = 0, kGeneric = 1 };
@@ -85,7 +89,8 @@ inline size_t staged_smem_bytes(int stages, int groups, int warps_per_row, uint3
   const int nred = reduce_buffers(q, ln);
   size_t bars = (size_t)(2 * stages + nred * groups) * 8;
   size_t red = (size_t)groups * nred * warps_per_row * 8;
-  size_t head = (bars + red + 127) / 128 * 128;
+  size_t rows = (size_t)stages * 8;  // the row held by each ring slot
+  size_t head = (bars + red + rows + 127) / 128 * 128;
   return head + (w_smem_bytes + 127) / 128 * 128 + (size_t)stages * stage_bytes;
 }
 
