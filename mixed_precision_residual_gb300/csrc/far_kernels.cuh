@@ -4,7 +4,9 @@
 // staged_kernel -- the hot path.  Persistent (one CTA per SM), warp-specialised:
 //   warp 0, lane 0 (producer) bulk-copies each row of x and of the residual into
 //   a ring of shared-memory slots (cp.async.bulk, mbarrier completion, plain
-//   copies into the CTA's own shared memory);
+//   copies into the CTA's own shared memory), at a fixed stride over the rows
+//   for the first ring-full and then, given a row counter, in runs claimed from
+//   it, so that CTAs served faster take more rows;
 //   `groups` groups of G consumer warps each take a row from the ring: every
 //   thread widens its 16-byte chunks, forms s = fl32(x + r) and keeps s in
 //   registers, accumulates the squares, releases the slot, reduces across the

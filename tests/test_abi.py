@@ -106,6 +106,22 @@ def test_zero_tokens_is_a_noop(far):
     assert far.lib.rmsnorm(None, None, 1e-6, None, 0, 128, code("f32", "f32"), None) == 0
 
 
+def test_row_schedule_hook(far):
+    """far_set_row_schedule takes 0, 1 or 2 and refuses anything else (FAR_ERR_SHAPE);
+    nothing launched on this thread means no rows claimed (a zero-token call launches
+    nothing)."""
+    try:
+        for mode in (0, 1, 2):
+            assert far.lib.far_set_row_schedule(mode) == 0
+        for mode in (-1, 3, 1 << 20):
+            assert far.lib.far_set_row_schedule(mode) == 4
+    finally:
+        assert far.lib.far_set_row_schedule(0) == 0
+    assert far.lib.fused_add_rmsnorm(FAKE, FAKE, FAKE, 1e-6, FAKE, FAKE, 0, 64, code("bf16", "bf16"), None) == 0
+    assert far.lib.far_last_launch_claimed_rows() == 0
+    assert far.last_launch_claimed_rows() is False
+
+
 def test_host_workspace_size(far):
     n1 = far.lib.far_host_workspace_bytes(1, 4096, code("bf16", "f32"), 1)
     n8 = far.lib.far_host_workspace_bytes(8, 4096, code("bf16", "f32"), 1)
