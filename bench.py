@@ -515,6 +515,14 @@ def main():
 
     for _ in range(max(3, args.warmup)):
         step()
+    # the row schedule of each kernel (the flag of this thread's last launch), outside the
+    # timed region
+    if fused():
+        raise RuntimeError("fused launch failed")
+    rows_fused = far.last_launch_claimed_rows()
+    if variant():
+        raise RuntimeError("variant launch failed")
+    rows_variant = far.last_launch_claimed_rows()
     torch.cuda.synchronize()
     assert far.device_status() == 0
 
@@ -651,7 +659,9 @@ def main():
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": f"staged_kernel ({kernel_name})", "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": fb, "avg_launch_ms": round(fused_ms, 5),
-                     "launch_plan": plan},
+                     "launch_plan": plan,
+                     "row_schedule": {k: ("rows claimed from a per-launch counter" if v else "fixed stride")
+                                      for k, v in (("fused", rows_fused), ("variant", rows_variant))}},
         "clocks": clk,
         "e2e": e2e,
     }
