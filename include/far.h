@@ -349,9 +349,9 @@ int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_resid
  * rows.  Each CTA first takes rows at a fixed stride (its own index, plus the grid size
  * each time), as many as its shared-memory ring holds; after that it either keeps the
  * stride or claims the next free rows, a few at a time, from a counter of the launch
- * (library-owned device memory, 64 counters a device; a counter is handed to a new
- * launch only after an event shows the previous launch that had it has finished, so
- * launches running side by side never share one).  Claimed rows keep the CTAs that the
+ * (library-owned device memory, 64 counters a device; a launch takes the counter of
+ * earlier launches on its own stream, which run before it, or one whose last launch an
+ * event shows finished, so launches that can run side by side never share one).  Claimed rows keep the CTAs that the
  * memory system serves faster busy until the last rows, instead of idling them while
  * slower ones finish.  A claim takes as many rows as keep the claims below ~150 M/s at
  * the copy rate (one row where a row moves 45 KB or more).  mode 0 (default): claimed

@@ -45,19 +45,24 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// The counter pairs of a device, each handed to one launch at a time: a pair is given out
-// again only once the event recorded after its last launch has completed (that launch's
-// last CTA has zeroed it by then), so launches running side by side on different streams
-// never share one. No pair during stream capture (a captured event cannot be polled) or
-// when all are busy: the launch takes fixed-stride rows.
+// The counter pairs of a device. A launch on stream S may take a pair whose launches still
+// pending are all on S: S runs them in order, so each has left the pair zero before the next
+// starts. Otherwise it takes a pair with no launch pending whose event (recorded after its
+// last launch) has completed. So launches that can run side by side (different streams)
+// never share a pair, while a stream with many launches queued keeps claiming rows. Streams
+// are told apart by their context-unique id, not their handle (a destroyed stream's handle
+// can come back; every thread's per-thread default stream has one handle). No pair during
+// stream capture (a captured event cannot be polled) or when all are busy: the launch takes
+// fixed-stride rows.
 struct SchedPool {
   std::mutex mu;
   bool ready = false, broken = false;
   unsigned long long* pairs = nullptr;  // device address of g_sched on this device
   cudaEvent_t ev[kSchedSlots] = {};
-  bool used[kSchedSlots] = {};     // launched at least once: wait for ev before reuse
-  bool pending[kSchedSlots] = {};  // handed out, its event not yet recorded
-  bool retired[kSchedSlots] = {};  // its event could not be recorded: never reused
+  unsigned long long stream_id[kSchedSlots] = {};  // the stream of its pending launches
+  int pending[kSchedSlots] = {};   // handed out, event not yet recorded after the launch
+  bool used[kSchedSlots] = {};     // launched at least once: its event shows the last launch
+  bool retired[kSchedSlots] = {};  // an event could not be recorded: never handed out again
   int next = 0;
 };
 SchedPool g_sched_pool[kMaxDevices];
@@ -66,8 +71,10 @@ SchedPool g_sched_pool[kMaxDevices];
 std::atomic<int> g_row_schedule{0};
 thread_local int g_last_claimed = 0;  // this thread's last staged launch claimed rows
 
-// a free counter pair for a launch on `stream`, or -1
+// a counter pair for a launch on `stream`, or -1
 int sched_acquire(int dev, cudaStream_t stream) {
+  // a capturing stream gets no pair, and no other call: one (the stream's id) was seen to
+  // invalidate the capture
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
     cudaGetLastError();
@@ -82,6 +89,12 @@ int sched_acquire(int dev, cudaStream_t stream) {
   cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
   cudaThreadExchangeStreamCaptureMode(&mode);
   int got = -1;
+  unsigned long long sid = 0;
+  if (cudaStreamGetId(stream, &sid) != cudaSuccess) {
+    cudaGetLastError();
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    return -1;
+  }
   if (!sp.ready) {
     void* addr = nullptr;
     bool ok = cudaGetSymbolAddress(&addr, g_sched) == cudaSuccess;
@@ -95,9 +108,13 @@ int sched_acquire(int dev, cudaStream_t stream) {
       sp.broken = true;
     }
   }
+  // a pair last given to this stream (whatever is pending on it runs before this launch)
+  for (int s = 0; sp.ready && s < kSchedSlots && got < 0; ++s)
+    if (!sp.retired[s] && (sp.used[s] || sp.pending[s] > 0) && sp.stream_id[s] == sid) got = s;
+  // else a pair nothing is pending on, whose last launch has finished
   for (int i = 0; sp.ready && i < kSchedSlots && got < 0; ++i) {
     const int s = (sp.next + i) % kSchedSlots;
-    if (sp.pending[s] || sp.retired[s]) continue;
+    if (sp.pending[s] > 0 || sp.retired[s]) continue;
     if (sp.used[s]) {
       const cudaError_t e = cudaEventQuery(sp.ev[s]);
       if (e != cudaSuccess) {
@@ -106,16 +123,18 @@ int sched_acquire(int dev, cudaStream_t stream) {
       }
     }
     got = s;
+    sp.next = (s + 1) % kSchedSlots;
   }
   if (got >= 0) {
-    sp.pending[got] = true;
-    sp.next = (got + 1) % kSchedSlots;
+    sp.stream_id[got] = sid;
+    ++sp.pending[got];
   }
   cudaThreadExchangeStreamCaptureMode(&mode);
   return got;
 }
 
-// after the launch that used pair `s` (launched: the kernel was enqueued)
+// after the launch that used pair `s` (launched: the kernel was enqueued). The event is
+// recorded after the launch, so once no launch is pending it follows all of them.
 void sched_release(int dev, int s, cudaStream_t stream, bool launched) {
   SchedPool& sp = g_sched_pool[dev];
   std::lock_guard<std::mutex> lk(sp.mu);
@@ -129,7 +148,7 @@ void sched_release(int dev, int s, cudaStream_t stream, bool launched) {
       sp.retired[s] = true;
     }
   }
-  sp.pending[s] = false;
+  --sp.pending[s];
   cudaThreadExchangeStreamCaptureMode(&mode);
 }
 
