@@ -4,7 +4,8 @@ way by whichever CTA takes it). Claimed rows must also survive:
 - launches back to back (each launch's last CTA must leave its counter zero, or the next
   launch given it would skip rows);
 - launches side by side on two streams (they must never share a counter);
-- more launches in flight than counters (the rest take the fixed stride);
+- more launches in flight on one stream than counters (they share the stream's counter),
+  and more streams than counters (the rest take the fixed stride);
 - graph capture (the fixed stride: a captured event cannot be polled).
 Outputs start as NaN (0xFF bytes for quantised codes), so a row nobody wrote shows."""
 import pytest
@@ -158,8 +159,9 @@ def test_two_streams_side_by_side(far):
 
 
 def test_more_launches_in_flight_than_counters(far):
-    """100 launches queued without a wait: once every counter is taken the rest keep the
-    fixed stride; all results equal the reference."""
+    """100 launches queued on one stream without a wait (more than the 64 counters): they
+    share their stream's counter, which the stream's order keeps apart, so every one claims
+    rows; all results equal the reference."""
     _, t = _inputs("bf16", "bf16", 4096, 4096, seed=21)
     try:
         far.set_row_schedule(1)
@@ -171,9 +173,32 @@ def test_more_launches_in_flight_than_counters(far):
             claimed += far.last_launch_claimed_rows()
         torch.cuda.synchronize()
         assert far.device_status() == 0
-        assert claimed >= 1
+        assert claimed == 100
         for got in outs:
             assert _same(got, ref)
+    finally:
+        far.set_row_schedule(0)
+
+
+def test_more_streams_than_counters(far):
+    """One launch on each of 70 streams, queued without a wait: a stream finds no counter of
+    its own, so it takes one that no launch is pending on and whose last launch has
+    finished, or keeps the fixed stride; every result equals the reference."""
+    _, t = _inputs("bf16", "bf16", 2048, 4096, seed=41)
+    try:
+        far.set_row_schedule(1)
+        ref = _run(far, "rms_fused", t)
+        far.set_row_schedule(2)
+        streams = [torch.cuda.Stream() for _ in range(70)]
+        torch.cuda.synchronize()
+        outs = []
+        for s in streams:
+            with torch.cuda.stream(s):
+                outs.append(_run(far, "rms_fused", t, stream=s))
+        torch.cuda.synchronize()
+        assert far.device_status() == 0
+        for got in outs:
+            assert _same(got, ref), "a launch lost rows to another stream's launch"
     finally:
         far.set_row_schedule(0)
 
