@@ -257,6 +257,8 @@ struct Call {
   float* scale = nullptr;
   bool ln = false;            // LayerNorm: gamma in w, beta [hidden] in the weight dtype
   const void* beta = nullptr;
+  bool fixed_stride = false;  // never claim rows (no counter pair, no event: the
+                              // allocation-free entry point creates and records none)
 };
 
 int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
@@ -667,7 +669,8 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
   int pair = -1;
   const int devno = (int)(&dev - g_dev);
-  if (L.kind == kStaged && mode != 1 && (mode == 2 ? c.tokens > r0 : (run <= 2 && c.tokens >= 2 * r0))) {
+  if (L.kind == kStaged && !c.fixed_stride && mode != 1 &&
+      (mode == 2 ? c.tokens > r0 : (run <= 2 && c.tokens >= 2 * r0))) {
     pair = sched_acquire(devno, stream);
     if (pair >= 0) {
       L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
@@ -700,10 +703,12 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
 }
 
 int run(const void* x, const void* r, const void* w, float eps, void* out, void* res_out, int64_t tokens,
-        int64_t hidden, int dtype, bool residual, void* stream, const Strides* strides = nullptr) {
+        int64_t hidden, int dtype, bool residual, void* stream, const Strides* strides = nullptr,
+        bool fixed_stride = false) {
   Call c;
   int st = validate(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, c, strides);
   if (st != FAR_OK || tokens == 0) return st;
+  c.fixed_stride = fixed_stride;
   DeviceState* dev = nullptr;
   st = current_device(dev);
   if (st != FAR_OK) return st;
@@ -914,9 +919,11 @@ int check_call(const void* x, const void* r, const void* w, float eps, void* out
   return st;
 }
 
+// the allocation-free entry point's launches: fixed-stride rows, so no counter pair and no
+// event is created or recorded for them
 int enqueue_device_call(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
                         int64_t tokens, int64_t hidden, int dtype, bool residual, cudaStream_t stream) {
-  return run(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, stream);
+  return run(x, r, w, eps, out, res_out, tokens, hidden, dtype, residual, stream, nullptr, true);
 }
 
 int device_info(unsigned int** status, int* sms) {
