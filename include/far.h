@@ -358,7 +358,8 @@ int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_resid
  * rows where a claim takes one or two rows, the rows left after the first ring-full of
  * every CTA are at least as many again, the stream is not capturing a graph and a
  * counter is free; 1: the fixed stride always; 2: claimed rows whenever there are rows
- * left to claim (and a counter is free, and the stream is not capturing).  The results
+ * left to claim (and a counter is free, and the stream is not capturing).  The
+ * allocation-free entry point always keeps the fixed stride.  The results
  * are the same bits in every mode (each row is computed the same way by whichever CTA
  * takes it).  Returns FAR_ERR_SHAPE for another mode.
  */
