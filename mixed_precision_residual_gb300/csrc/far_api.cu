@@ -664,17 +664,17 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   // at least as many rows are left after every CTA's first ring-full as those take: on
   // shorter rows the fixed stride was as fast or faster; forced, wherever rows are left.
   const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od)));
-  const int64_t run = (45333 + row_traffic - 1) / row_traffic;
+  const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
   const int mode = g_row_schedule.load();
   const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
   int pair = -1;
   const int devno = (int)(&dev - g_dev);
   if (L.kind == kStaged && !c.fixed_stride && mode != 1 &&
-      (mode == 2 ? c.tokens > r0 : (run <= 2 && c.tokens >= 2 * r0))) {
+      (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 2 * r0))) {
     pair = sched_acquire(devno, stream);
     if (pair >= 0) {
       L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
-      L.p.sched_run = (int32_t)(run < (1 << 20) ? run : (1 << 20));
+      L.p.sched_run = (int32_t)(claim_rows < (1 << 20) ? claim_rows : (1 << 20));
     }
   }
   cudaError_t e;
