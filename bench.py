@@ -174,6 +174,16 @@ def traffic_from_profile(workload: str, op: str = "rmsnorm", plan: dict | None =
     return e.get("dram_bytes_per_launch")
 
 
+def row_schedule_text(far, claimed, tokens, hidden, act, wd, residual, op, sms):
+    """How a launch's CTAs shared rows (the library's flag after the launch, and its rule for
+    the rows a claim)."""
+    if not claimed:
+        return "fixed stride"
+    n = far.row_schedule_for_sms(tokens, hidden, act, wd, residual,
+                                 {"rmsnorm": "rmsnorm", "layernorm": "layernorm"}.get(op, "quant"), sms)
+    return f"rows claimed from a per-launch counter, {n} a claim"
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
 
@@ -660,8 +670,10 @@ def main():
                      "kernel": f"staged_kernel ({kernel_name})", "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": fb, "avg_launch_ms": round(fused_ms, 5),
                      "launch_plan": plan,
-                     "row_schedule": {k: ("rows claimed from a per-launch counter" if v else "fixed stride")
-                                      for k, v in (("fused", rows_fused), ("variant", rows_variant))}},
+                     "row_schedule": {k: row_schedule_text(far, claimed, T, H, x.dtype, wt.dtype, residual, args.op,
+                                                           torch.cuda.get_device_properties(dev).multi_processor_count)
+                                      for k, claimed, residual in (("fused", rows_fused, True),
+                                                                   ("variant", rows_variant, False))}},
         "clocks": clk,
         "e2e": e2e,
     }

@@ -364,6 +364,13 @@ int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_resid
  * takes it).  Returns FAR_ERR_SHAPE for another mode.
  */
 int far_set_row_schedule(int mode);
+/* rows_per_claim: the rows a claim would take for such a call on a device with `sms` SMs
+   under the current mode, or 0 where it keeps the fixed stride (host logic only: whether
+   a counter is free or the stream capturing is decided at launch); op as
+   far_host_workspace_bytes_op (0 RMSNorm, 1 LayerNorm, 2 a quantised output).
+   FAR_ERR_SHAPE for tokens 0, sms < 1 or another op. */
+int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int op, int sms,
+                             int* rows_per_claim);
 /* 1 if the calling thread's last kernel launch by this library claimed rows from a
    counter, else 0 (fixed-stride rows, the generic kernel, or no launch) */
 int far_last_launch_claimed_rows(void);

@@ -106,6 +106,8 @@ lib.far_set_row_schedule.argtypes = [_int]
 lib.far_set_row_schedule.restype = _int
 lib.far_last_launch_claimed_rows.argtypes = []
 lib.far_last_launch_claimed_rows.restype = _int
+lib.far_row_schedule_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
+lib.far_row_schedule_for_sms.restype = _int
 lib.far_describe_launch.argtypes = [_i64, _i64, _int, _int, _vp]
 lib.far_describe_launch.restype = _int
 lib.far_plan_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _vp]
@@ -256,6 +258,16 @@ def set_row_schedule(mode: int = 0) -> None:
     """How the staged kernel's CTAs share rows: 0 automatic, 1 fixed stride, 2 claimed rows
     whenever possible (the same bits in every mode)."""
     _check(lib.far_set_row_schedule(mode))
+
+
+def row_schedule_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool, op: str,
+                         sms: int) -> int:
+    """Rows a claim for such a call under the current mode, 0 for the fixed stride (host
+    logic only); op "rmsnorm", "layernorm" or "quant"."""
+    out = ctypes.c_int(0)
+    _check(lib.far_row_schedule_for_sms(tokens, hidden, dtypes(act, wd), int(residual),
+                                        {"rmsnorm": 0, "layernorm": 1, "quant": 2}[op], sms, ctypes.addressof(out)))
+    return out.value
 
 
 def last_launch_claimed_rows() -> bool:

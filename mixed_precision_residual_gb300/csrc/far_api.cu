@@ -652,29 +652,38 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   return FAR_OK;
 }
 
+// Rows a claim for a call's launch under schedule `mode`, or 0 for the fixed stride (host
+// logic only; whether a counter pair is free, or the stream capturing, is decided at
+// launch). Rows a claim: as few as keep the claims below ~150 M/s at the copy rate
+// (~6.8 TB/s), well under the ~250 M/s that one counter's atomics were measured to sustain
+// on GB300. Claimed rows by default where that is one or two rows (rows moving 23 KB or
+// more) and at least as many rows are left after every CTA's first ring-full as those
+// take: on shorter rows the fixed stride was as fast or faster; forced, wherever rows are
+// left.
+int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
+  if (L.kind != kStaged || c.fixed_stride || mode == 1) return 0;
+  const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od)));
+  const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
+  const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
+  if (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 2 * r0))
+    return claim_rows < (1 << 20) ? claim_rows : (1 << 20);
+  return 0;
+}
+
 int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   g_last_claimed = 0;
   if (c.tokens == 0) return FAR_OK;
   Launch L;
   int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
-  // Rows a claim: as few as keep the claims below ~150 M/s at the copy rate (~6.8 TB/s),
-  // well under the ~250 M/s that one counter's atomics were measured to sustain on GB300.
-  // Claimed rows by default where that is one or two rows (rows moving 23 KB or more) and
-  // at least as many rows are left after every CTA's first ring-full as those take: on
-  // shorter rows the fixed stride was as fast or faster; forced, wherever rows are left.
-  const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od)));
-  const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
-  const int mode = g_row_schedule.load();
-  const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
+  const int64_t claim_rows = claim_rows_for(c, L, g_row_schedule.load());
   int pair = -1;
   const int devno = (int)(&dev - g_dev);
-  if (L.kind == kStaged && !c.fixed_stride && mode != 1 &&
-      (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 2 * r0))) {
+  if (claim_rows > 0) {
     pair = sched_acquire(devno, stream);
     if (pair >= 0) {
       L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
-      L.p.sched_run = (int32_t)(claim_rows < (1 << 20) ? claim_rows : (1 << 20));
+      L.p.sched_run = (int32_t)claim_rows;
     }
   }
   cudaError_t e;
@@ -1193,6 +1202,33 @@ int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual
   out8[5] = (int)L.grid.x;
   out8[6] = (int)L.block.x;
   out8[7] = (int)L.smem;
+  return FAR_OK;
+}
+
+int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int op, int sms,
+                             int* rows_per_claim) {
+  if (sms < 1 || !rows_per_claim || op < 0 || op > 2) return FAR_ERR_SHAPE;
+  Call c;
+  const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
+  char* mb = const_cast<char*>(base);
+  const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;
+  const void* r = has_residual ? base + span : nullptr;
+  void* ro = has_residual ? mb + 4 * span : nullptr;
+  int st;
+  if (op == 0)
+    st = validate(base, r, base + 2 * span, 1e-6f, mb + 3 * span, ro, tokens, hidden, dtype, has_residual != 0, c);
+  else if (op == 1)
+    st = validate_ln(base, r, base + 2 * span, base + 5 * span, 1e-6f, mb + 3 * span, ro, tokens, hidden, dtype,
+                     has_residual != 0, c);
+  else
+    st = validate_quant(base, r, base + 2 * span, 1e-6f, mb + 3 * span, reinterpret_cast<float*>(mb + 5 * span), ro,
+                        tokens, hidden, dtype, FAR_Q_INT8, has_residual != 0, c);
+  if (st != FAR_OK) return st;
+  if (tokens == 0) return FAR_ERR_SHAPE;
+  Launch L;
+  st = plan(c, sms, nullptr, nullptr, L);
+  if (st != FAR_OK) return st;
+  *rows_per_claim = (int)claim_rows_for(c, L, g_row_schedule.load());
   return FAR_OK;
 }
 

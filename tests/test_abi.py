@@ -122,6 +122,37 @@ def test_row_schedule_hook(far):
     assert far.last_launch_claimed_rows() is False
 
 
+def test_row_schedule_rule(far):
+    """The automatic row schedule (host logic): one row a claim where a row moves 45 KB or
+    more, two down to 23 KB, the fixed stride on shorter rows and on launches with fewer
+    than two ring-fulls of rows a CTA left; forced modes override it."""
+    f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
+
+    def rows(tokens, hidden, act, wd, residual, op, sms=152):
+        return far.row_schedule_for_sms(tokens, hidden, act, wd, residual, op, sms)
+
+    for op in ("rmsnorm", "layernorm", "quant"):
+        assert rows(65536, 8192, f16, f16, True, op) == 1      # 64 KB (56 KB quantised) a row
+        assert rows(65536, 8192, f16, f16, False, op) == 2     # 32 KB (24 KB)
+    assert rows(16384, 5120, bf16, bf16, True, "rmsnorm") == 2   # 40 KB
+    assert rows(16384, 5120, bf16, bf16, False, "rmsnorm") == 0  # 20 KB: fixed stride
+    assert rows(4096, 4096, bf16, f32, True, "rmsnorm") == 2     # 40 KB
+    assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 0   # 8 KB
+    for tokens, hidden, dt in ((512, 8192, f16), (512, 5120, bf16), (8, 2048, bf16)):
+        assert rows(tokens, hidden, dt, dt, True, "rmsnorm") == 0  # under two ring-fulls a CTA
+    try:
+        far.set_row_schedule(1)
+        assert rows(65536, 8192, f16, f16, True, "rmsnorm") == 0
+        far.set_row_schedule(2)
+        assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 6  # ceil(45333 / 8192)
+        assert rows(16384, 5120, bf16, bf16, False, "rmsnorm") == 3
+    finally:
+        far.set_row_schedule(0)
+    out = ctypes.c_int(0)
+    for args in ((0, 8192, 1, 1, 0, 152), (64, 8192, 1, 1, 3, 152), (64, 8192, 1, 1, 0, 0)):
+        assert far.lib.far_row_schedule_for_sms(*args, ctypes.addressof(out)) == 4  # FAR_ERR_SHAPE
+
+
 def test_host_workspace_size(far):
     n1 = far.lib.far_host_workspace_bytes(1, 4096, code("bf16", "f32"), 1)
     n8 = far.lib.far_host_workspace_bytes(8, 4096, code("bf16", "f32"), 1)
