@@ -16,10 +16,22 @@ region, and the CPU oracle timed on the host cores as a baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl far|reference]
                   [--op rmsnorm|layernorm|rmsnorm_int8|rmsnorm_fp8]
+                  [--row-schedule claimed|fixed]
 Under torchrun each rank runs its own replica (weak scaling, no collective on
 the data path); rank 0 prints one JSON line.  --op measures one of the other
 operations of the library the same way (its fused form, then its no-residual
 variant), the end-to-end leg through that op's host-buffer entry points.
+
+For the RMSNorm op the line also carries `configs`: every workload (bf16
+8x2048 up to fp16 65536x8192), the fused op and the variant each, timed per
+launch with CUDA events both after an L2 read sweep and back to back, with the
+mean, median, min and max launch time, GB/s, tokens/s and the fraction of the
+measured copy rate.
+
+--row-schedule: `claimed` (the default here) opts in to rows claimed from a
+per-launch counter by the library's automatic rule (far_set_row_schedule(0));
+`fixed` times the library's default, the fixed stride (mode 1), which keeps no
+state between calls.  The line says which was timed.
 """
 from __future__ import annotations
 
@@ -76,7 +88,16 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", choices=sorted(OP_METRIC), default="rmsnorm")
     ap.add_argument("--gemm-shape", default="8192x8192x8192", help="M x N x K of the GEMM op")
+    ap.add_argument("--row-schedule", choices=["claimed", "fixed"], default="claimed",
+                    help="claimed: the library's opt-in automatic claimed-row rule; fixed: its default")
+    ap.add_argument("--config-launches", type=int, default=30,
+                    help="launches timed per workload, op and L2 condition in `configs` (0: none)")
     return ap.parse_args()
+
+
+ROW_SCHEDULE_MODE = {"claimed": 0, "fixed": 1}
+ROW_SCHEDULE_TEXT = {"claimed": "claimed rows by the automatic rule (opt-in: far_set_row_schedule(0))",
+                     "fixed": "fixed stride (the library default, far_set_row_schedule(1))"}
 
 
 def dist_env():
@@ -233,27 +254,148 @@ class ClockSampler:
                 "power_w_median": statistics.median(power) if power else None}
 
 
-def cpu_baseline(d, seconds: float, op: str = "rmsnorm"):
-    """The oracle, as it stands, on the first rows of the batch (fused + variant), host threads."""
-    import oracle
+# Arm core names by (implementer, part), for CPUs whose /proc/cpuinfo gives no model name
+ARM_PARTS = {(0x41, 0xd4f): "Arm Neoverse-V2", (0x41, 0xd40): "Arm Neoverse-V1", (0x41, 0xd0c): "Arm Neoverse-N1",
+             (0x41, 0xd49): "Arm Neoverse-N2", (0x41, 0xd8f): "Arm Neoverse-V3"}
 
-    threads = oracle.default_threads()
-    H = d["hidden"]
-    act, wd = d["act"], d["wd"]
-    od = "f32" if "f32" in (act, wd) else act
+
+def cpu_model() -> str:
+    """The host CPU's model, from /proc/cpuinfo (x86: its model name; Arm: the core named by
+    implementer and part), with the logical CPU count."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            text = f.read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip().lower(), v.strip())
+    n = os.cpu_count() or 0
+    if "model name" in fields:
+        return f"{fields['model name']} ({n} logical CPUs)"
+    try:
+        key = (int(fields.get("cpu implementer", "0"), 0), int(fields.get("cpu part", "0"), 0))
+    except ValueError:
+        key = (0, 0)
+    if key in ARM_PARTS:
+        return f"{ARM_PARTS[key]} ({n} logical CPUs)"
+    if key != (0, 0):
+        return f"Arm implementer {key[0]:#x} part {key[1]:#x} ({n} logical CPUs)"
+    return f"unknown ({n} logical CPUs)"
+
+
+def oracle_sample(d, seconds: float, op: str, threads: int):
+    """The oracle, as it stands, on the first rows of the batch (fused + variant) for about
+    `seconds`: rows done and elapsed seconds."""
     rows_done, t0 = 0, time.perf_counter()
     chunk = max(threads * 4, 64)
     while time.perf_counter() - t0 < seconds and rows_done < d["tokens"]:
         sl = slice(rows_done, min(d["tokens"], rows_done + chunk))
         oracle_step(op, d, d["x"][sl], d["r"][sl], threads)
         rows_done = sl.stop
-    el = time.perf_counter() - t0
+    return rows_done, time.perf_counter() - t0
+
+
+def cpu_baseline(d, seconds: float, op: str = "rmsnorm"):
+    """The oracle, as it stands, timed on the host cores on the first rows of the batch:
+    on every core (row blocks over threads), then on one thread; GB/s of the same
+    algorithmic bytes, tokens/s, and the CPU model."""
+    import oracle
+
+    threads = oracle.default_threads()
+    H = d["hidden"]
+    act, wd = d["act"], d["wd"]
+    od = "f32" if "f32" in (act, wd) else act
     tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    fb, nb = step_bytes(rows_done, H, tdt[act], tdt[wd], tdt[od], op)
-    return {"value": round((fb + nb) / el / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "seconds": round(el, 2), "tokens_per_s": round(rows_done / el, 1),
-            "sample": f"first {rows_done} of {d['tokens']} rows of the {d['workload']} batch, {OP_STEP[op]}, "
-                      f"oracle on {threads} host threads"}
+    model = cpu_model()
+    legs = {}
+    for name, n, secs in (("threads_all", threads, seconds), ("threads_1", 1, seconds / 2)):
+        rows_done, el = oracle_sample(d, secs, op, n)
+        fb, nb = step_bytes(rows_done, H, tdt[act], tdt[wd], tdt[od], op)
+        legs[name] = {"value": round((fb + nb) / el / 1e9, 4), "unit": "GB/s", "threads": n,
+                      "seconds": round(el, 2), "tokens_per_s": round(rows_done / el, 1),
+                      "sample": f"first {rows_done} of {d['tokens']} rows of the {d['workload']} batch"}
+    return {"value": legs["threads_all"]["value"], "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "cpu_model": model, "seconds": legs["threads_all"]["seconds"],
+            "tokens_per_s": legs["threads_all"]["tokens_per_s"],
+            "sample": f"{legs['threads_all']['sample']}, {OP_STEP[op]}, oracle on {threads} host threads "
+                      f"(row blocks over threads); threads_1: the same on one thread",
+            "threads_all": legs["threads_all"], "threads_1": legs["threads_1"]}
+
+
+def launch_stats(ms):
+    """Mean, median, min and max of per-launch times (ms)."""
+    return {"mean_ms": round(statistics.fmean(ms), 5), "median_ms": round(statistics.median(ms), 5),
+            "min_ms": round(min(ms), 5), "max_ms": round(max(ms), 5), "launches": len(ms)}
+
+
+def time_launches(fn, stream, n, flush=None):
+    """CUDA-event times (ms) of n launches of fn on `stream` (torch's current stream): back to
+    back, or each after a read sweep of `flush` (outside the events), which leaves the L2
+    holding no line of the launch's tensors and no dirty line to write back."""
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for k in range(n):
+        if flush is not None:
+            flush.sum()
+        ev0[k].record(stream)
+        if fn():
+            raise RuntimeError("launch failed")
+        ev1[k].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+
+
+def measure_configs(far, dev, stream, launches, flush, peak, sms, resident=None):
+    """Every workload's fused add+RMSNorm and no-residual RMSNorm, timed per launch both after
+    an L2 read sweep and back to back; GB/s and tokens/s from the mean launch time, the
+    fraction of the measured copy rate, and the spread.  `resident` maps a workload name to
+    device tensors already allocated (the bench step's own batch)."""
+    import far_gen
+
+    L = far.lib
+    sh = stream.cuda_stream
+    entries = []
+    for name in ("c1", "c2", "c3", "c4", "c5"):
+        w = far_gen.WORKLOADS[name]
+        if resident and name in resident:
+            x, r, wt, eps = resident[name]
+        else:
+            d = far_gen.make_inputs(w)
+            x, r, wt, eps = d["x"].to(dev), d["r"].to(dev), d["w"].to(dev), d["eps"]
+        T, H = x.shape
+        od = far.output_dtype(x.dtype, wt.dtype)
+        out = torch.empty(x.shape, dtype=od, device=dev)
+        res = torch.empty_like(x)
+        out2 = torch.empty(x.shape, dtype=od, device=dev)
+        code = far.dtypes(x.dtype, wt.dtype)
+        xp, rp, wp, op, rop, o2p = (t.data_ptr() for t in (x, r, wt, out, res, out2))
+        fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od)
+        ops = (("fused", lambda: L.fused_add_rmsnorm(xp, rp, wp, eps, op, rop, T, H, code, sh), fb, True),
+               ("variant", lambda: L.rmsnorm(xp, wp, eps, o2p, T, H, code, sh), nb, False))
+        e = {"workload": name, "note": w.note, "tokens": T, "hidden": H, "act_dtype": w.act, "weight_dtype": w.wd}
+        for kind, fn, nbytes, residual in ops:
+            for _ in range(3):
+                if fn():
+                    raise RuntimeError(f"{name} {kind} launch failed")
+            claimed = far.last_launch_claimed_rows()
+            torch.cuda.synchronize()
+            k = {"algorithmic_bytes_per_launch": nbytes,
+                 "launch_plan": far.describe_launch(T, H, x.dtype, wt.dtype, residual),
+                 "row_schedule": row_schedule_text(far, claimed, T, H, x.dtype, wt.dtype, residual, "rmsnorm", sms)}
+            for cond, fl in (("flushed", flush), ("back_to_back", None)):
+                st = launch_stats(time_launches(fn, stream, launches, fl))
+                gbs = nbytes / (st["mean_ms"] * 1e-3) / 1e9
+                k[cond] = {"gbs": round(gbs, 1), "tokens_per_s": round(T / (st["mean_ms"] * 1e-3), 1),
+                           "frac": round(gbs / peak, 4), **st}
+            e[kind] = k
+        if far.device_status() != 0:
+            raise RuntimeError(f"device status after the {name} launches")
+        entries.append(e)
+        del out, res, out2
+    return entries
 
 
 def run_reference(args):
@@ -523,6 +665,7 @@ def main():
         if s1 or s2:
             raise RuntimeError(f"launch failed: {s1} {s2}")
 
+    far.set_row_schedule(ROW_SCHEDULE_MODE[args.row_schedule])
     for _ in range(max(3, args.warmup)):
         step()
     # the row schedule of each kernel (the flag of this thread's last launch), outside the
@@ -556,16 +699,29 @@ def main():
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    clk = clocks.stop()
     status = far.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     total_ms = max_over_ranks(ev_start.elapsed_time(ev_end), dist, dev)
-    fused_ms = sum(a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)) / args.steps
+    fused_launch_ms = [a.elapsed_time(b) for a, b in zip(ev_f0, ev_f1)]
+    fused_ms = sum(fused_launch_ms) / args.steps
     ms_per_step = total_ms / args.steps
     fb, nb = step_bytes(T, H, x.dtype, wt.dtype, od, args.op)
     value = job_rate(fb + nb, world, ms_per_step) / 1e9
     tokens_per_s = job_rate(T, world, ms_per_step)
+    peak, peak_kind = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    # every workload, fused and variant, flushed and back to back (the RMSNorm op only);
+    # the clock sampler keeps running through these launches, so its window is long enough
+    # for nvidia-smi's 100 ms samples
+    configs = None
+    if args.op == "rmsnorm" and args.config_launches > 0 and not args.tokens:
+        flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)  # 512 MB read sweep
+        configs = measure_configs(far, dev, stream, args.config_launches, flush, peak, sms,
+                                  resident={args.workload: (x, r, wt, eps)})
+        del flush
+    clk = clocks.stop()
+    clk["window"] = ("the timed steps" + (" and the per-workload launches after them" if configs else ""))
 
     # end to end through the host-buffer entry points: copies inside the timed region
     e2e = None
@@ -636,7 +792,6 @@ def main():
                "path": f"{path} (pinned host buffers, {chunk}-row chunks, two internal streams)"}
         assert far.device_status() == 0
 
-    peak, peak_kind = measured_peaks()
     achieved = fb / (fused_ms * 1e-3) / 1e9
     if args.op == "rmsnorm":
         plan = far.describe_launch(T, H, x.dtype, wt.dtype, True)
@@ -661,14 +816,19 @@ def main():
                    "eps": eps, "step": OP_STEP[args.op],
                    "l2": "no flush: every tensor (1 GiB) is larger than the 129 MB L2",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)",
-                   "op": args.op},
+                   "op": args.op, "row_schedule": ROW_SCHEDULE_TEXT[args.row_schedule]},
         "tokens_per_s": round(tokens_per_s, 1),
+        "value_covers": (f"the whole step: both kernels ({OP_STEP[args.op]}), their algorithmic bytes over the "
+                         f"step time; the fused kernel alone is `roofline`"),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "gpu_launches": 2 * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": f"staged_kernel ({kernel_name})", "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": fb, "avg_launch_ms": round(fused_ms, 5),
+                     "median_launch_ms": round(statistics.median(fused_launch_ms), 5),
+                     "min_launch_ms": round(min(fused_launch_ms), 5),
+                     "max_launch_ms": round(max(fused_launch_ms), 5),
                      "launch_plan": plan,
                      "row_schedule": {k: row_schedule_text(far, claimed, T, H, x.dtype, wt.dtype, residual, args.op,
                                                            torch.cuda.get_device_properties(dev).multi_processor_count)
@@ -677,6 +837,13 @@ def main():
         "clocks": clk,
         "e2e": e2e,
     }
+    if configs is not None:
+        line["configs"] = configs
+        line["configs_note"] = (f"per workload: the fused op and the no-residual variant, {args.config_launches} "
+                                f"launches each after a 512 MB L2 read sweep (flushed) and {args.config_launches} "
+                                f"back to back; GB/s and tokens/s from the mean launch time (CUDA events on the "
+                                f"launching stream); frac against the measured copy rate {peak} GB/s; row schedule "
+                                f"as the line's config")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds, args.op)
     if rank == 0:

@@ -26,8 +26,17 @@
  * GPU cannot reach is a CUDA error, not a slow path.
  *
  * Memory: all tensors are caller-owned, contiguous and row-major (row stride =
- * hidden elements).  The device entry points allocate nothing and keep no
- * per-call state; they only enqueue on the stream they are given.
+ * hidden elements).  By default the device entry points allocate nothing and
+ * keep no state from one call to the next: they only enqueue on the stream
+ * they are given.  What the library holds is fixed at load time or created
+ * once per device: a 4-byte device error word (far_device_status); the
+ * host-buffer entry points' two internal streams and four events (created on
+ * their first call on a device); the allocation-free entry point's 16 MiB
+ * staging array (FAR_NOALLOC_SCRATCH_BYTES).  One opt-in mode keeps state
+ * across calls: claimed rows (far_set_row_schedule(0) or (2)) use a 1 KB
+ * device array of 64 row counters, create 64 CUDA events on a device's first
+ * claimed launch, and remember which stream last used each counter; see
+ * far_set_row_schedule.  The default, far_set_row_schedule(1), keeps none.
  *
  * Aliasing: an output may be the very same buffer as an input of the same
  * element size (in-place use: out == x, residual_out == residual, ...).  Any
@@ -348,20 +357,29 @@ int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_resid
  * far_set_row_schedule: process-wide choice of how the staged kernel's CTAs share
  * rows.  Each CTA first takes rows at a fixed stride (its own index, plus the grid size
  * each time), as many as its shared-memory ring holds; after that it either keeps the
- * stride or claims the next free rows, a few at a time, from a counter of the launch
- * (library-owned device memory, 64 counters a device; a launch takes the counter of
- * earlier launches on its own stream, which run before it, or one whose last launch an
- * event shows finished, so launches that can run side by side never share one).  Claimed rows keep the CTAs that the
- * memory system serves faster busy until the last rows, instead of idling them while
- * slower ones finish.  A claim takes as many rows as keep the claims below ~150 M/s at
- * the copy rate (one row where a row moves 45 KB or more).  mode 0 (default): claimed
- * rows where a claim takes one or two rows, the rows left after the first ring-full of
- * every CTA are at least as many again, the stream is not capturing a graph and a
- * counter is free; 1: the fixed stride always; 2: claimed rows whenever there are rows
- * left to claim (and a counter is free, and the stream is not capturing).  The
- * allocation-free entry point always keeps the fixed stride.  The results
- * are the same bits in every mode (each row is computed the same way by whichever CTA
- * takes it).  Returns FAR_ERR_SHAPE for another mode.
+ * stride or claims the next free rows, a few at a time, from a counter of the launch.
+ * Claimed rows keep the CTAs that the memory system serves faster busy until the last
+ * rows, instead of idling them while slower ones finish (measured 2.5-4.4 % less time on
+ * launches whose rows move 23 KB or more).  A claim takes as many rows as keep the claims
+ * below ~150 M/s at the copy rate (one row where a row moves 45 KB or more).
+ *   mode 1 (the default): the fixed stride always.  No state is kept between calls.
+ *   mode 0: claimed rows where a claim takes one or two rows, the rows left after the
+ *           first ring-full of every CTA are at least as many again, the stream is not
+ *           capturing a graph and a counter is free; else the fixed stride.
+ *   mode 2: claimed rows whenever there are rows left to claim (and a counter is free,
+ *           and the stream is not capturing).
+ * State of modes 0 and 2: the counters are a library-owned device array of 64 pairs a
+ * device, each zero between launches (a launch's last CTA zeroes its pair).  A launch
+ * takes the pair last used on its own stream (earlier launches there run before it), or
+ * a pair with no launch pending whose CUDA event, recorded after its last launch, has
+ * completed; so launches that can run side by side never share one.  The 64 events are
+ * created on a device's first claimed launch and kept until exit.  A launch finding no
+ * free pair, or a capturing stream, takes the fixed stride.  A stream must not begin a
+ * capture while another host thread is launching on it in these modes (a pair whose
+ * event record fell into a capture is retired for good).  The allocation-free entry
+ * point always keeps the fixed stride.  The results are the same bits in every mode
+ * (each row is computed the same way by whichever CTA takes it).  Returns FAR_ERR_SHAPE
+ * for another mode.
  */
 int far_set_row_schedule(int mode);
 /* rows_per_claim: the rows a claim would take for such a call on a device with `sms` SMs
@@ -371,9 +389,22 @@ int far_set_row_schedule(int mode);
    FAR_ERR_SHAPE for tokens 0, sms < 1 or another op. */
 int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int op, int sms,
                              int* rows_per_claim);
+/* the current mode of far_set_row_schedule */
+int far_get_row_schedule(void);
 /* 1 if the calling thread's last kernel launch by this library claimed rows from a
    counter, else 0 (fixed-stride rows, the generic kernel, or no launch) */
 int far_last_launch_claimed_rows(void);
+/*
+ * The counter pool's bookkeeping run alone, as host logic (no CUDA call), on a fresh pool
+ * of 64 pairs: n operations of three int64 each, {op, a, b}:
+ *   op 1  a launch on the stream with id a asks for a pair; b is a bit mask of the pairs
+ *         whose event (recorded after their last launch) has completed, bit s for pair s;
+ *         results[i] = the pair handed out, or -1 (the launch keeps the fixed stride);
+ *   op 2  pair a is given back after its launch; b bit 0: the kernel was enqueued, bit 1:
+ *         an event was recorded after it; results[i] = 0.
+ * FAR_ERR_SHAPE for an unknown op, or for giving back a pair that is not handed out.
+ */
+int far_sched_pool_model(const int64_t* ops, int n, int* results);
 
 #ifdef __cplusplus
 }

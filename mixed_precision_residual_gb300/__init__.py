@@ -106,6 +106,10 @@ lib.far_set_row_schedule.argtypes = [_int]
 lib.far_set_row_schedule.restype = _int
 lib.far_last_launch_claimed_rows.argtypes = []
 lib.far_last_launch_claimed_rows.restype = _int
+lib.far_get_row_schedule.argtypes = []
+lib.far_get_row_schedule.restype = _int
+lib.far_sched_pool_model.argtypes = [_vp, _int, _vp]
+lib.far_sched_pool_model.restype = _int
 lib.far_row_schedule_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
 lib.far_row_schedule_for_sms.restype = _int
 lib.far_describe_launch.argtypes = [_i64, _i64, _int, _int, _vp]
@@ -254,10 +258,27 @@ def set_launch_override(kind: int = -1, nch: int = 0, groups: int = 0, stages: i
     _check(lib.far_set_launch_override(kind, nch, groups, stages))
 
 
-def set_row_schedule(mode: int = 0) -> None:
-    """How the staged kernel's CTAs share rows: 0 automatic, 1 fixed stride, 2 claimed rows
-    whenever possible (the same bits in every mode)."""
+def set_row_schedule(mode: int = 1) -> None:
+    """How the staged kernel's CTAs share rows: 1 the fixed stride (the default, no state kept
+    between calls), 0 claimed rows by the automatic rule, 2 claimed rows whenever possible
+    (the same bits in every mode)."""
     _check(lib.far_set_row_schedule(mode))
+
+
+def get_row_schedule() -> int:
+    """The current row-schedule mode (see set_row_schedule)."""
+    return int(lib.far_get_row_schedule())
+
+
+def sched_pool_model(ops) -> list:
+    """Run the counter pool's bookkeeping alone (host logic, no CUDA call) on a fresh pool:
+    ops is a list of (1, stream_id, done_mask) acquisitions and (2, pair, flags) releases;
+    returns each operation's result (the pair handed out or -1; 0 for a release)."""
+    n = len(ops)
+    flat = (ctypes.c_int64 * (3 * max(n, 1)))(*[int(v) for op in ops for v in op])
+    res = (ctypes.c_int * max(n, 1))()
+    _check(lib.far_sched_pool_model(ctypes.addressof(flat), n, ctypes.addressof(res)))
+    return list(res)[:n]
 
 
 def row_schedule_for_sms(tokens: int, hidden: int, act: torch.dtype, wd: torch.dtype, residual: bool, op: str,

@@ -45,42 +45,88 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 
-// The counter pairs of a device. A launch on stream S may take a pair whose launches still
-// pending are all on S: S runs them in order, so each has left the pair zero before the next
-// starts. Otherwise it takes a pair with no launch pending whose event (recorded after its
-// last launch) has completed. So launches that can run side by side (different streams)
-// never share a pair, while a stream with many launches queued keeps claiming rows. Streams
-// are told apart by their context-unique id, not their handle (a destroyed stream's handle
-// can come back; every thread's per-thread default stream has one handle). No pair during
-// stream capture (a captured event cannot be polled) or when all are busy: the launch takes
-// fixed-stride rows.
+// The counter pairs of a device (claimed rows, an opt-in row schedule). A launch on stream S
+// may take a pair whose launches still pending are all on S: S runs them in order, so each
+// has left the pair zero before the next starts. Otherwise it takes a pair with no launch
+// pending whose event (recorded after its last launch) has completed. So launches that can
+// run side by side (different streams) never share a pair, while a stream with many
+// launches queued keeps claiming rows. Streams are told apart by their context-unique id,
+// not their handle (a destroyed stream's handle can come back; every thread's per-thread
+// default stream has one handle). No pair during stream capture (a captured event cannot
+// be polled) or when all are busy: the launch takes fixed-stride rows.
+//
+// PoolBook is that bookkeeping alone, apart from CUDA (the event's state is asked through
+// a callback), so that the host-only model far_sched_pool_model can drive it.
+struct PoolBook {
+  unsigned long long stream_id[kSchedSlots] = {};  // the stream of its pending launches
+  int pending[kSchedSlots] = {};   // handed out, not yet released after the launch
+  bool used[kSchedSlots] = {};     // launched at least once: its event shows the last launch
+  bool retired[kSchedSlots] = {};  // no trustworthy event: never handed out again
+  int next = 0;
+
+  // a pair for a launch on stream `sid`, or -1; event_done(s) is 1 when the event recorded
+  // after pair s's last launch has completed, else 0
+  template <typename Done>
+  int acquire(unsigned long long sid, Done event_done) {
+    int got = -1;
+    // a pair last given to this stream (whatever is pending on it runs before this launch)
+    for (int s = 0; s < kSchedSlots && got < 0; ++s)
+      if (!retired[s] && (used[s] || pending[s] > 0) && stream_id[s] == sid) got = s;
+    // else a pair nothing is pending on, whose last launch has finished
+    for (int i = 0; i < kSchedSlots && got < 0; ++i) {
+      const int s = (next + i) % kSchedSlots;
+      if (pending[s] > 0 || retired[s]) continue;
+      if (used[s] && event_done(s) != 1) continue;
+      got = s;
+      next = (s + 1) % kSchedSlots;
+    }
+    if (got >= 0) {
+      stream_id[got] = sid;
+      ++pending[got];
+    }
+    return got;
+  }
+
+  // after the launch that used pair s: launched (the kernel was enqueued) and recorded (an
+  // event was recorded after it, outside any capture); a launched pair without such an
+  // event is retired
+  void release(int s, bool launched, bool recorded) {
+    if (launched) {
+      if (recorded) used[s] = true;
+      else retired[s] = true;
+    }
+    --pending[s];
+  }
+};
+
 struct SchedPool {
   std::mutex mu;
   bool ready = false, broken = false;
   unsigned long long* pairs = nullptr;  // device address of g_sched on this device
   cudaEvent_t ev[kSchedSlots] = {};
-  unsigned long long stream_id[kSchedSlots] = {};  // the stream of its pending launches
-  int pending[kSchedSlots] = {};   // handed out, event not yet recorded after the launch
-  bool used[kSchedSlots] = {};     // launched at least once: its event shows the last launch
-  bool retired[kSchedSlots] = {};  // an event could not be recorded: never handed out again
-  int next = 0;
+  PoolBook book;
 };
 SchedPool g_sched_pool[kMaxDevices];
 
-// row schedule: 0 automatic, 1 fixed stride always, 2 claimed rows whenever a pair is free
-std::atomic<int> g_row_schedule{0};
+// row schedule: 1 fixed stride always (the default: no state kept between calls),
+// 0 claimed rows by the automatic rule, 2 claimed rows whenever a pair is free
+std::atomic<int> g_row_schedule{1};
 thread_local int g_last_claimed = 0;  // this thread's last staged launch claimed rows
+
+bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;  // unknown: treat as capturing (no pair)
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
 
 // a counter pair for a launch on `stream`, or -1
 int sched_acquire(int dev, cudaStream_t stream) {
   // a capturing stream gets no pair, and no other call: one (the stream's id) was seen to
   // invalidate the capture
-  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
-    cudaGetLastError();
-    return -1;
-  }
-  if (cs != cudaStreamCaptureStatusNone) return -1;
+  if (stream_capturing(stream)) return -1;
   SchedPool& sp = g_sched_pool[dev];
   std::lock_guard<std::mutex> lk(sp.mu);
   if (sp.broken) return -1;
@@ -88,7 +134,6 @@ int sched_acquire(int dev, cudaStream_t stream) {
   // relax this thread's mode for the pool's own calls
   cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
   cudaThreadExchangeStreamCaptureMode(&mode);
-  int got = -1;
   unsigned long long sid = 0;
   if (cudaStreamGetId(stream, &sid) != cudaSuccess) {
     cudaGetLastError();
@@ -108,47 +153,34 @@ int sched_acquire(int dev, cudaStream_t stream) {
       sp.broken = true;
     }
   }
-  // a pair last given to this stream (whatever is pending on it runs before this launch)
-  for (int s = 0; sp.ready && s < kSchedSlots && got < 0; ++s)
-    if (!sp.retired[s] && (sp.used[s] || sp.pending[s] > 0) && sp.stream_id[s] == sid) got = s;
-  // else a pair nothing is pending on, whose last launch has finished
-  for (int i = 0; sp.ready && i < kSchedSlots && got < 0; ++i) {
-    const int s = (sp.next + i) % kSchedSlots;
-    if (sp.pending[s] > 0 || sp.retired[s]) continue;
-    if (sp.used[s]) {
+  int got = -1;
+  if (sp.ready) {
+    got = sp.book.acquire(sid, [&](int s) {
       const cudaError_t e = cudaEventQuery(sp.ev[s]);
-      if (e != cudaSuccess) {
-        if (e != cudaErrorNotReady) cudaGetLastError();
-        continue;
-      }
-    }
-    got = s;
-    sp.next = (s + 1) % kSchedSlots;
-  }
-  if (got >= 0) {
-    sp.stream_id[got] = sid;
-    ++sp.pending[got];
+      if (e == cudaSuccess) return 1;
+      if (e != cudaErrorNotReady) cudaGetLastError();
+      return 0;
+    });
   }
   cudaThreadExchangeStreamCaptureMode(&mode);
   return got;
 }
 
 // after the launch that used pair `s` (launched: the kernel was enqueued). The event is
-// recorded after the launch, so once no launch is pending it follows all of them.
+// recorded after the launch, so once no launch is pending it follows all of them. A stream
+// that began capturing after the launch would take the record into its graph, where the
+// pool could never see it: such a pair is retired instead.
 void sched_release(int dev, int s, cudaStream_t stream, bool launched) {
   SchedPool& sp = g_sched_pool[dev];
   std::lock_guard<std::mutex> lk(sp.mu);
   cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
   cudaThreadExchangeStreamCaptureMode(&mode);
-  if (launched) {
-    if (cudaEventRecord(sp.ev[s], stream) == cudaSuccess) {
-      sp.used[s] = true;
-    } else {
-      cudaGetLastError();
-      sp.retired[s] = true;
-    }
+  bool recorded = false;
+  if (launched && !stream_capturing(stream)) {
+    recorded = cudaEventRecord(sp.ev[s], stream) == cudaSuccess;
+    if (!recorded) cudaGetLastError();
   }
-  --sp.pending[s];
+  sp.book.release(s, launched, recorded);
   cudaThreadExchangeStreamCaptureMode(&mode);
 }
 
@@ -261,6 +293,15 @@ struct Call {
                               // allocation-free entry point creates and records none)
 };
 
+// Set while a host-only plan query validates its stand-in addresses: the plan depends on
+// shapes and alignment alone, and stand-ins spread over the address space for the largest
+// accepted shapes could wrap past 2^64 and read as overlapping, so no overlap is checked.
+thread_local bool t_plan_query = false;
+struct PlanQuery {
+  PlanQuery() { t_plan_query = true; }
+  ~PlanQuery() { t_plan_query = false; }
+};
+
 int validate(const void* x, const void* r, const void* w, float eps, void* out, void* res_out,
              int64_t tokens, int64_t hidden, int dtype, bool residual, Call& c, const Strides* strides = nullptr) {
   int st = decode(dtype, c.act, c.wd, c.od);
@@ -278,6 +319,8 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
            c.ln, c.beta};
   if (tokens == 0) return FAR_OK;
   if (!x || !w || !out || (residual && (!r || !res_out))) return FAR_ERR_NULL;
+  if (c.ln && !c.beta) return FAR_ERR_NULL;
+  if (t_plan_query) return FAR_OK;
   const int64_t sa = dsize(c.act), so = c.quant ? 1 : dsize(c.od);  // a quantised output is one byte
   const Region X = region(x, tokens, hidden * sa, sd.x * sa);
   const Region O = region(out, tokens, hidden * so, sd.out * so);
@@ -290,7 +333,6 @@ int validate(const void* x, const void* r, const void* w, float eps, void* out, 
     if (bad_overlap(RO, X) || bad_overlap(RO, R) || regions_overlap(RO, W)) return FAR_ERR_ALIAS;
   }
   if (c.ln) {  // LayerNorm's shift: read-only, so no output may touch it
-    if (!c.beta) return FAR_ERR_NULL;
     const Region B = region(c.beta, 1, hidden * dsize(c.wd), hidden * dsize(c.wd));
     if (regions_overlap(O, B)) return FAR_ERR_ALIAS;
     if (residual && regions_overlap(region(res_out, tokens, hidden * sa, sd.res * sa), B)) return FAR_ERR_ALIAS;
@@ -323,6 +365,10 @@ int validate_quant(const void* x, const void* r, const void* w, float eps, void*
   int st = validate(x, r, w, eps, q, res_out, tokens, hidden, dtype, residual, c, &sd);
   if (st != FAR_OK || tokens == 0) return st;
   if (!scale) return FAR_ERR_NULL;
+  if (t_plan_query) {
+    c.out = nullptr;
+    return FAR_OK;
+  }
   const int64_t sa = dsize(c.act);
   const Region Q = region(q, tokens, hidden, hidden);
   const Region S = region(scale, 1, tokens * 4, tokens * 4);
@@ -662,7 +708,11 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
 // left.
 int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
   if (L.kind != kStaged || c.fixed_stride || mode == 1) return 0;
-  const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od)));
+  // bytes a row moves: x (and the residual and residual_out), then out, or the quantised
+  // codes plus the row's binary32 scale (LayerNorm's beta, like the weight, is read once a
+  // launch, not a row)
+  const int64_t row_traffic = c.hidden * (dsize(c.act) * (c.residual ? 3 : 1) + (c.quant ? 1 : dsize(c.od))) +
+                              (c.quant ? 4 : 0);
   const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
   const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
   if (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 2 * r0))
@@ -681,6 +731,11 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   const int devno = (int)(&dev - g_dev);
   if (claim_rows > 0) {
     pair = sched_acquire(devno, stream);
+    // a capture begun on another thread since the pair was taken: give it back unused
+    if (pair >= 0 && stream_capturing(stream)) {
+      sched_release(devno, pair, stream, false);
+      pair = -1;
+    }
     if (pair >= 0) {
       L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
       L.p.sched_run = (int32_t)claim_rows;
@@ -1173,11 +1228,33 @@ int far_set_row_schedule(int mode) {
   return FAR_OK;
 }
 
+int far_get_row_schedule(void) { return g_row_schedule.load(); }
+
 int far_last_launch_claimed_rows(void) { return g_last_claimed; }
+
+int far_sched_pool_model(const int64_t* ops, int n, int* results) {
+  if (n < 0 || (n > 0 && (!ops || !results))) return FAR_ERR_SHAPE;
+  PoolBook book;
+  for (int i = 0; i < n; ++i) {
+    const int64_t op = ops[3 * i], a = ops[3 * i + 1], b = ops[3 * i + 2];
+    if (op == 1) {
+      const uint64_t done = (uint64_t)b;
+      results[i] = book.acquire((unsigned long long)a, [&](int s) { return (int)((done >> s) & 1u); });
+    } else if (op == 2) {
+      if (a < 0 || a >= kSchedSlots || book.pending[a] <= 0) return FAR_ERR_SHAPE;
+      book.release((int)a, (b & 1) != 0, (b & 2) != 0);
+      results[i] = 0;
+    } else {
+      return FAR_ERR_SHAPE;
+    }
+  }
+  return FAR_OK;
+}
 
 int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int sms, int* out8) {
   // kind, nch, warps per row, groups, stages, grid, threads per CTA, dynamic shared bytes
   if (sms < 1 || !out8) return FAR_ERR_SHAPE;
+  PlanQuery query;  // stand-in addresses: no overlap check
   Call c;
   // distinct, aligned, non-overlapping stand-in addresses: only the plan is computed
   const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
@@ -1208,6 +1285,7 @@ int far_plan_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual
 int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int op, int sms,
                              int* rows_per_claim) {
   if (sms < 1 || !rows_per_claim || op < 0 || op > 2) return FAR_ERR_SHAPE;
+  PlanQuery query;  // stand-in addresses: no overlap check
   Call c;
   const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
   char* mb = const_cast<char*>(base);
@@ -1235,6 +1313,7 @@ int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_
 int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int qtype, int sms,
                            int* out8) {
   if (sms < 1 || !out8) return FAR_ERR_SHAPE;
+  PlanQuery query;  // stand-in addresses: no overlap check
   Call c;
   const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
   const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;
@@ -1255,6 +1334,7 @@ int far_plan_quant_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_re
 int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_residual, int beta_offset, int sms,
                         int* out8) {
   if (sms < 1 || !out8 || beta_offset < 0 || beta_offset > 15) return FAR_ERR_SHAPE;
+  PlanQuery query;  // stand-in addresses: no overlap check
   Call c;
   const char* base = reinterpret_cast<const char*>((uintptr_t)1 << 40);
   const uint64_t span = (uint64_t)tokens * hidden * 4 + 4096;

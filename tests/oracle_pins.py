@@ -25,6 +25,16 @@ What pins what:
                     the Luminal page's tolerance of the fp64 evaluation rounded at
                     the declared boundaries.
   pin_policy        fp16 with bf16 rejected; output dtype is the promotion.
+  pin_exhaustive_h1 hidden = 1 over EVERY finite fp16 and every finite bf16 x, with
+                    a few residuals (zero, a permutation of the same values, -x),
+                    weights and eps: every binary32 step of every row against its
+                    binary64 evaluation rounded once to binary32, which is the
+                    correctly rounded binary32 result (the squares and products
+                    of binary32 values are exact in binary64, and for + / sqrt
+                    binary64 carries 53 >= 2 * 24 + 2 bits, so the double rounding
+                    is innocuous: S. A. Figueroa, "When is double rounding
+                    innocuous?", SIGNUM Newsletter 30(3), 1995); residual_out and
+                    the two casts by torch's RNE conversions.
 """
 from __future__ import annotations
 
@@ -334,3 +344,73 @@ def pin_policy(L):
 
 
 ALL_PINS = [pin_policy, pin_residual, pin_sum, pin_steps, pin_closed_forms, pin_fp64]
+
+
+# --------------------------------------------------------------------------
+# hidden = 1, exhaustively over the 16-bit inputs
+# --------------------------------------------------------------------------
+
+def finite_values(dt: str) -> torch.Tensor:
+    """Every finite value of a 16-bit dtype (all 2^16 bit patterns but the infinities and
+    NaNs), as a [N, 1] tensor."""
+    bits = torch.from_numpy(np.arange(65536, dtype=np.uint16).view(np.int16).copy())
+    v = bits.view(TD[dt])
+    return v[torch.isfinite(v.float())].reshape(-1, 1).contiguous()
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def _check_h1_rows(L, x, r, w, eps, act, wd, where):
+    """One hidden = 1 call of the fused op (r given) or of the variant (r None), every row
+    checked step by step against the binary64 evaluation rounded once to binary32."""
+    od = _od(act, wd)
+    eps32 = np.float32(eps)
+    with np.errstate(all="ignore"):
+        if r is not None:
+            # fl32(x + r): the binary64 sum of two binary32 values rounded to binary32
+            s32 = np.float32(_f64(x.float().numpy()[:, 0]) + _f64(r.float().numpy()[:, 0]))
+        else:
+            s32 = x.float().numpy()[:, 0].astype(np.float32)  # exact widening
+        s64 = _f64(s32)
+        S_ref = np.float32(s64 * s64)                       # one square: exact in binary64
+        var_ref = np.float32(_f64(S_ref) / 1.0)             # S / hidden, hidden = 1
+        tv_ref = np.float32(_f64(var_ref) + _f64(eps32))
+        root_ref = np.float32(np.sqrt(_f64(tv_ref)))
+        rstd_ref = np.float32(1.0 / _f64(root_ref))
+        a_ref = np.float32(s64 * _f64(rstd_ref))            # exact product, one rounding
+        n = torch.from_numpy(a_ref).to(TD[wd])              # RNE to the weight dtype
+        prod = np.float32(_f64(n.float().numpy()) * float(w.float()[0]))  # exact product
+        out_ref = torch.from_numpy(prod).to(TD[od]).reshape(-1, 1)
+    S, var, rstd = oracle_mod.row_stats(x, r, eps, act, L=L)
+    for name, got, want in (("S", S, S_ref), ("var", var, var_ref), ("rstd", rstd, rstd_ref)):
+        assert bits_equal(torch.from_numpy(got), torch.from_numpy(want)), \
+            f"{name} differs from its binary64 evaluation ({where})"
+    if r is not None:
+        out, res = oracle_mod.fused_add_rmsnorm(x, r, w, eps, act, wd, L=L)
+        res_ref = torch.from_numpy(s32).to(TD[act]).reshape(-1, 1)  # RNE_act of the binary32 sum
+        assert bits_equal(res, res_ref), f"residual_out ({where})"
+    else:
+        out = oracle_mod.rmsnorm(x, w, eps, act, wd, L=L)
+    assert bits_equal(out, out_ref), f"out ({where})"
+
+
+def pin_exhaustive_h1(L):
+    """hidden = 1 over every finite fp16 and every finite bf16 x (see the module doc)."""
+    for act in ("f16", "bf16"):
+        x = finite_values(act)
+        n = x.shape[0]
+        perm = torch.from_numpy(np.random.default_rng(5).permutation(n))
+        residuals = {"zero": torch.zeros_like(x), "permuted": x[perm].contiguous(), "negated": (-x).contiguous()}
+        weights = [(act, 1.0), (act, -1.375), (act, 0.1), (act, 2.0 ** -20), ("f32", 0.7)]
+        for wd, wv in weights:
+            w = torch.tensor([wv], dtype=TD[wd])
+            for rname, r in residuals.items():
+                _check_h1_rows(L, x, r, w, 1e-6, act, wd, f"{act} x, r {rname}, w {wv} {wd}, eps 1e-6")
+            _check_h1_rows(L, x, None, w, 1e-6, act, wd, f"{act} x, no residual, w {wv} {wd}, eps 1e-6")
+        # eps 0 (a zero row then has rstd = inf and a NaN output) and a large eps
+        w = torch.tensor([1.0], dtype=TD[act])
+        for eps in (0.0, 0.5):
+            _check_h1_rows(L, x, residuals["permuted"], w, eps, act, act, f"{act} x, r permuted, eps {eps}")
+            _check_h1_rows(L, x, None, w, eps, act, act, f"{act} x, no residual, eps {eps}")

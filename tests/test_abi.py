@@ -107,30 +107,40 @@ def test_zero_tokens_is_a_noop(far):
 
 
 def test_row_schedule_hook(far):
-    """far_set_row_schedule takes 0, 1 or 2 and refuses anything else (FAR_ERR_SHAPE);
-    nothing launched on this thread means no rows claimed (a zero-token call launches
-    nothing)."""
+    """The default row schedule is the fixed stride (mode 1: no state kept between calls);
+    far_set_row_schedule takes 0, 1 or 2 and refuses anything else (FAR_ERR_SHAPE), leaving
+    the mode as it was; nothing launched on this thread means no rows claimed (a zero-token
+    call launches nothing)."""
+    assert far.lib.far_get_row_schedule() == 1
     try:
         for mode in (0, 1, 2):
             assert far.lib.far_set_row_schedule(mode) == 0
+            assert far.get_row_schedule() == mode
         for mode in (-1, 3, 1 << 20):
             assert far.lib.far_set_row_schedule(mode) == 4
+            assert far.get_row_schedule() == 2
     finally:
-        assert far.lib.far_set_row_schedule(0) == 0
+        assert far.lib.far_set_row_schedule(1) == 0
     assert far.lib.fused_add_rmsnorm(FAKE, FAKE, FAKE, 1e-6, FAKE, FAKE, 0, 64, code("bf16", "bf16"), None) == 0
     assert far.lib.far_last_launch_claimed_rows() == 0
     assert far.last_launch_claimed_rows() is False
 
 
 def test_row_schedule_rule(far):
-    """The automatic row schedule (host logic): one row a claim where a row moves 45 KB or
-    more, two down to 23 KB, the fixed stride on shorter rows and on launches with fewer
-    than two ring-fulls of rows a CTA left; forced modes override it."""
+    """The default keeps the fixed stride everywhere. The automatic claimed-row rule (mode 0,
+    host logic): one row a claim where a row moves 45 KB or more, two down to 23 KB, the
+    fixed stride on shorter rows and on launches with fewer than two ring-fulls of rows a
+    CTA left; mode 2 claims wherever rows are left."""
     f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
 
     def rows(tokens, hidden, act, wd, residual, op, sms=152):
         return far.row_schedule_for_sms(tokens, hidden, act, wd, residual, op, sms)
 
+    assert far.get_row_schedule() == 1
+    for op in ("rmsnorm", "layernorm", "quant"):
+        assert rows(65536, 8192, f16, f16, True, op) == 0
+        assert rows(65536, 8192, f16, f16, False, op) == 0
+    far.set_row_schedule(0)
     for op in ("rmsnorm", "layernorm", "quant"):
         assert rows(65536, 8192, f16, f16, True, op) == 1      # 64 KB (56 KB quantised) a row
         assert rows(65536, 8192, f16, f16, False, op) == 2     # 32 KB (24 KB)
@@ -140,14 +150,19 @@ def test_row_schedule_rule(far):
     assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 0   # 8 KB
     for tokens, hidden, dt in ((512, 8192, f16), (512, 5120, bf16), (8, 2048, bf16)):
         assert rows(tokens, hidden, dt, dt, True, "rmsnorm") == 0  # under two ring-fulls a CTA
+    assert rows(65536, 1888, bf16, bf16, False, "quant") == 0
     try:
         far.set_row_schedule(1)
         assert rows(65536, 8192, f16, f16, True, "rmsnorm") == 0
         far.set_row_schedule(2)
         assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 6  # ceil(45333 / 8192)
         assert rows(16384, 5120, bf16, bf16, False, "rmsnorm") == 3
+        # a quantised row also moves its 4-byte scale: 1888 x (2 + 1) + 4 = 5668 B, so
+        # ceil(45333 / 5668) = 8 rows a claim (9 if the scale were left out)
+        assert rows(65536, 1888, bf16, bf16, False, "quant") == 8
+        assert rows(65536, 2048, bf16, bf16, False, "rmsnorm") == 6  # ceil(45333 / 8192)
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
     out = ctypes.c_int(0)
     for args in ((0, 8192, 1, 1, 0, 152), (64, 8192, 1, 1, 3, 152), (64, 8192, 1, 1, 0, 0)):
         assert far.lib.far_row_schedule_for_sms(*args, ctypes.addressof(out)) == 4  # FAR_ERR_SHAPE
@@ -407,3 +422,61 @@ def test_host_workspace_size_per_op(far):
     assert far.lib.far_host_workspace_bytes_op(T, H, bf, 1, 1) == 2 * a256(H * 4) + 2 * (3 * a256(T * H * 2) + a256(T * H * 4))
     assert far.lib.far_host_workspace_bytes_op(T, H, bf, 0, 2) == a256(H * 4) + 2 * (a256(T * H * 2) + a256(T * H) + a256(T * 4))
     assert far.lib.far_host_workspace_bytes_op(T, H, bf, 1, 3) == -4
+
+
+def test_counter_pool_bookkeeping(far):
+    """The claimed-row counter pool as host logic (far_sched_pool_model): a stream keeps
+    reusing its own pair, even with launches still pending on it and no event completed; a
+    pair with a launch pending, or whose last launch's event has not completed, is never
+    handed to another stream; a completed event frees it; a pair whose launch got no event
+    is retired for good; with every pair busy a launch gets none (fixed stride)."""
+    ACQ, REL = 1, 2
+    LAUNCHED, RECORDED = 1, 2
+    done_none, done_all = 0, (1 << 64) - 1
+    m = far.sched_pool_model
+    # one stream: the same pair over and over, with launches pending and no event done
+    assert m([(ACQ, 7, done_none), (REL, 0, LAUNCHED | RECORDED), (ACQ, 7, done_none), (ACQ, 7, done_none)]) == \
+        [0, 0, 0, 0]
+    # another stream while pair 0 is pending on stream 7: a fresh pair
+    assert m([(ACQ, 7, done_none), (ACQ, 8, done_none)]) == [0, 1]
+    # pair 0 released, its event not yet done: stream 8 takes a fresh pair; done: next free in turn
+    ops = [(ACQ, 7, done_none), (REL, 0, LAUNCHED | RECORDED), (ACQ, 8, done_none)]
+    assert m(ops) == [0, 0, 1]
+    # after every other pair is taken by other streams, pair 0 goes to stream 9 once its event is done
+    ops = [(ACQ, 7, done_none), (REL, 0, LAUNCHED | RECORDED)]
+    ops += [(ACQ, 100 + s, done_none) for s in range(1, 64)]
+    assert m(ops + [(ACQ, 9, done_none)])[-1] == -1       # every pair busy or unfinished
+    assert m(ops + [(ACQ, 9, 1 << 0)])[-1] == 0            # pair 0's event completed
+    assert m(ops + [(ACQ, 7, done_none)])[-1] == 0         # its own stream still may
+    # a launched pair without an event is retired: neither its stream nor any other gets it back
+    ops = [(ACQ, 7, done_none), (REL, 0, LAUNCHED)]
+    assert m(ops + [(ACQ, 7, done_all)])[-1] == 1
+    assert m(ops + [(ACQ, 8, done_all)])[-1] == 1
+    # a launch that failed to enqueue gives its pair back unused: any stream may take it
+    ops = [(ACQ, 7, done_none), (REL, 0, 0)] + [(ACQ, 100 + s, done_none) for s in range(1, 64)]
+    assert m(ops + [(ACQ, 8, done_none)])[-1] == 0
+    # 64 streams with a launch pending each exhaust the pool; the 65th gets none
+    res = m([(ACQ, 1000 + s, done_all) for s in range(65)])
+    assert sorted(res[:64]) == list(range(64)) and res[64] == -1
+    # errors: an unknown op, giving back a pair that is not handed out
+    flat = (ctypes.c_int64 * 3)(3, 0, 0)
+    out = (ctypes.c_int * 1)()
+    assert far.lib.far_sched_pool_model(ctypes.addressof(flat), 1, ctypes.addressof(out)) == 4
+    flat = (ctypes.c_int64 * 3)(2, 5, 1)
+    assert far.lib.far_sched_pool_model(ctypes.addressof(flat), 1, ctypes.addressof(out)) == 4
+
+
+def test_plan_queries_take_the_largest_shapes(far):
+    """The host-only plan queries answer for every shape the entry points accept, however
+    large: their stand-in addresses are never checked for overlap, so they cannot wrap into
+    a false FAR_ERR_ALIAS."""
+    out = (ctypes.c_int * 8)()
+    one = ctypes.c_int(0)
+    code_ = code("f32", "f32")
+    tokens = (2 ** 63 - 1) // 8 // (1 << 24)  # the largest accepted at hidden 2^24
+    assert far.lib.far_plan_for_sms(tokens, 1 << 24, code_, 1, 152, ctypes.addressof(out)) == 0
+    assert far.lib.far_row_schedule_for_sms(tokens, 1 << 24, code_, 1, 0, 152, ctypes.addressof(one)) == 0
+    assert far.lib.far_plan_quant_for_sms(tokens, 1 << 24, code_, 1, 1, 152, ctypes.addressof(out)) == 0
+    assert far.lib.far_plan_ln_for_sms(tokens, 1 << 24, code_, 1, 0, 152, ctypes.addressof(out)) == 0
+    # one more row is a shape error, as for the entry points
+    assert far.lib.far_plan_for_sms(tokens + 1, 1 << 24, code_, 1, 152, ctypes.addressof(out)) == 4

@@ -32,9 +32,9 @@ def far():
     import mixed_precision_residual_gb300 as far
 
     far.set_launch_override()
-    far.set_row_schedule(0)
+    far.set_row_schedule(1)
     yield far
-    far.set_row_schedule(0)
+    far.set_row_schedule(1)
 
 
 def _nan(shape, dtype):
@@ -100,7 +100,7 @@ def test_claimed_rows_give_the_fixed_stride_bits(far, op, act, wd, tokens, hidde
             assert far.device_status() == 0
             assert _same(got, ref), f"{op} {act}/{wd} {tokens}x{hidden}: launch {i} differs"
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
     assert not any(torch.isnan(o).any() for o in ref if o.is_floating_point()), "a row was left unwritten"
 
 
@@ -117,21 +117,30 @@ def test_claimed_rows_against_the_oracle(far):
         assert far.last_launch_claimed_rows()
         gate(out.cpu(), oracle.rmsnorm(d["x"], d["w"], d["eps"], d["act"], d["wd"]), where="claimed rows")
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
 
 
 def test_default_schedule(far):
-    """The automatic choice claims rows for the fused op at 16384 x 5120 bf16 (40 KB moved a
-    row, two rows a claim, over 2 ring-fulls a CTA) and keeps the fixed stride for its
-    no-residual variant (20 KB a row: three rows a claim) and for the fused op at 512 rows."""
+    """The default keeps the fixed stride (no state between calls). The automatic rule
+    (mode 0) claims rows for the fused op at 16384 x 5120 bf16 (40 KB moved a row, two rows
+    a claim, over 2 ring-fulls a CTA) and keeps the fixed stride for its no-residual variant
+    (20 KB a row: three rows a claim) and for the fused op at 512 rows."""
+    assert far.get_row_schedule() == 1
     _, t = _inputs("bf16", "bf16", 16384, 5120, seed=3)
-    _run(far, "rms_fused", t)
-    assert far.last_launch_claimed_rows()
-    _run(far, "rms", t)
-    assert not far.last_launch_claimed_rows()
-    _, t = _inputs("bf16", "bf16", 512, 5120, seed=4)
-    _run(far, "rms_fused", t)
-    assert not far.last_launch_claimed_rows()
+    for op in ("rms_fused", "rms", "ln_fused", "q_fused"):
+        _run(far, op, t)
+        assert not far.last_launch_claimed_rows(), op
+    try:
+        far.set_row_schedule(0)
+        _run(far, "rms_fused", t)
+        assert far.last_launch_claimed_rows()
+        _run(far, "rms", t)
+        assert not far.last_launch_claimed_rows()
+        _, t = _inputs("bf16", "bf16", 512, 5120, seed=4)
+        _run(far, "rms_fused", t)
+        assert not far.last_launch_claimed_rows()
+    finally:
+        far.set_row_schedule(1)
     assert far.device_status() == 0
 
 
@@ -155,7 +164,7 @@ def test_two_streams_side_by_side(far):
         for which, got in outs:
             assert _same(got, refs[which]), "a launch on one stream lost rows to the other"
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
 
 
 def test_more_launches_in_flight_than_counters(far):
@@ -177,7 +186,7 @@ def test_more_launches_in_flight_than_counters(far):
         for got in outs:
             assert _same(got, ref)
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
 
 
 def test_more_streams_than_counters(far):
@@ -200,7 +209,7 @@ def test_more_streams_than_counters(far):
         for got in outs:
             assert _same(got, ref), "a launch lost rows to another stream's launch"
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)
 
 
 def test_graph_capture_keeps_the_fixed_stride(far):
@@ -231,4 +240,4 @@ def test_graph_capture_keeps_the_fixed_stride(far):
             assert _same([out, res], ref)
         assert far.device_status() == 0
     finally:
-        far.set_row_schedule(0)
+        far.set_row_schedule(1)

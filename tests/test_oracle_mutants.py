@@ -109,6 +109,19 @@ def test_mutant_is_caught(tmp_path, cases, name):
     assert failed, f"no pin rejects the planted mistake {name!r}"
 
 
+@pytest.mark.parametrize("name", ["rstd_single_rounding", "eps_outside_root", "eps_dropped", "early_rounding"])
+def test_exhaustive_hidden_1_catches(tmp_path, name):
+    """The exhaustive hidden = 1 sweep alone rejects mistakes in the rstd step (and the
+    early rounding of the sum); the unmutated copy passes it."""
+    L = _mutant_lib(tmp_path, name, MUTANTS[name])
+    with pytest.raises(AssertionError):
+        P.pin_exhaustive_h1(L)
+
+
+def test_exhaustive_hidden_1_passes_the_unmutated_copy(tmp_path):
+    P.pin_exhaustive_h1(_mutant_lib(tmp_path, "identity_h1", []))
+
+
 def test_unmutated_copy_passes(tmp_path, cases):
     L = _mutant_lib(tmp_path, "identity", [])
     assert _failed_pins(L, cases) == []

@@ -43,6 +43,13 @@ def test_fp64(L, cases):
     P.pin_fp64(L, cases)
 
 
+def test_exhaustive_hidden_1(L):
+    """Every finite fp16 and bf16 x at hidden = 1, every step against binary64."""
+    assert P.finite_values("f16").shape[0] == 65536 - 2 * 1024   # 2 x (1023 NaN + 1 inf)
+    assert P.finite_values("bf16").shape[0] == 65536 - 2 * 128   # 2 x (127 NaN + 1 inf)
+    P.pin_exhaustive_h1(L)
+
+
 def _matrix_cases():
     g = P.golden("contract.json")["test_matrix"]
     return list(itertools.product(g["dtypes"], g["tokens"], g["hidden"]))
