@@ -171,8 +171,9 @@ def test_quantisation_bit_exact_given_out(far, act, wd, hidden):
 
 @pytest.mark.parametrize("act,wd,hidden", [("bf16", "bf16", 4096), ("f16", "f16", 1000), ("f32", "f32", 2048)])
 def test_strided_inputs(far, act, wd, hidden):
-    """x, the residual and residual_out as column slices: codes, scales and residual_out bit
-    for bit the contiguous call's (q and scale stay contiguous)."""
+    """x, the residual and residual_out as column slices: against the oracle (residual_out
+    and scale bit for bit, q within the quantised gate), and bit for bit the contiguous
+    call's (q and scale stay contiguous)."""
     d = far_gen.custom_inputs(act, wd, 40, hidden, seed=hidden + 2)
     T, H = 40, hidden
     x_c, r_c, w = d["x"].cuda(), d["r"].cuda(), d["w"].cuda()
@@ -181,18 +182,24 @@ def test_strided_inputs(far, act, wd, hidden):
     x.copy_(x_c)
     r.copy_(r_c)
     for qtype in ("int8", "fp8"):
+        rq, rs, rres = oracle.fused_add_rmsnorm_quant(d["x"], d["r"], d["w"], d["eps"], act, wd, qtype)
         q, s, res_o = far.fused_add_rmsnorm_quant(x, r, w, d["eps"], qtype, residual_out=res)
         q_c, s_c, res_c = far.fused_add_rmsnorm_quant(x_c, r_c, w, d["eps"], qtype)
         assert far.device_status() == 0
+        assert bits_equal(res.cpu(), rres), f"strided {qtype}: residual_out differs from the oracle"
+        _q_gate(q.cpu().view(torch.uint8) if qtype == "fp8" else q.cpu(), s.cpu(), rq, rs, f"strided {qtype} fused")
         assert torch.equal(q.cpu(), q_c.cpu()) and bits_equal(s.cpu(), s_c.cpu()) and bits_equal(res.cpu(), res_c.cpu())
+        rq, rs = oracle.rmsnorm_quant(d["x"], d["w"], d["eps"], act, wd, qtype)
         q, s = far.rmsnorm_quant(x, w, d["eps"], qtype)
         q_c, s_c = far.rmsnorm_quant(x_c, w, d["eps"], qtype)
         assert far.device_status() == 0
+        _q_gate(q.cpu().view(torch.uint8) if qtype == "fp8" else q.cpu(), s.cpu(), rq, rs, f"strided {qtype}")
         assert torch.equal(q.cpu(), q_c.cpu()) and bits_equal(s.cpu(), s_c.cpu())
 
 
 def test_host_buffers(far):
-    """The host-buffer pipeline for the quantised outputs gives the device path's bits."""
+    """The host-buffer pipeline for the quantised outputs against the oracle (the quantised
+    gate), and bit for bit the device path's."""
     d = far_gen.custom_inputs("f16", "f16", 300, 4096, seed=43)
     xh, rh, wh = (t.pin_memory() for t in (d["x"], d["r"], d["w"]))
     for qtype in ("int8", "fp8"):
@@ -208,6 +215,11 @@ def test_host_buffers(far):
         far.rmsnorm_quant_host(xh, wh, d["eps"], qtype, q2, sc2, ws)
         torch.cuda.synchronize()
         assert far.device_status() == 0
+        oq, os_, ores = oracle.fused_add_rmsnorm_quant(d["x"], d["r"], d["w"], d["eps"], "f16", "f16", qtype)
+        assert bits_equal(res, ores), f"host {qtype}: residual_out differs from the oracle"
+        _q_gate(q.view(torch.uint8) if qtype == "fp8" else q, sc, oq, os_, f"host {qtype} fused")
+        oq, os_ = oracle.rmsnorm_quant(d["x"], d["w"], d["eps"], "f16", "f16", qtype)
+        _q_gate(q2.view(torch.uint8) if qtype == "fp8" else q2, sc2, oq, os_, f"host {qtype}")
         rq, rs, rr = far.fused_add_rmsnorm_quant(d["x"].cuda(), d["r"].cuda(), d["w"].cuda(), d["eps"], qtype)
         assert torch.equal(q, rq.cpu()) and bits_equal(sc, rs.cpu()) and bits_equal(res, rr.cpu())
         rq2, rs2 = far.rmsnorm_quant(d["x"].cuda(), d["w"].cuda(), d["eps"], qtype)
