@@ -348,6 +348,23 @@ def time_launches(fn, stream, n, flush=None):
     return [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
 
 
+def time_stream(fn, stream, n, blocks=5):
+    """Launches in a stream: `blocks` blocks of n launches back to back, each block between
+    two CUDA events (no event between launches, so a launch may be dispatched while the one
+    ahead of it finishes); each block's mean time a launch (ms)."""
+    out = []
+    for _ in range(blocks):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            if fn():
+                raise RuntimeError("launch failed")
+        b.record(stream)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b) / n)
+    return out
+
+
 def measure_configs(far, dev, stream, launches, flush, peak, sms, resident=None):
     """Every workload's fused add+RMSNorm and no-residual RMSNorm, timed per launch both after
     an L2 read sweep and back to back; GB/s and tokens/s from the mean launch time, the
@@ -385,11 +402,17 @@ def measure_configs(far, dev, stream, launches, flush, peak, sms, resident=None)
             k = {"algorithmic_bytes_per_launch": nbytes,
                  "launch_plan": far.describe_launch(T, H, x.dtype, wt.dtype, residual),
                  "row_schedule": row_schedule_text(far, claimed, T, H, x.dtype, wt.dtype, residual, "rmsnorm", sms)}
-            for cond, fl in (("flushed", flush), ("back_to_back", None)):
-                st = launch_stats(time_launches(fn, stream, launches, fl))
+            for cond in ("flushed", "back_to_back", "stream"):
+                if cond == "stream":
+                    ms = time_stream(fn, stream, max(2, launches // 3))
+                else:
+                    ms = time_launches(fn, stream, launches, flush if cond == "flushed" else None)
+                st = launch_stats(ms)
                 gbs = nbytes / (st["mean_ms"] * 1e-3) / 1e9
                 k[cond] = {"gbs": round(gbs, 1), "tokens_per_s": round(T / (st["mean_ms"] * 1e-3), 1),
                            "frac": round(gbs / peak, 4), **st}
+                if cond == "stream":
+                    k[cond]["launches"] = f"{len(ms)} blocks of {max(2, launches // 3)}"
             e[kind] = k
         if far.device_status() != 0:
             raise RuntimeError(f"device status after the {name} launches")
@@ -816,7 +839,9 @@ def main():
                    "eps": eps, "step": OP_STEP[args.op],
                    "l2": "no flush: every tensor (1 GiB) is larger than the 129 MB L2",
                    "parallelism": f"replicas x{world} (rows are independent; no collective)",
-                   "op": args.op, "row_schedule": ROW_SCHEDULE_TEXT[args.row_schedule]},
+                   "op": args.op, "row_schedule": ROW_SCHEDULE_TEXT[args.row_schedule],
+                   "launch": ("programmatic dependent launches (the library default)" if far.get_programmatic_launch()
+                              else "plain launches")},
         "tokens_per_s": round(tokens_per_s, 1),
         "value_covers": (f"the whole step: both kernels ({OP_STEP[args.op]}), their algorithmic bytes over the "
                          f"step time; the fused kernel alone is `roofline`"),
@@ -841,9 +866,13 @@ def main():
         line["configs"] = configs
         line["configs_note"] = (f"per workload: the fused op and the no-residual variant, {args.config_launches} "
                                 f"launches each after a 512 MB L2 read sweep (flushed) and {args.config_launches} "
-                                f"back to back; GB/s and tokens/s from the mean launch time (CUDA events on the "
-                                f"launching stream); frac against the measured copy rate {peak} GB/s; row schedule "
-                                f"as the line's config")
+                                f"back to back, each launch between its own CUDA events on the launching stream "
+                                f"(on the small workloads these include the host's time to issue the launch); "
+                                f"stream: blocks of launches back to back with events only around each block, "
+                                f"spread over the block means (programmatic launch lets each launch be "
+                                f"dispatched while the one ahead finishes); GB/s and tokens/s from the mean launch "
+                                f"time; frac against the measured copy rate {peak} GB/s; row schedule and launch "
+                                f"mode as the line's config")
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds, args.op)
     if rank == 0:

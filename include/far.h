@@ -391,6 +391,22 @@ int far_row_schedule_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_
                              int* rows_per_claim);
 /* the current mode of far_set_row_schedule */
 int far_get_row_schedule(void);
+
+/*
+ * far_set_programmatic_launch: process-wide choice of how the normalisation kernels are
+ * launched.  1 (the default): as programmatic dependent launches, so that a kernel is
+ * dispatched while the kernel ahead of it on the stream finishes, and its CTAs take SMs as
+ * that kernel's CTAs leave them; every kernel of this library first waits until the
+ * kernels ahead of it have completed and their memory operations are visible, before it
+ * touches any global memory, and it allows the next programmatic launch on the stream to
+ * be dispatched as soon as it starts.  Stream order therefore holds as for a plain launch;
+ * a stream of launches (this library's, or a caller's kernels launched the same way and
+ * waiting the same way) loses less time between kernels.  0: plain launches.  The results
+ * are the same bits either way.  Returns FAR_ERR_SHAPE for another value.
+ */
+int far_set_programmatic_launch(int enable);
+/* the current choice of far_set_programmatic_launch */
+int far_get_programmatic_launch(void);
 /* 1 if the calling thread's last kernel launch by this library claimed rows from a
    counter, else 0 (fixed-stride rows, the generic kernel, or no launch) */
 int far_last_launch_claimed_rows(void);

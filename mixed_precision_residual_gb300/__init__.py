@@ -108,6 +108,10 @@ lib.far_last_launch_claimed_rows.argtypes = []
 lib.far_last_launch_claimed_rows.restype = _int
 lib.far_get_row_schedule.argtypes = []
 lib.far_get_row_schedule.restype = _int
+lib.far_set_programmatic_launch.argtypes = [_int]
+lib.far_set_programmatic_launch.restype = _int
+lib.far_get_programmatic_launch.argtypes = []
+lib.far_get_programmatic_launch.restype = _int
 lib.far_sched_pool_model.argtypes = [_vp, _int, _vp]
 lib.far_sched_pool_model.restype = _int
 lib.far_row_schedule_for_sms.argtypes = [_i64, _i64, _int, _int, _int, _int, _vp]
@@ -263,6 +267,16 @@ def set_row_schedule(mode: int = 1) -> None:
     between calls), 0 claimed rows by the automatic rule, 2 claimed rows whenever possible
     (the same bits in every mode)."""
     _check(lib.far_set_row_schedule(mode))
+
+
+def set_programmatic_launch(enable: bool = True) -> None:
+    """Launch the normalisation kernels as programmatic dependent launches (the default) or
+    plainly (the same bits either way)."""
+    _check(lib.far_set_programmatic_launch(int(bool(enable))))
+
+
+def get_programmatic_launch() -> bool:
+    return bool(lib.far_get_programmatic_launch())
 
 
 def get_row_schedule() -> int:

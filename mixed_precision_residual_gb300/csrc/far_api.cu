@@ -108,6 +108,9 @@ struct SchedPool {
 };
 SchedPool g_sched_pool[kMaxDevices];
 
+// programmatic dependent launch of the norm kernels: 1 (default) on, 0 off
+std::atomic<int> g_programmatic{1};
+
 // row schedule: 1 fixed stride always (the default: no state kept between calls),
 // 0 claimed rows by the automatic rule, 2 claimed rows whenever a pair is free
 std::atomic<int> g_row_schedule{1};
@@ -409,6 +412,7 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
   p.status = status;
   p.timeout_ns = kWaitTimeoutNs;
   L.stream = stream;
+  L.programmatic = g_programmatic.load() != 0;
 
   const int sa = dsize(c.act), sw = dsize(c.wd);
   const int64_t row_bytes = c.hidden * sa;
@@ -1229,6 +1233,14 @@ int far_set_row_schedule(int mode) {
 }
 
 int far_get_row_schedule(void) { return g_row_schedule.load(); }
+
+int far_set_programmatic_launch(int enable) {
+  if (enable != 0 && enable != 1) return FAR_ERR_SHAPE;
+  g_programmatic = enable;
+  return FAR_OK;
+}
+
+int far_get_programmatic_launch(void) { return g_programmatic.load(); }
 
 int far_last_launch_claimed_rows(void) { return g_last_claimed; }
 

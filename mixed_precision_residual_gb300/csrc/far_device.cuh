@@ -423,6 +423,22 @@ __device__ __forceinline__ float row_rstd(float S, float hidden_f, float eps) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch (inline PTX; both are no-ops in a kernel launched without
+// the programmatic-stream-serialization attribute)
+// ---------------------------------------------------------------------------
+
+// Let the next kernel on the stream, if it was launched with the attribute, be dispatched
+// now: its CTAs take SMs as this grid's CTAs leave them.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until every kernel before this one on the stream has completed and its memory
+// operations are visible.  Every kernel here calls it before its first access to global
+// memory, so stream order holds whatever the launch attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // mbarrier, bulk copy, timer (inline PTX)
 // ---------------------------------------------------------------------------
 

@@ -26,6 +26,8 @@
 // the weight multiply.
 #pragma once
 
+#include <type_traits>
+
 #include "far_device.cuh"
 
 namespace far {
@@ -66,10 +68,23 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
   // no residual and 16-bit x: s = x exactly, so x stays packed between the passes
   // (LayerNorm needs the binary32 deviations s - mean instead)
   constexpr bool PACKED = packed_rows(RES, ACT) && !LN;
+  // 16-bit activations with a binary32 out: a thread's chunk j is two 8-byte pieces of the
+  // row, 32 lanes apart (pieces 2b + lane and 2b + 32 + lane of the warp's window of 32
+  // chunks starting at chunk b), so that every warp-wide access is contiguous: out in
+  // 512-byte runs (one 16-byte store of 4 binary32 values a lane), residual_out in 256-byte
+  // runs.  Lanes of a 16-byte chunk instead would leave each out store covering every
+  // other 16 bytes of 1 KB (32 half-written sectors a request instead of 16).  (A
+  // quantised output stores no binary32 values: its stores are contiguous already.)
+  constexpr bool PIECE = (SA == 2 && SO == 4 && Q == kQuantNone);
+  constexpr int PB = PIECE ? 8 : 16;   // activation bytes a piece (a whole chunk unless PIECE)
 
   constexpr int NRED = reduce_buffers(Q, LN);  // cross-warp reduction buffers per group
 
   extern __shared__ __align__(128) unsigned char smem[];
+  // the next kernel on the stream may be dispatched now; nothing of global memory is touched
+  // before the kernels ahead of this one have completed
+  pdl_launch_dependents();
+  pdl_wait();
   const int stages = p.stages, groups = p.groups, G = p.warps_per_row;
   // layout: full[stages] | empty[stages] | reduce[groups][NRED] | partials[groups][NRED][G] |
   //         slot_row[stages] | w | ring
@@ -209,6 +224,64 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
   int slot = g;          // k % stages for this group's positions k = g, g + groups, ...
   uint32_t phase = 0;    // (k / stages) & 1
   uint32_t it = 0;       // this group's row count, for the reduction buffers
+  // This thread's chunk j: its pieces (in PB-byte units of the activation row: one piece, the
+  // chunk itself, unless PIECE) and whether each lies inside the row.  Elements 0 .. V/2 - 1
+  // of the chunk come from piece pa, V/2 .. V - 1 from piece pb (the same piece unless PIECE).
+  struct Where {
+    int pa, pb;
+    bool va, vb;
+  };
+  auto where = [&](int j) {
+    const int c = (j * G + wg) * 32 + lane;
+    Where w;
+    if constexpr (PIECE) {
+      w.pa = 2 * c - lane;  // piece 2b + lane of the window of chunks b = c - lane ..
+      w.pb = w.pa + 32;
+      w.va = EXACT || w.pa < 2 * C;
+      w.vb = EXACT || w.pb < 2 * C;
+    } else {
+      w.pa = w.pb = c;
+      w.va = w.vb = EXACT || c < C;
+    }
+    return w;
+  };
+  // the chunk's 16 activation bytes from a shared-memory row (zeros for a piece past the row)
+  auto load_act = [&](const unsigned char* base, const Where& w, uint32_t* v) {
+    if constexpr (PIECE) {
+      uint32_t a[2] = {0u, 0u}, b2[2] = {0u, 0u};
+      if (w.va) load_bytes<8>(base + (size_t)w.pa * 8, a);
+      if (w.vb) load_bytes<8>(base + (size_t)w.pb * 8, b2);
+      v[0] = a[0];
+      v[1] = a[1];
+      v[2] = b2[0];
+      v[3] = b2[1];
+    } else {
+      load_bytes<16>(base + (size_t)w.pa * 16, v);
+    }
+  };
+  // the chunk's NB bytes of a per-element vector held in shared memory (the weight, beta):
+  // NB / 2 bytes a piece; zeros for a piece past the row
+  auto load_vec = [&](const unsigned char* base, const Where& w, uint32_t* v, auto nb) {
+    constexpr int NB = decltype(nb)::value;
+    if constexpr (PIECE) {
+#pragma unroll
+      for (int i = 0; i < NB / 4; ++i) v[i] = 0u;
+      if (w.va) load_bytes<NB / 2>(base + (size_t)w.pa * (NB / 2), v);
+      if (w.vb) load_bytes<NB / 2>(base + (size_t)w.pb * (NB / 2), v + NB / 8);
+    } else {
+      load_bytes<NB>(base + (size_t)w.pa * NB, v);
+    }
+  };
+  // the chunk's NB bytes of an output row (NB / 2 a piece; pieces past the row not written)
+  auto store_row = [&](char* rowp, const Where& w, const uint32_t* v, auto nb) {
+    constexpr int NB = decltype(nb)::value;
+    if constexpr (PIECE) {
+      if (w.va) store_bytes<NB / 2>(rowp + (size_t)w.pa * (NB / 2), v);
+      if (w.vb) store_bytes<NB / 2>(rowp + (size_t)w.pb * (NB / 2), v + NB / 8);
+    } else {
+      store_bytes<NB>(rowp + (size_t)w.pa * NB, v);
+    }
+  };
   for (;; ++it) {
     if (!mbar_wait(smem_addr(&bars[slot]), phase, p.timeout_ns, p.status)) return;
     const int64_t row = slot_row[slot];  // read before the slot is released
@@ -222,11 +295,11 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     DW2 accp[2] = {{0ull, 0ull}, {0ull, 0ull}};  // LayerNorm: four chains in packed pairs
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const int c = (j * G + wg) * 32 + lane;
+      const Where w = where(j);
       if constexpr (PACKED) {
-        if (EXACT || c < C) {
-          const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
-          const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+        if (w.va) {
+          uint32_t xw[4];
+          load_act(xs, w, xw);
 #pragma unroll
           for (int e = 0; e < V / 2; ++e) {
             xk[j][e] = xw[e];
@@ -235,13 +308,14 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
             dw_add(acc[(2 * e + 1) & 3], q.y);
           }
         }
-      } else if (EXACT || c < C) {
-        const uint4 xv = *reinterpret_cast<const uint4*>(xs + (size_t)c * 16);
-        const uint32_t* xw = reinterpret_cast<const uint32_t*>(&xv);
+      } else if (w.va) {
+        uint32_t xw[4];
+        load_act(xs, w, xw);
         if constexpr (RES) {
-          const uint4 rv = *reinterpret_cast<const uint4*>(xs + r_off + (size_t)c * 16);
+          uint32_t rv[4];
+          load_act(xs + r_off, w, rv);
           float rf[V];
-          widen<ACT, V>(reinterpret_cast<const uint32_t*>(&rv), rf);
+          widen<ACT, V>(rv, rf);
           if constexpr (ACT == FAR_F32) {
 #pragma unroll
             for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(__uint_as_float(xw[e]), rf[e]);
@@ -290,12 +364,12 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       DW2 accq[2] = {{0ull, 0ull}, {0ull, 0ull}};
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        const int c = (j * G + wg) * 32 + lane;
-        if (EXACT || c < C) {
+        const Where w = where(j);
+        if (w.va) {
           if constexpr (RES) {
             uint32_t rw[4];
             narrow<ACT, V>(s[j], rw);
-            store_bytes<16>(rrow + (size_t)c * 16, rw);
+            store_row(rrow, w, rw, std::integral_constant<int, 16>{});
           }
 #pragma unroll
           for (int e = 0; e < V / 2; ++e) {
@@ -303,7 +377,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
             const float2 df = unpk(dv);
             s[j][2 * e] = df.x;
             s[j][2 * e + 1] = df.y;
-            dw2_add_nonneg(accq[e & 1], mul_x2(dv, dv));  // fl32(d * d), through max / min
+            // (a piece past the row holds zeros, not values of s: no deviation of it is summed)
+            if (!PIECE || e < V / 4 || w.vb) dw2_add_nonneg(accq[e & 1], mul_x2(dv, dv));  // fl32(d * d), through max / min
           }
         }
       }
@@ -330,8 +405,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     uint32_t amax2 = 0u;  // packed running max of |out| for a 16-bit out
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
-      const int c = (j * G + wg) * 32 + lane;
-      if (EXACT || c < C) {
+      const Where w = where(j);
+      if (w.va) {
         float sj[V];  // s for this chunk: kept in registers, or widened from the packed x
         if constexpr (PACKED) widen<ACT, V>(xk[j], sj);
         else {
@@ -339,12 +414,12 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
           for (int e = 0; e < V; ++e) sj[e] = s[j][e];
         }
         uint32_t ww[WB / 4];
-        load_bytes<WB>(wsm + (size_t)c * WB, ww);
+        load_vec(wsm, w, ww, std::integral_constant<int, WB>{});
         uint32_t ow[OB / 4];
         if constexpr (LN) {
           // out = RNE_od(fl32(fl32(RNE_wd(d * rstd) * gamma) + beta)), two lanes at a time
           uint32_t bw[WB / 4];
-          load_bytes<WB>(bsm + (size_t)c * WB, bw);
+          load_vec(bsm, w, bw, std::integral_constant<int, WB>{});
           const uint64_t rstd2 = pk(rstd, rstd);
           float o[V];
 #pragma unroll
@@ -391,12 +466,12 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
 #pragma unroll
           for (int e = 0; e < OB / 4; ++e) okeep[j][e] = ow[e];
         } else {
-          store_bytes<OB>(orow + (size_t)c * OB, ow);
+          store_row(orow, w, ow, std::integral_constant<int, OB>{});
         }
         if constexpr (RES && !LN) {
           uint32_t rw[4];
           narrow<ACT, V>(sj, rw);
-          store_bytes<16>(rrow + (size_t)c * 16, rw);
+          store_row(rrow, w, rw, std::integral_constant<int, 16>{});
         }
       }
     }
@@ -426,8 +501,8 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       unsigned char* qrow = static_cast<unsigned char*>(p.q) + row * (int64_t)p.hidden;
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
-        const int c = (j * G + wg) * 32 + lane;
-        if (EXACT || c < C) {
+        const Where w = where(j);
+        if (w.va) {
           float of[V];
           widen<OD, V>(okeep[j], of);
           uint32_t qw[V / 4];
@@ -435,10 +510,11 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
           for (int e = 0; e < V / 4; ++e)
             qw[e] = quantise4<Q>(__fmul_rn(of[4 * e], inv), __fmul_rn(of[4 * e + 1], inv),
                                  __fmul_rn(of[4 * e + 2], inv), __fmul_rn(of[4 * e + 3], inv));
-          if constexpr (V == 8)
-            store_bytes<8>(qrow + (size_t)c * 8, qw);
-          else
-            asm volatile("st.global.b32 [%0], %1;" ::"l"(qrow + (size_t)c * 4), "r"(qw[0]) : "memory");
+          if constexpr (V == 8) {
+            store_bytes<8>(qrow + (size_t)w.pa * 8, qw);
+          } else {
+            asm volatile("st.global.b32 [%0], %1;" ::"l"(qrow + (size_t)w.pa * 4), "r"(qw[0]) : "memory");
+          }
         }
       }
     }
@@ -523,6 +599,8 @@ __global__ void __launch_bounds__(kGenericThreads) generic_kernel(const Params p
   constexpr int NW = kGenericThreads / 32;
   __shared__ float2 part[NW];
   __shared__ float mpart[NW];
+  pdl_launch_dependents();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t H = p.hidden;
   for (int64_t row = blockIdx.x; row < p.tokens; row += gridDim.x) {
@@ -629,8 +707,23 @@ cudaError_t launch_typed(const Launch& L) {
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(k), L.smem);
     if (e != cudaSuccess) return e;
   }
-  k<<<L.grid, L.block, L.smem, L.stream>>>(L.p);
-  return cudaGetLastError();
+  if (!L.programmatic) {
+    k<<<L.grid, L.block, L.smem, L.stream>>>(L.p);
+    return cudaGetLastError();
+  }
+  // programmatic dependent launch: this kernel may be dispatched while the kernel ahead of
+  // it on the stream finishes (it waits for that kernel's completion before touching memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = L.grid;
+  cfg.blockDim = L.block;
+  cfg.dynamicSmemBytes = L.smem;
+  cfg.stream = L.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, L.p);
 }
 
 // the plain output

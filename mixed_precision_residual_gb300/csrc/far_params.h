@@ -76,6 +76,7 @@ struct Launch {
   dim3 grid, block;
   size_t smem;
   cudaStream_t stream;
+  bool programmatic;  // launched as a programmatic dependent launch
 };
 
 // cross-warp reduction buffers per group: two (the sum of squares, double-buffered over
