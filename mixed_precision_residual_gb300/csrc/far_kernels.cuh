@@ -76,7 +76,6 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
   // other 16 bytes of 1 KB (32 half-written sectors a request instead of 16).  (A
   // quantised output stores no binary32 values: its stores are contiguous already.)
   constexpr bool PIECE = (SA == 2 && SO == 4 && Q == kQuantNone);
-  constexpr int PB = PIECE ? 8 : 16;   // activation bytes a piece (a whole chunk unless PIECE)
 
   constexpr int NRED = reduce_buffers(Q, LN);  // cross-warp reduction buffers per group
 
@@ -438,11 +437,23 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
           }
           narrow<OD, V>(o, ow);
         } else if constexpr (WD == OD && WD != FAR_F32) {
-          // 16-bit weight and output (then act == wd): cast to the weight dtype,
-          // then one packed multiply rounds the exact product once
+          // 16-bit weight and output (then act == wd): cast to the weight dtype, then one
+          // packed multiply rounds the exact product once.  With a quantised output s * rstd
+          // is formed two lanes at a time (each half rounded as the scalar multiply; it feeds
+          // only the cast, never an add); the plain kernels keep the scalar form, whose
+          // registers fit without spilling
+          if constexpr (Q != kQuantNone) {
+            const uint64_t rstd2 = pk(rstd, rstd);
 #pragma unroll
-          for (int e = 0; e < V / 2; ++e)
-            ow[e] = mul2<WD>(narrow2<WD>(__fmul_rn(sj[2 * e], rstd), __fmul_rn(sj[2 * e + 1], rstd)), ww[e]);
+            for (int e = 0; e < V / 2; ++e) {
+              const float2 a = unpk(mul_x2(pk(sj[2 * e], sj[2 * e + 1]), rstd2));
+              ow[e] = mul2<WD>(narrow2<WD>(a.x, a.y), ww[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < V / 2; ++e)
+              ow[e] = mul2<WD>(narrow2<WD>(__fmul_rn(sj[2 * e], rstd), __fmul_rn(sj[2 * e + 1], rstd)), ww[e]);
+          }
         } else {
           float wf[V];
           widen<WD, V>(ww, wf);
@@ -499,6 +510,13 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       const float inv = amax == 0.f ? 0.f : __fdiv_rn(QMAX, amax);
       if (wg == 0 && lane == 0) p.scale[row] = __fdiv_rn(amax, QMAX);
       unsigned char* qrow = static_cast<unsigned char*>(p.q) + row * (int64_t)p.hidden;
+      // int8 of a row whose largest |out| is finite: every v = fl32(out * inv) lies within
+      // +-(127 + 2^-17), so adding 1.5 * 2^23 in binary32 rounds it to the nearest integer,
+      // ties to even, and leaves that integer (two's complement) in the low byte: the
+      // saturating conversion's result, on the FMA pipe and two lanes an instruction.  A row
+      // whose largest |out| is NaN or infinite has every v NaN or +-0: all codes 0.
+      const bool finite_row = isfinite(amax);
+      const uint64_t magic2 = pk(12582912.0f, 12582912.0f);
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const Where w = where(j);
@@ -506,10 +524,22 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
           float of[V];
           widen<OD, V>(okeep[j], of);
           uint32_t qw[V / 4];
+          if constexpr (Q == kQuantInt8) {
 #pragma unroll
-          for (int e = 0; e < V / 4; ++e)
-            qw[e] = quantise4<Q>(__fmul_rn(of[4 * e], inv), __fmul_rn(of[4 * e + 1], inv),
-                                 __fmul_rn(of[4 * e + 2], inv), __fmul_rn(of[4 * e + 3], inv));
+            for (int e = 0; e < V / 4; ++e) {
+              // the products by the scalar multiply (never contracted into the add)
+              const uint64_t t01 = add_x2(pk(__fmul_rn(of[4 * e], inv), __fmul_rn(of[4 * e + 1], inv)), magic2);
+              const uint64_t t23 = add_x2(pk(__fmul_rn(of[4 * e + 2], inv), __fmul_rn(of[4 * e + 3], inv)), magic2);
+              const uint32_t lo = __byte_perm((uint32_t)t01, (uint32_t)(t01 >> 32), 0x0040);
+              const uint32_t hi = __byte_perm((uint32_t)t23, (uint32_t)(t23 >> 32), 0x0040);
+              qw[e] = finite_row ? __byte_perm(lo, hi, 0x5410) : 0u;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < V / 4; ++e)
+              qw[e] = quantise4<Q>(__fmul_rn(of[4 * e], inv), __fmul_rn(of[4 * e + 1], inv),
+                                   __fmul_rn(of[4 * e + 2], inv), __fmul_rn(of[4 * e + 3], inv));
+          }
           if constexpr (V == 8) {
             store_bytes<8>(qrow + (size_t)w.pa * 8, qw);
           } else {
