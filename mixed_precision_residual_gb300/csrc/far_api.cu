@@ -496,9 +496,12 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       } else if (c.residual) {
         group_cap = G >= 4 ? 3 : (G == 1 ? 10 : 5);
       } else {
-        group_cap = wide_out ? 5 : kMaxConsumerWarps;
+        // the variant: one-warp rows at most 10 groups (12 measured 9 % slower in a stream,
+        // bf16 16384 x 2048); rows of 4+ warps two ring slots a group (fp16 65536 x 8192:
+        // 424 us against 436 with claimed rows, 458 against 467 at the fixed stride)
+        group_cap = wide_out ? 5 : (G == 1 ? 10 : kMaxConsumerWarps);
       }
-      slots_per_group = 1;
+      slots_per_group = (!c.residual && !wide_out && G >= 4) ? 2 : 1;
     } else if (c.ln) {
       // LayerNorm on rows of one warp at up to 4 chunks a thread (hidden up to 1024 in
       // 16-bit): 7 groups (measured 5-50 % faster than a rows-per-group cap), of two slots
@@ -531,16 +534,22 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
         group_cap = c.residual ? 7 : 10;
       }
       // (the variant on 16-bit rows holds up to 19 warps: measured 5-10 % faster than 12 on
-      // hidden 4096 and 8192)
-      slots_per_group = 1;
+      // hidden 4096 and 8192); the variant on rows of 4+ warps takes two ring slots a group
+      // (int8, fp16 65536 x 8192: 347 us against 359 in a stream; 16384 x 8192: 94.5 / 97.1)
+      slots_per_group = (!c.residual && G >= 4) ? 2 : 1;
     } else if (c.od == FAR_F32 && !c.quant) {
       // fp32 output (or fp32 activations): rows are long in bytes; keep about 128 KB
-      // (fused) or 120 KB (variant) of rows in progress per SM, one ring slot per group
+      // (fused) or 120 KB (variant) of rows in progress per SM, one ring slot per group.
+      // The variant of 16-bit activations, from a sweep timed in a stream (launches back to
+      // back) and after an L2 flush: 72 KB in progress above 64 rows an SM, and 3 slots a
+      // group on one-warp rows, 2 on two-warp rows (bf16 / fp32 weight 4096 x 4096: 18.1 us
+      // against 19.2; 16384 x 4096: 66.0 against 67.5; 32768 x 2048: ~65 against 69.0)
       const int64_t row_total = c.hidden * (c.residual ? (3 * sa + dsize(c.od)) : (sa + dsize(c.od)));
-      const int64_t budget = c.residual ? 128 * 1024 : 120 * 1024;
+      const bool variant16 = !c.residual && c.act != FAR_F32;
+      const int64_t budget = c.residual ? 128 * 1024 : ((variant16 && rows_per_sm > 64) ? 72 : 120) * 1024;
       const int64_t want = (budget + row_total / 2) / row_total;
       group_cap = (int)(want < 1 ? 1 : want);
-      slots_per_group = 1;
+      slots_per_group = variant16 ? (G == 1 ? 3 : (G == 2 ? 2 : 1)) : 1;
     } else if (c.residual && C > 128 && G <= max_consumer_warps(nch, false)) {
       // fused rows, one ring slot per group, from sweeps of every plan timed both after an
       // L2 flush and back to back (where each launch writes back the previous one's output
@@ -572,15 +581,20 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       // the no-residual variant on 16-bit rows (x kept packed), from a sweep of every plan
       // on 59 shapes (hidden 1024 to 16384, 512 to 65536 tokens): rows of up to 192 chunks
       // 7 groups of 2 slots; one warp a row 7 groups of 3 slots (1 below 100 rows an SM);
-      // two warps 8 groups of one slot; three 6; four 4; more, 16 warps in groups of 2 slots
-      // (of one slot at 8+ warps a row, measured back to back)
+      // three warps 6 groups of one slot; four 4; more, 16 warps in groups of 2 slots (of one
+      // slot at 8+ warps a row, measured back to back).  Two warps a row: 5 groups of 2
+      // slots, from a later sweep timed in a stream (programmatic launch) and after an L2
+      // flush (fp16 16384 x 4096: 44.6 us against 47.8 for 8 groups of one slot); three
+      // warps with idle lanes (hidden 5120 at 8 chunks, taken above 128 rows an SM, see
+      // below) 5 groups of 2 slots as well
       if (C <= 192) {
         group_cap = 7;
         slots_per_group = 2;
       } else if (G <= 4) {
-        const int caps[5] = {0, 7, 8, 6, 4};
-        group_cap = caps[G];
-        slots_per_group = (G == 1 && rows_per_sm >= 100) ? 3 : 1;
+        const bool idle3 = G == 3 && C % 256 != 0;
+        const int caps[5] = {0, 7, 5, 6, 4};
+        group_cap = idle3 ? 5 : caps[G];
+        slots_per_group = G == 1 ? (rows_per_sm >= 100 ? 3 : 1) : ((G == 2 || idle3) ? 2 : 1);
       } else {
         group_cap = kMaxConsumerWarps / G;
         slots_per_group = G >= 8 ? 1 : 2;
@@ -607,15 +621,19 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
     // the same number of warps (hidden 2560 or 3072 in 16-bit) takes the exact plan: measured
     // 3-8 % faster (at most 6 groups fused, 7 for the variant); plain RMSNorm only.
     // The packed variant on rows of 640 chunks (hidden 5120 in 16-bit), which 8 chunks cover
-    // with 3 warps and idle lanes, runs 10 chunks on 2 warps: measured 6-10 % faster from
-    // 2048 to 24576 tokens and as fast above, with 7 groups of one slot above 128 rows an
-    // SM, 5 groups of 2 slots from 65 to 128 (the best mean of timings after an L2 flush
-    // and back to back at 16384 tokens) and 9 of one slot below.
-    if (nch == 8 && packed && C == 640 && c.od != FAR_F32 && !one_group) {
+    // with 3 warps and idle lanes: up to 128 rows an SM it runs 10 chunks on 2 warps, 5
+    // groups of one slot (two above 32 rows an SM); above, 8 chunks on 3 warps in 5 groups
+    // of 2 slots, as the rule above gives.  Timed in a stream (programmatic launch) and
+    // after an L2 flush, bf16: 4096 tokens 15.6 us against 17.2 (9 groups of one slot);
+    // 8192 30.4 against 33.1; 65536 196.7 against 208.4 (10 chunks, 7 groups).  At 16384
+    // tokens (108 rows an SM) 8 chunks on 3 warps were faster in a stream (55.9 against
+    // 58.2 us) but slower from a clean L2 (57.4 against 53.5; under ncu 56.2 against
+    // 52.5), so 10 chunks stay there.
+    if (nch == 8 && packed && C == 640 && c.od != FAR_F32 && !one_group && rows_per_sm <= 128) {
       nch = 10;
       G = 2;
-      group_cap = rows_per_sm > 128 ? 7 : (rows_per_sm > 64 ? 5 : 9);
-      slots_per_group = (rows_per_sm > 64 && rows_per_sm <= 128) ? 2 : 1;
+      group_cap = 5;
+      slots_per_group = rows_per_sm > 32 ? 2 : 1;
     }
     if (nch == 8 && !c.quant && !c.ln && C % 256 != 0 && !one_group) {
       for (int cand : {6, 5}) {
