@@ -724,10 +724,12 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
 // logic only; whether a counter pair is free, or the stream capturing, is decided at
 // launch). Rows a claim: as few as keep the claims below ~150 M/s at the copy rate
 // (~6.8 TB/s), well under the ~250 M/s that one counter's atomics were measured to sustain
-// on GB300. Claimed rows by default where that is one or two rows (rows moving 23 KB or
-// more) and at least as many rows are left after every CTA's first ring-full as those
-// take: on shorter rows the fixed stride was as fast or faster; forced, wherever rows are
-// left.
+// on GB300. Claimed rows by the automatic rule where that is one or two rows (rows moving
+// 23 KB or more) and at least three times as many rows are left after every CTA's first
+// ring-full as those take: on shorter rows the fixed stride was as fast or faster, and on
+// launches of fewer ring-fulls the claims' round trips delay the loads more than the
+// balance gains (bf16 / fp32-weight 4096 x 4096 variant, 2.7 ring-fulls a CTA: 19.7 us
+// against 18.0 at the fixed stride); forced, wherever rows are left.
 int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
   if (L.kind != kStaged || c.fixed_stride || mode == 1) return 0;
   // bytes a row moves: x (and the residual and residual_out), then out, or the quantised
@@ -737,7 +739,7 @@ int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
                               (c.quant ? 4 : 0);
   const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
   const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
-  if (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 2 * r0))
+  if (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 4 * r0))
     return claim_rows < (1 << 20) ? claim_rows : (1 << 20);
   return 0;
 }

@@ -129,8 +129,8 @@ def test_row_schedule_hook(far):
 def test_row_schedule_rule(far):
     """The default keeps the fixed stride everywhere. The automatic claimed-row rule (mode 0,
     host logic): one row a claim where a row moves 45 KB or more, two down to 23 KB, the
-    fixed stride on shorter rows and on launches with fewer than two ring-fulls of rows a
-    CTA left; mode 2 claims wherever rows are left."""
+    fixed stride on shorter rows and on launches with fewer than four ring-fulls of rows a
+    CTA; mode 2 claims wherever rows are left."""
     f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
 
     def rows(tokens, hidden, act, wd, residual, op, sms=152):
@@ -149,7 +149,10 @@ def test_row_schedule_rule(far):
     assert rows(4096, 4096, bf16, f32, True, "rmsnorm") == 2     # 40 KB
     assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 0   # 8 KB
     for tokens, hidden, dt in ((512, 8192, f16), (512, 5120, bf16), (8, 2048, bf16)):
-        assert rows(tokens, hidden, dt, dt, True, "rmsnorm") == 0  # under two ring-fulls a CTA
+        assert rows(tokens, hidden, dt, dt, True, "rmsnorm") == 0  # under four ring-fulls a CTA
+    # bf16 / fp32-weight 4096 x 4096 variant: 24 KB a row (two a claim) but 10 ring slots, so
+    # 4096 rows are 2.7 ring-fulls of 152 CTAs: the fixed stride
+    assert rows(4096, 4096, bf16, f32, False, "rmsnorm") == 0
     assert rows(65536, 1888, bf16, bf16, False, "quant") == 0
     try:
         far.set_row_schedule(1)
@@ -480,3 +483,31 @@ def test_plan_queries_take_the_largest_shapes(far):
     assert far.lib.far_plan_ln_for_sms(tokens, 1 << 24, code_, 1, 0, 152, ctypes.addressof(out)) == 0
     # one more row is a shape error, as for the entry points
     assert far.lib.far_plan_for_sms(tokens + 1, 1 << 24, code_, 1, 152, ctypes.addressof(out)) == 4
+
+
+def test_plans_of_the_bench_workloads(far):
+    """The planner's choices on a 152-SM GB300 for the five workloads, fused op and variant,
+    and LayerNorm and int8 on the fp16 65536 x 8192 one: {kind, chunks a thread, warps a
+    row, groups, ring slots, grid}. Each was chosen from timed sweeps of every plan (a change
+    here should come with new measurements)."""
+    f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
+    keys = ("kind", "nch", "warps_per_row", "groups", "stages", "grid")
+    want = {
+        ("c1", True): [0, 1, 8, 1, 4, 8], ("c1", False): [0, 1, 8, 1, 4, 8],
+        ("c2", True): [0, 8, 4, 3, 3, 152], ("c2", False): [0, 8, 4, 4, 4, 128],
+        ("c3", True): [0, 8, 2, 3, 3, 152], ("c3", False): [0, 8, 2, 5, 10, 152],
+        ("c4", True): [0, 5, 4, 3, 3, 152], ("c4", False): [0, 10, 2, 5, 10, 152],
+        ("c5", True): [0, 8, 4, 2, 2, 152], ("c5", False): [0, 8, 4, 4, 4, 152],
+    }
+    shapes = {"c1": (bf16, bf16, 8, 2048), "c2": (f16, f16, 512, 8192), "c3": (bf16, f32, 4096, 4096),
+              "c4": (bf16, bf16, 16384, 5120), "c5": (f16, f16, 65536, 8192)}
+    for (name, residual), plan in want.items():
+        a, w, T, H = shapes[name]
+        p = far.plan_for_sms(T, H, a, w, residual, 152)
+        assert [p[k] for k in keys] == plan, (name, residual, p)
+    for residual, ln, q8 in ((True, [0, 8, 4, 2, 2, 152], [0, 8, 4, 2, 2, 152]),
+                             (False, [0, 8, 4, 3, 6, 152], [0, 8, 4, 4, 8, 152])):
+        p = far.plan_ln_for_sms(65536, 8192, f16, f16, residual, 152)
+        assert [p[k] for k in keys] == ln, ("layernorm", residual, p)
+        p = far.plan_quant_for_sms(65536, 8192, f16, f16, residual, "int8", 152)
+        assert [p[k] for k in keys] == q8, ("int8", residual, p)
