@@ -498,7 +498,17 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       } else {
         // the variant: one-warp rows at most 10 groups (12 measured 9 % slower in a stream,
         // bf16 16384 x 2048); rows of 4+ warps two ring slots a group (fp16 65536 x 8192:
-        // 424 us against 436 with claimed rows, 458 against 467 at the fixed stride)
+        // 424 us against 436 with claimed rows, 458 against 467 at the fixed stride); with
+        // a 16-bit output, rows that 8 chunks a thread would cover with idle lanes take 5 or
+        // 6 chunks where those cover them exactly (hidden 2560, 3072, 5120 in 16-bit)
+        if (!wide_out && C % 256 != 0) {
+          for (int cand : {5, 6})
+            if (C % (32LL * cand) == 0 && C / (32LL * cand) <= kMaxConsumerWarps) {
+              nch = cand;
+              G = (int)(C / (32LL * cand));
+              break;
+            }
+        }
         group_cap = wide_out ? 5 : (G == 1 ? 10 : kMaxConsumerWarps);
       }
       slots_per_group = (!c.residual && !wide_out && G >= 4) ? 2 : 1;
@@ -654,8 +664,8 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       one_group = false;
     }
     staged = G <= max_consumer_warps(nch, packed);
-    // 5 or 6 chunks a thread exist only as exact plain-RMSNorm kernels
-    if ((nch == 5 || nch == 6) && (C != 32LL * nch * G || c.quant || c.ln)) staged = false;
+    // 5 or 6 chunks a thread exist only as exact kernels without a quantised output
+    if ((nch == 5 || nch == 6) && (C != 32LL * nch * G || c.quant)) staged = false;
     // 10 chunks a thread exist only as exact kernels of the packed no-residual variant
     if (nch == 10 && (C != 320LL * G || !packed)) staged = false;
     if (staged) {

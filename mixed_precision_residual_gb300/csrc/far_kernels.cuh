@@ -712,16 +712,17 @@ cudaError_t launch_typed(const Launch& L) {
       case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q, LN>; break;
       case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q, LN>; break;
       // 5 or 6 chunks a thread, only where they cover a row exactly (hidden 5120 or 2560 in
-      // 16-bit with 4 or 2 warps a row, 3072 with 2): plain RMSNorm only
+      // 16-bit with 4 or 2 warps a row, 3072 with 2): RMSNorm and LayerNorm, no quantised
+      // output
       case 11:
-        if constexpr (Q == kQuantNone && !LN) {
+        if constexpr (Q == kQuantNone) {
           k = staged_kernel<ACT, WD, RES, 5, true, Q, LN>;
           break;
         } else {
           return cudaErrorInvalidValue;
         }
       case 13:
-        if constexpr (Q == kQuantNone && !LN) {
+        if constexpr (Q == kQuantNone) {
           k = staged_kernel<ACT, WD, RES, 6, true, Q, LN>;
           break;
         } else {

@@ -88,11 +88,12 @@ def test_dtype_pairs(far, act, wd, hidden):
 
 
 @pytest.mark.parametrize("act,wd", [("bf16", "bf16"), ("f16", "f32"), ("f32", "f32")])
-@pytest.mark.parametrize("hidden", [256, 768, 1024, 3000, 6144, 10240])
+@pytest.mark.parametrize("hidden", [256, 768, 1024, 2560, 3000, 3072, 5120, 6144, 10240])
 @pytest.mark.parametrize("tokens", [600, 2500])
 def test_default_plans_across_widths(far, act, wd, hidden, tokens):
-    """The default plans (short one-warp rows in 7 groups, 8 chunks a thread above)
-    at 4 and 17 rows an SM."""
+    """The default plans (short one-warp rows in 7 groups, 8 chunks a thread above, the
+    variant's exact 5 or 6 chunks on 16-bit rows of 2560, 3072 and 5120) at 4 and 17 rows
+    an SM."""
     d = with_beta(far_gen.custom_inputs(act, wd, tokens, hidden, seed=hidden + tokens))
     check_ln(far, d, f"{act}/{wd} {tokens}x{hidden}")
 
