@@ -586,6 +586,10 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
                                       : 70 * 1024 + (rows_per_sm <= 32 ? slot : 0);
       const int64_t want = (target + slot / 2) / slot;
       group_cap = (int)(want < 1 ? 1 : want);
+      // rows of 4+ warps at up to 4 rows an SM: 2 groups (fp16 512 x 8192: 7.7 us against
+      // 8.1 for 3 in a stream, 12.3 against 12.8 after an L2 flush; rows of 2 warps were
+      // slower so, bf16 600 x 4096)
+      if (rows_per_sm <= 4 && G >= 4 && group_cap > 2) group_cap = 2;
       slots_per_group = 1;
     } else if (packed && c.od != FAR_F32) {
       // the no-residual variant on 16-bit rows (x kept packed), from a sweep of every plan

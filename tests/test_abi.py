@@ -494,7 +494,7 @@ def test_plans_of_the_bench_workloads(far):
     keys = ("kind", "nch", "warps_per_row", "groups", "stages", "grid")
     want = {
         ("c1", True): [0, 1, 8, 1, 4, 8], ("c1", False): [0, 1, 8, 1, 4, 8],
-        ("c2", True): [0, 8, 4, 3, 3, 152], ("c2", False): [0, 8, 4, 4, 4, 128],
+        ("c2", True): [0, 8, 4, 2, 2, 152], ("c2", False): [0, 8, 4, 4, 4, 128],
         ("c3", True): [0, 8, 2, 3, 3, 152], ("c3", False): [0, 8, 2, 5, 10, 152],
         ("c4", True): [0, 5, 4, 3, 3, 152], ("c4", False): [0, 10, 2, 5, 10, 152],
         ("c5", True): [0, 8, 4, 2, 2, 152], ("c5", False): [0, 8, 4, 4, 4, 152],
