@@ -401,8 +401,12 @@ int far_get_row_schedule(void);
  * touches any global memory, and it allows the next programmatic launch on the stream to
  * be dispatched as soon as it starts.  Stream order therefore holds as for a plain launch;
  * a stream of launches (this library's, or a caller's kernels launched the same way and
- * waiting the same way) loses less time between kernels.  0: plain launches.  The results
- * are the same bits either way.  Returns FAR_ERR_SHAPE for another value.
+ * waiting the same way) loses less time between kernels.  A caller's kernel launched on
+ * the same stream with the programmatic-stream-serialization attribute right after one of
+ * these may start before it finishes: it must wait (griddepcontrol.wait, or
+ * cudaGridDependencySynchronize) before it reads their outputs, as with any programmatic
+ * launch; kernels launched without the attribute are ordered as usual.  0: plain launches.
+ * The results are the same bits either way.  Returns FAR_ERR_SHAPE for another value.
  */
 int far_set_programmatic_launch(int enable);
 /* the current choice of far_set_programmatic_launch */
