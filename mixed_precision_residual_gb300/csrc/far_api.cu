@@ -530,8 +530,14 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       // op on rows of 2+ warps at 8 chunks keeps to 8 warps: with 12 it is 5-10 % faster
       // after an L2 flush but 3-10 % slower when the previous launch's output is still
       // being written back (back-to-back launches, as in the bench)
+      // (5 chunks where 8 do not cover the row exactly but 5 do: hidden 2560 and 5120 in
+      // 16-bit run 5 chunks on 2 or 4 warps instead of 4 on 3 or 5; measured in a stream,
+      // bf16 16384 x 5120 int8 variant 73.1 us against 83.9, E4M3 71.8 against 85.4, fused
+      // 92.3 / 88.8 against 93.8 / 92.8; fp16 32768 x 2560 int8 variant 70.0 against 85.0,
+      // fused 88.9 against 102.3)
       if (C > 128) {
         nch = (C % 256 == 0 && C / 256 <= 12 && C / 256 != 3) ? 8 : 4;
+        if (nch == 4 && C % 160 == 0 && C / 160 <= 12) nch = 5;
         G = (int)((C + 32LL * nch - 1) / (32LL * nch));
         if (G > kMaxConsumerWarps) {
           nch = 8;
@@ -668,8 +674,8 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
       one_group = false;
     }
     staged = G <= max_consumer_warps(nch, packed);
-    // 5 or 6 chunks a thread exist only as exact kernels without a quantised output
-    if ((nch == 5 || nch == 6) && (C != 32LL * nch * G || c.quant)) staged = false;
+    // 5 or 6 chunks a thread exist only as exact kernels (6 without a quantised output)
+    if ((nch == 5 || nch == 6) && (C != 32LL * nch * G || (c.quant && nch == 6))) staged = false;
     // 10 chunks a thread exist only as exact kernels of the packed no-residual variant
     if (nch == 10 && (C != 320LL * G || !packed)) staged = false;
     if (staged) {

@@ -712,10 +712,10 @@ cudaError_t launch_typed(const Launch& L) {
       case 16: k = staged_kernel<ACT, WD, RES, 8, false, Q, LN>; break;
       case 17: k = staged_kernel<ACT, WD, RES, 8, true, Q, LN>; break;
       // 5 or 6 chunks a thread, only where they cover a row exactly (hidden 5120 or 2560 in
-      // 16-bit with 4 or 2 warps a row, 3072 with 2): RMSNorm and LayerNorm, no quantised
-      // output
+      // 16-bit with 4 or 2 warps a row, 3072 with 2): RMSNorm and LayerNorm; 5 chunks also
+      // with a quantised output
       case 11:
-        if constexpr (Q == kQuantNone) {
+        if constexpr (true) {
           k = staged_kernel<ACT, WD, RES, 5, true, Q, LN>;
           break;
         } else {
