@@ -365,7 +365,10 @@ int far_plan_ln_for_sms(int64_t tokens, int64_t hidden, int dtype, int has_resid
  *   mode 1 (the default): the fixed stride always.  No state is kept between calls.
  *   mode 0: claimed rows where a claim takes one or two rows, the rows left after the
  *           first ring-full of every CTA are at least three times as many, the stream is
- *           not capturing a graph and a counter is free; else the fixed stride.
+ *           not capturing a graph and a counter is free; also three rows a claim for the
+ *           no-residual RMSNorm (16-bit out) and quantised kernels on 16-bit rows that
+ *           are not a whole number of 256 16-byte chunks, with at least eight ring-fulls
+ *           of rows; else the fixed stride.
  *   mode 2: claimed rows whenever there are rows left to claim (and a counter is free,
  *           and the stream is not capturing).
  * State of modes 0 and 2: the counters are a library-owned device array of 64 pairs a

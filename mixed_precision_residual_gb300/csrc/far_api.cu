@@ -750,6 +750,15 @@ int plan(const Call& c, int sms, unsigned int* status, cudaStream_t stream, Laun
 // launches of fewer ring-fulls the claims' round trips delay the loads more than the
 // balance gains (bf16 / fp32-weight 4096 x 4096 variant, 2.7 ring-fulls a CTA: 19.7 us
 // against 18.0 at the fixed stride); forced, wherever rows are left.
+// Also three rows a claim for the packed no-residual kernels on 16-bit rows (RMSNorm with a
+// 16-bit out, or a quantised out) with at least eight ring-fulls of rows and a row that is
+// not a whole number of 256 chunks: there the fixed stride loses 7-16 % when the launch
+// follows another on the stream (dirty lines of the one ahead written back meanwhile)
+// and claims cost at most ~1.5 % after an L2 flush (bf16 16384 x 5120: 53.3 us against 59.9
+// in a stream, 53.7 against 52.9 after a flush; 32768 x 4608 90.9 against 105.8 and 94.2
+// against 94.7; fp16 24576 x 5120 76.7 against 88.2 and 76.1 against 80.5; int8 out within
+// -0.1 / +2.6 % either way). Rows of whole 256-chunk multiples keep the stride (hidden
+// 4096: claims 2.8 % slower in a stream, 10 % after a flush).
 int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
   if (L.kind != kStaged || c.fixed_stride || mode == 1) return 0;
   // bytes a row moves: x (and the residual and residual_out), then out, or the quantised
@@ -759,9 +768,27 @@ int64_t claim_rows_for(const Call& c, const Launch& L, int mode) {
                               (c.quant ? 4 : 0);
   const int64_t claim_rows = (45333 + row_traffic - 1) / row_traffic;
   const int64_t r0 = (int64_t)L.grid.x * L.p.stages;
-  if (mode == 2 ? c.tokens > r0 : (claim_rows <= 2 && c.tokens >= 4 * r0))
+  const bool packed16 = !c.residual && !c.ln && c.act != FAR_F32 && (c.quant || c.od != FAR_F32);
+  const int64_t chunks = c.hidden * dsize(c.act) / 16;
+  if (mode == 2 ? c.tokens > r0
+                : ((claim_rows <= 2 && c.tokens >= 4 * r0) ||
+                   (packed16 && claim_rows == 3 && c.tokens >= 8 * r0 && chunks % 256 != 0)))
     return claim_rows < (1 << 20) ? claim_rows : (1 << 20);
   return 0;
+}
+
+// Rows a CTA takes at the fixed stride before it claims (with claimed rows): its first
+// ring-full, except for the automatic rule's three-row claims of the packed kernels, which
+// claim only the last quarter of a CTA's share. bf16 16384 x 5120, after an L2 flush / in a
+// stream: 52.8 / 54.2 us against 53.4 / 54.2 claiming from the first ring-full and 53.4 /
+// 59.7 at the fixed stride. (Claims from the first ring-full stay best where they take one
+// or two rows: fp16 65536 x 8192 variant 303 us against 307 with the last quarter claimed.)
+int64_t static_rows_for(const Call& c, const Launch& L, int mode) {
+  const int64_t ring = L.p.stages;
+  if (mode != 0 || claim_rows_for(c, L, mode) != 3) return ring;
+  const int64_t per = c.tokens / (int64_t)L.grid.x;
+  const int64_t s = per - (per + 3) / 4;
+  return s > ring ? (s < (1 << 30) ? s : (1 << 30)) : ring;
 }
 
 int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
@@ -770,7 +797,8 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
   Launch L;
   int st = plan(c, dev.sms, dev.status, stream, L);
   if (st != FAR_OK) return st;
-  const int64_t claim_rows = claim_rows_for(c, L, g_row_schedule.load());
+  const int mode = g_row_schedule.load();
+  const int64_t claim_rows = claim_rows_for(c, L, mode);
   int pair = -1;
   const int devno = (int)(&dev - g_dev);
   if (claim_rows > 0) {
@@ -783,6 +811,7 @@ int launch(const Call& c, const DeviceState& dev, cudaStream_t stream) {
     if (pair >= 0) {
       L.p.sched = g_sched_pool[devno].pairs + 2 * pair;
       L.p.sched_run = (int32_t)claim_rows;
+      L.p.sched_static = (int32_t)static_rows_for(c, L, mode);
     }
   }
   cudaError_t e;

@@ -359,6 +359,32 @@ __device__ __forceinline__ void dw2_add_nonneg(DW2& acc, uint64_t v) {
   acc.lo = add_x2(acc.lo, sub_x2(small, sub_x2(s, big)));
 }
 
+// Sums of non-negative terms whose largest term is known before the first addition: each
+// chain starts at B, the largest power of two not above that term (its exponent, the
+// mantissa cleared; 0 for a subnormal term), and only grows.  So a chain's exponent is
+// never below a term's, and Dekker's Fast2Sum -- s = a + b, t = b - (s - a) -- is exact
+// without ordering the operands (its condition is e_a >= e_b): three packed operations and
+// the low-part add a pair, nothing on the integer pipe.  At the end hi - B is exact (hi and
+// B are multiples of ulp(hi) while hi < 2^24 B, i.e. fewer than 2^22 terms a chain), and
+// (hi - B) + lo is the chain's sum as a double word.  Each rounding error carried in lo is
+// relative to B + the chain's sum, where B is at most the largest term of the whole sum:
+// the row's double word stays within a few units of 2^-44 (relative) of the exact sum.
+__device__ __forceinline__ float pow2_floor(float q) {
+  return __uint_as_float(__float_as_uint(q) & 0x7f800000u);  // NaN -> +inf, inf stays
+}
+__device__ __forceinline__ void dwb_add(DW2& acc, uint64_t v) {
+  const uint64_t s = add_x2(acc.hi, v);
+  acc.lo = add_x2(acc.lo, sub_x2(v, sub_x2(s, acc.hi)));
+  acc.hi = s;
+}
+// the two chains of an offset DW2 as double words, B taken off: exact.  B infinite (an
+// infinite or NaN term, so the chains are infinite or NaN): hi stands
+__device__ __forceinline__ void dwb_split(DW2 a, float B, DW& c0, DW& c1) {
+  const float2 h = unpk(isfinite(B) ? sub_x2(a.hi, pk(B, B)) : a.hi), l = unpk(a.lo);
+  c0 = DW{h.x, l.x};
+  c1 = DW{h.y, l.y};
+}
+
 // the two chains of a DW2 folded into one double word
 __device__ __forceinline__ DW dw2_fold(DW2 a) {
   const float2 h = unpk(a.hi), l = unpk(a.lo);

@@ -106,14 +106,14 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     return;
   }
   // Rows enter the ring in this order: first the CTA's fixed-stride rows b + k * nb (all of
-  // them; or, with a row counter, only those with k < stages), then runs of n rows R0 + c ..
-  // R0 + c + n - 1, R0 = nb * stages, n = sched_run, each claimed by one atomic add of n to
-  // the launch's counter (which returns c), until the claims pass the last row. The CTAs
-  // that are served faster take more rows, all finish within a run of each other, and at
-  // any time they all work in one window of neighbouring rows.
+  // them; or, with a row counter, only those with k < S, S = sched_static), then runs of n
+  // rows R0 + c .. R0 + c + n - 1, R0 = nb * S, n = sched_run, each claimed by one atomic add
+  // of n to the launch's counter (which returns c), until the claims pass the last row. The
+  // CTAs that are served faster take more rows, all finish within a run of each other, and
+  // while they claim they all work in one window of neighbouring rows.
   const int64_t b = blockIdx.x, nb = gridDim.x;
   int64_t n_static = (p.tokens > b) ? (p.tokens - b + nb - 1) / nb : 0;
-  if (p.sched != nullptr && n_static > stages) n_static = stages;
+  if (p.sched != nullptr && n_static > p.sched_static) n_static = p.sched_static;
   const uint32_t tx = RES ? 2u * p.row_bytes : p.row_bytes;
   const int64_t first = n_static < stages ? n_static : stages;  // rows issued before the consumers start
 
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       bool ok = true;
       for (int64_t i = first; ok && i < n_static; ++i) ok = put(b + i * nb);
       if (p.sched != nullptr) {
-        const int64_t R0 = nb * stages;
+        const int64_t R0 = nb * (int64_t)p.sched_static;
         const unsigned long long n = p.sched_run > 1 ? (unsigned long long)p.sched_run : 1ull;
         // the next run is claimed while this one is issued (its atomic's latency hidden); a
         // thread's adds to one address are ordered, so every run after a spent one is spent
@@ -296,53 +296,89 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
     uint32_t xk[PACKED ? NCH : 1][PACKED ? V / 2 : 1];  // the packed x of the no-residual variant
     DW acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};  // four independent chains
     DW2 accp[2] = {{0ull, 0ull}, {0ull, 0ull}};  // LayerNorm: four chains in packed pairs
+    if constexpr (PACKED) {
+      // s = x exactly, kept packed.  The first sweep brings the thread's chunks into
+      // registers with their largest magnitude M; the second sums the squares in chains
+      // that start at the largest square's power of two (Fast2Sum exact without ordering)
+      uint32_t m2 = 0u;  // packed running max of |x|
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const Where w = where(j);
-      if constexpr (PACKED) {
+      for (int j = 0; j < NCH; ++j) {
+        const Where w = where(j);
+        if (w.va) {
+          load_act(xs, w, xk[j]);
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e) m2 = habs_max2<ACT>(m2, xk[j][e]);
+        }
+      }
+      const float2 mq = square2_mixed<ACT>(m2);  // fl32(M * M), the largest square
+      const float B = pow2_floor(max_nan(mq.x, mq.y));
+      DW2 sq[2] = {{pk(B, B), 0ull}, {pk(B, B), 0ull}};
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        if (where(j).va) {
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e) {
+            const float2 q = square2_mixed<ACT>(xk[j][e]);
+            dwb_add(sq[e & 1], pk(q.x, q.y));
+          }
+        }
+      }
+      dwb_split(sq[0], B, acc[0], acc[1]);
+      dwb_split(sq[1], B, acc[2], acc[3]);
+    } else {
+      float smax = 0.f;  // RMSNorm: the largest |s| of the thread's chunks (NaN-propagating)
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const Where w = where(j);
         if (w.va) {
           uint32_t xw[4];
           load_act(xs, w, xw);
+          if constexpr (RES) {
+            uint32_t rv[4];
+            load_act(xs + r_off, w, rv);
+            float rf[V];
+            widen<ACT, V>(rv, rf);
+            if constexpr (ACT == FAR_F32) {
 #pragma unroll
-          for (int e = 0; e < V / 2; ++e) {
-            xk[j][e] = xw[e];
-            const float2 q = square2_mixed<ACT>(xw[e]);
-            dw_add(acc[(2 * e) & 3], q.x);
-            dw_add(acc[(2 * e + 1) & 3], q.y);
+              for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(__uint_as_float(xw[e]), rf[e]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < V / 2; ++e) {
+                const float2 t = add2_mixed<ACT>(xw[e], rf[2 * e], rf[2 * e + 1]);
+                s[j][2 * e] = t.x;
+                s[j][2 * e + 1] = t.y;
+              }
+            }
+          } else {
+            widen<ACT, V>(xw, s[j]);
           }
-        }
-      } else if (w.va) {
-        uint32_t xw[4];
-        load_act(xs, w, xw);
-        if constexpr (RES) {
-          uint32_t rv[4];
-          load_act(xs + r_off, w, rv);
-          float rf[V];
-          widen<ACT, V>(rv, rf);
-          if constexpr (ACT == FAR_F32) {
+          if constexpr (LN) {
 #pragma unroll
-            for (int e = 0; e < V; ++e) s[j][e] = __fadd_rn(__uint_as_float(xw[e]), rf[e]);
+            for (int e = 0; e < V / 2; ++e) dw2_add_ordered(accp[e & 1], s[j][2 * e], s[j][2 * e + 1]);  // for the mean
           } else {
 #pragma unroll
-            for (int e = 0; e < V / 2; ++e) {
-              const float2 t = add2_mixed<ACT>(xw[e], rf[2 * e], rf[2 * e + 1]);
-              s[j][2 * e] = t.x;
-              s[j][2 * e + 1] = t.y;
-            }
+            for (int e = 0; e < V; ++e) smax = max_nan(smax, fabsf(s[j][e]));
           }
         } else {
-          widen<ACT, V>(xw, s[j]);
+#pragma unroll
+          for (int e = 0; e < V; ++e) s[j][e] = 0.f;
         }
-        if constexpr (LN) {
+      }
+      if constexpr (!LN) {
+        // the squares fl32(s * s) (scalar mul.rn: never fused into the adds) in chains that
+        // start at the largest square's power of two, as in the packed variant
+        const float B = pow2_floor(__fmul_rn(smax, smax));
+        DW2 sq[2] = {{pk(B, B), 0ull}, {pk(B, B), 0ull}};
 #pragma unroll
-          for (int e = 0; e < V / 2; ++e) dw2_add_ordered(accp[e & 1], s[j][2 * e], s[j][2 * e + 1]);  // for the mean
-        } else {
+        for (int j = 0; j < NCH; ++j) {
+          if (where(j).va) {
 #pragma unroll
-          for (int e = 0; e < V; ++e) dw_add(acc[e & 3], __fmul_rn(s[j][e], s[j][e]));
+            for (int e = 0; e < V / 2; ++e)
+              dwb_add(sq[e & 1], pk(__fmul_rn(s[j][2 * e], s[j][2 * e]), __fmul_rn(s[j][2 * e + 1], s[j][2 * e + 1])));
+          }
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < V; ++e) s[j][e] = 0.f;
+        dwb_split(sq[0], B, acc[0], acc[1]);
+        dwb_split(sq[1], B, acc[2], acc[3]);
       }
     }
     __syncwarp();

@@ -60,6 +60,7 @@ struct Params {
   // launch and left zero by the launch's last CTA; null: every CTA takes a fixed stride
   unsigned long long* sched;
   int32_t sched_run;     // rows taken per claim from sched (>= 1)
+  int32_t sched_static;  // with sched: rows a CTA takes at the fixed stride before it claims
 };
 
 enum Kind { kStaged = 0, kGeneric = 1 };

@@ -130,7 +130,9 @@ def test_row_schedule_rule(far):
     """The default keeps the fixed stride everywhere. The automatic claimed-row rule (mode 0,
     host logic): one row a claim where a row moves 45 KB or more, two down to 23 KB, the
     fixed stride on shorter rows and on launches with fewer than four ring-fulls of rows a
-    CTA; mode 2 claims wherever rows are left."""
+    CTA; three rows a claim (15-22 KB) only for the packed no-residual kernels on 16-bit
+    rows (16-bit or quantised out) with eight ring-fulls or more and a row that is not a
+    whole number of 256 chunks; mode 2 claims wherever rows are left."""
     f16, bf16, f32 = torch.float16, torch.bfloat16, torch.float32
 
     def rows(tokens, hidden, act, wd, residual, op, sms=152):
@@ -145,7 +147,14 @@ def test_row_schedule_rule(far):
         assert rows(65536, 8192, f16, f16, True, op) == 1      # 64 KB (56 KB quantised) a row
         assert rows(65536, 8192, f16, f16, False, op) == 2     # 32 KB (24 KB)
     assert rows(16384, 5120, bf16, bf16, True, "rmsnorm") == 2   # 40 KB
-    assert rows(16384, 5120, bf16, bf16, False, "rmsnorm") == 0  # 20 KB: fixed stride
+    assert rows(16384, 5120, bf16, bf16, False, "rmsnorm") == 3  # 20 KB, packed: 3 a claim
+    assert rows(16384, 5120, bf16, bf16, False, "quant") == 3    # 15.4 KB
+    assert rows(32768, 4608, bf16, bf16, False, "rmsnorm") == 3  # 18 KB, 576 chunks
+    assert rows(16384, 4096, f16, f16, False, "rmsnorm") == 0    # 16 KB, 512 chunks: stride
+    assert rows(8192, 5120, f16, f16, False, "rmsnorm") == 0     # 5.4 ring-fulls a CTA
+    assert rows(16384, 5120, bf16, bf16, False, "layernorm") == 0  # LayerNorm keeps the stride
+    assert rows(32768, 2048, f16, f16, True, "rmsnorm") == 0     # 16 KB fused: stride
+    assert rows(16384, 3072, bf16, f32, False, "rmsnorm") == 0   # binary32 out: stride
     assert rows(4096, 4096, bf16, f32, True, "rmsnorm") == 2     # 40 KB
     assert rows(65536, 1024, bf16, bf16, True, "rmsnorm") == 0   # 8 KB
     for tokens, hidden, dt in ((512, 8192, f16), (512, 5120, bf16), (8, 2048, bf16)):

@@ -333,6 +333,67 @@ def test_strided_in_place(far):
     gate(xbig[:, :H].cpu(), ref_out, rbig[:, :H].cpu(), ref_res, "strided in place")
 
 
+def _tiny_square_rows(T, H, seed):
+    """bf16 rows whose squares fall in binary32's subnormal range and are rounded there:
+    x = +-m/128 * 2^-68 with m odd in 129..255 (m and the signs drawn from the seeded
+    generator), so x^2 = m^2 * 2^-150 lies halfway between two subnormals and, m^2/2 being
+    4j + 1/2, rounds down to the even one: every square loses 2^-150, and a row of
+    thousands loses enough to move var = S / hidden by about half its last place.  Every
+    third row carries one element 2^8 larger (a normal square that dominates its thread's
+    chain)."""
+    import numpy as np
+
+    d = far_gen.custom_inputs("bf16", "f32", T, H, seed=seed, eps=0.0)
+    u = d["x"].double().numpy()
+    m = 129.0 + 2.0 * (np.floor(np.abs(u) * 1000.0) % 64)
+    x = np.sign(u) * m / 128.0 * 2.0 ** -68
+    x[::3, 7] *= 2.0 ** 8
+    return d, torch.from_numpy(x.astype(np.float32))
+
+
+@pytest.mark.parametrize("wd", ["f32", "bf16"])
+@pytest.mark.parametrize("hidden", [5120, 4096, 1000])
+def test_subnormal_squares_of_16_bit_rows(far, hidden, wd):
+    """The no-residual kernel keeps 16-bit x packed and sums its squares in chains that
+    start at the largest square's power of two; the fused kernel (residual 0) sums
+    fl32(s * s) in ordered chains.  On rows whose rounded squares (binary32 subnormals)
+    give another rstd than their exact squares would, both must still match the oracle
+    (with a binary32 out every element shows a change of rstd), on several plans."""
+    import math
+
+    import numpy as np
+
+    import oracle
+
+    d, x = _tiny_square_rows(1200, hidden, seed=hidden + 3)
+    xb = x.to(torch.bfloat16)
+    assert torch.equal(xb.float(), x)  # every value is a bf16
+    H = np.float32(hidden)
+
+    def rstd(S):
+        return np.float32(1.0) / np.sqrt(np.float32(S / H))
+
+    xf = x.numpy()
+    keep = []
+    for i, row in enumerate(xf):
+        S_rounded = np.float32(oracle.exact_sum((row * row).astype(np.float32)))
+        S_exact = np.float32(math.fsum(float(v) * float(v) for v in row.astype(np.float64)))
+        keep.append(rstd(S_rounded) != rstd(S_exact))
+    rows = np.nonzero(keep)[0]
+    assert len(rows) >= 100 and (rows % 3 == 0).sum() >= 20, len(rows)
+    w = d["w"] if wd == "f32" else d["w"].to(torch.bfloat16)
+    sel = dict(d, x=xb[rows].contiguous(), r=torch.zeros_like(xb[rows]), w=w, wd=wd, tokens=len(rows))
+    try:
+        for plan in [(-1, 0, 0, 0), (0, 2, 0, 0), (0, 8, 0, 0), (1, 0, 0, 0)]:
+            far.set_launch_override(*plan)
+            gate(far_norm(far, sel), oracle_norm(sel), where=f"subnormal squares rmsnorm {plan}")
+            out, res = far_fused(far, sel)
+            ref_out, ref_res = oracle_fused(sel)
+            gate(out, ref_out, res, ref_res, where=f"subnormal squares fused {plan}")
+    finally:
+        far.set_launch_override()
+
+
 def test_rounded_squares_are_summed(far):
     """The sum of squares adds fl32(s * s), each square rounded, not the exact squares
     (as a fused multiply-add would): rows where the two sums round to different binary32

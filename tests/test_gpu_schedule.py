@@ -123,8 +123,9 @@ def test_claimed_rows_against_the_oracle(far):
 def test_default_schedule(far):
     """The default keeps the fixed stride (no state between calls). The automatic rule
     (mode 0) claims rows for the fused op at 16384 x 5120 bf16 (40 KB moved a row, two rows
-    a claim, over 2 ring-fulls a CTA) and keeps the fixed stride for its no-residual variant
-    (20 KB a row: three rows a claim) and for the fused op at 512 rows."""
+    a claim, over 2 ring-fulls a CTA) and for its packed no-residual variant (20 KB a row,
+    three a claim, 640 chunks), keeps the fixed stride for LayerNorm's variant on the same
+    rows, for the variant at 16384 x 4096 (512 chunks) and for the fused op at 512 rows."""
     assert far.get_row_schedule() == 1
     _, t = _inputs("bf16", "bf16", 16384, 5120, seed=3)
     for op in ("rms_fused", "rms", "ln_fused", "q_fused"):
@@ -135,6 +136,11 @@ def test_default_schedule(far):
         _run(far, "rms_fused", t)
         assert far.last_launch_claimed_rows()
         _run(far, "rms", t)
+        assert far.last_launch_claimed_rows()
+        _run(far, "ln", t)
+        assert not far.last_launch_claimed_rows()
+        _, t4 = _inputs("bf16", "bf16", 16384, 4096, seed=5)
+        _run(far, "rms", t4)
         assert not far.last_launch_claimed_rows()
         _, t = _inputs("bf16", "bf16", 512, 5120, seed=4)
         _run(far, "rms_fused", t)

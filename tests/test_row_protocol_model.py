@@ -3,7 +3,8 @@
 The kernel's producer (one thread a CTA) and its consumer groups share a ring of
 `stages` shared-memory slots through two mbarriers a slot (full: the producer's arrive
 plus the bytes of the row's copies; empty: the group's release). Rows enter the ring at
-a fixed stride, then, with a row counter, in runs of `run` rows claimed by atomic adds;
+a fixed stride (with a row counter, only each CTA's first `static` rows: a ring-full or
+more), then in runs of `run` rows claimed by atomic adds;
 after the last row each group gets an end marker (row -1), and the last CTA to finish
 claiming zeroes the counter pair. This file restates those steps as coroutines, with
 the mbarrier's phase / parity rule (a wait on parity P returns once the phase of parity
@@ -50,7 +51,8 @@ class Deadlock(Exception):
     pass
 
 
-def simulate(tokens, grid, stages, groups, claimed, run, residual, rng, mutant=None):
+def simulate(tokens, grid, stages, groups, claimed, run, residual, rng, mutant=None, static=None):
+    static = stages if static is None else static
     counter = [0, 0]  # next claim, CTAs done
     processed = []
     landing = []      # barriers with a copy in flight, one entry per copy
@@ -61,8 +63,8 @@ def simulate(tokens, grid, stages, groups, claimed, run, residual, rng, mutant=N
         empty = [Bar(1) for _ in range(stages)]  # one arrival a group (the kernel: one a warp)
         slot_row = [None] * stages
         n_static = (tokens - b + grid - 1) // grid if tokens > b else 0
-        if claimed and n_static > stages:
-            n_static = stages
+        if claimed and n_static > static:
+            n_static = static
         first = min(n_static, stages)
         copies = 2 if residual else 1
 
@@ -94,7 +96,7 @@ def simulate(tokens, grid, stages, groups, claimed, run, residual, rng, mutant=N
             for i in range(first, n_static):
                 yield from put(b + i * grid)
             if claimed:
-                r0 = grid * stages
+                r0 = grid * (stages if mutant == "r0_from_stages" else static)
                 c0 = counter[0]
                 counter[0] += run
                 yield None
@@ -181,6 +183,27 @@ def test_every_row_once_no_deadlock_counter_zero(tokens, grid, stages, groups, c
     assert counter == [0, 0]
 
 
+def static_shapes(n, seed):
+    rng = random.Random(seed)
+    for _ in range(n):
+        stages = rng.choice([2, 4, 6, 10])
+        groups = rng.choice([g for g in range(1, stages + 1) if stages % g == 0])
+        tokens, grid = rng.randint(1, 160), rng.randint(1, 5)
+        per = tokens // grid
+        yield (tokens, grid, stages, groups, rng.choice([1, 2, 3]), rng.random() < 0.5,
+               max(stages, per - (per + 3) // 4) + rng.choice([0, 0, 1, 5]), rng.randrange(1 << 30))
+
+
+@pytest.mark.parametrize("tokens,grid,stages,groups,run,residual,static,seed", list(static_shapes(80, 77)))
+def test_claims_after_a_longer_fixed_stride(tokens, grid, stages, groups, run, residual, static, seed):
+    """Each CTA's first `static` rows at the fixed stride (a ring-full or more; up to its
+    whole share), then claimed runs from row grid * static."""
+    processed, counter = simulate(tokens, grid, stages, groups, True, run, residual, random.Random(seed),
+                                  static=static)
+    assert sorted(processed) == list(range(tokens))
+    assert counter == [0, 0]
+
+
 @pytest.mark.parametrize("seed", range(12))
 def test_many_interleavings_of_one_shape(seed):
     """Claims crossing the last row, more groups than rows per CTA, two copies a row."""
@@ -191,6 +214,9 @@ def test_many_interleavings_of_one_shape(seed):
 
 def test_planted_mistakes_are_caught():
     rng = random.Random(5)
+    # claims counted from the first ring-full while the fixed stride ran longer: rows twice
+    processed, _ = simulate(120, 3, 4, 2, True, 3, False, rng, mutant="r0_from_stages", static=30)
+    assert sorted(processed) != list(range(120))
     # one end marker short: a group waits forever
     with pytest.raises(Deadlock):
         simulate(40, 3, 4, 2, True, 2, False, rng, mutant="one_marker_short")
