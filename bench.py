@@ -202,7 +202,9 @@ def row_schedule_text(far, claimed, tokens, hidden, act, wd, residual, op, sms):
         return "fixed stride"
     n = far.row_schedule_for_sms(tokens, hidden, act, wd, residual,
                                  {"rmsnorm": "rmsnorm", "layernorm": "layernorm"}.get(op, "quant"), sms)
-    return f"rows claimed from a per-launch counter, {n} a claim"
+    # the automatic rule's three-row claims cover only the last quarter of each CTA's rows
+    tail = ", over the last quarter of each CTA's rows" if n == 3 and far.get_row_schedule() == 0 else ""
+    return f"rows claimed from a per-launch counter, {n} a claim{tail}"
 
 
 class ClockSampler:
