@@ -104,6 +104,32 @@ def test_claimed_rows_give_the_fixed_stride_bits(far, op, act, wd, tokens, hidde
     assert not any(torch.isnan(o).any() for o in ref if o.is_floating_point()), "a row was left unwritten"
 
 
+@pytest.mark.parametrize("op,act,tokens,hidden", [("rms", "bf16", 16384, 5120), ("rms", "bf16", 32768, 4608),
+                                                  ("rms", "f16", 24576, 5120), ("q", "bf16", 16384, 5120),
+                                                  ("q", "f16", 24576, 5120)])
+def test_claims_over_the_last_quarter_give_the_fixed_stride_bits(far, op, act, tokens, hidden):
+    """The automatic rule's three-row claims (packed no-residual kernels): each CTA takes the
+    first three quarters of its rows at the fixed stride, then claims; back to back, each
+    launch finds its counter zero, every row is written, and the bits are the fixed stride's."""
+    d, t = _inputs(act, act, tokens, hidden, seed=tokens + hidden + 1)
+    try:
+        far.set_row_schedule(1)
+        ref = _run(far, op, t)
+        assert not far.last_launch_claimed_rows()
+        far.set_row_schedule(0)
+        assert far.row_schedule_for_sms(tokens, hidden, t["x"].dtype, t["w"].dtype, False,
+                                        "rmsnorm" if op == "rms" else "quant",
+                                        torch.cuda.get_device_properties(0).multi_processor_count) == 3
+        for i in range(3):
+            got = _run(far, op, t)
+            assert far.last_launch_claimed_rows(), f"{op}: launch {i} did not claim rows"
+            assert far.device_status() == 0
+            assert _same(got, ref), f"{op} {act} {tokens}x{hidden}: launch {i} differs"
+    finally:
+        far.set_row_schedule(1)
+    assert not any(torch.isnan(o).any() for o in ref if o.is_floating_point()), "a row was left unwritten"
+
+
 def test_claimed_rows_against_the_oracle(far):
     """The fused op and the variant at many rows a CTA, claimed rows, against the oracle."""
     d, t = _inputs("bf16", "bf16", 6000, 2048, seed=77)
