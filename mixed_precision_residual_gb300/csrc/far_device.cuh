@@ -347,17 +347,6 @@ __device__ __forceinline__ void dw2_add_ordered(DW2& acc, float v0, float v1) {
   acc.hi = s;
   acc.lo = add_x2(acc.lo, sub_x2(small, sub_x2(s, big)));
 }
-// ... and for non-negative values, ordered by a NaN-propagating max / min pair; the
-// values enter through the max / min, so no multiply that formed them can be fused
-// into the add
-__device__ __forceinline__ void dw2_add_nonneg(DW2& acc, uint64_t v) {
-  const float2 h = unpk(acc.hi), q = unpk(v);
-  const uint64_t big = pk(max_nan(h.x, q.x), max_nan(h.y, q.y));
-  const uint64_t small = pk(min_nan(h.x, q.x), min_nan(h.y, q.y));
-  const uint64_t s = add_x2(big, small);
-  acc.hi = s;
-  acc.lo = add_x2(acc.lo, sub_x2(small, sub_x2(s, big)));
-}
 
 // Sums of non-negative terms whose largest term is known before the first addition: each
 // chain starts at B, the largest power of two not above that term (its exponent, the

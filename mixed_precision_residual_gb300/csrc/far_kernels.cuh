@@ -354,7 +354,14 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
           }
           if constexpr (LN) {
 #pragma unroll
-            for (int e = 0; e < V / 2; ++e) dw2_add_ordered(accp[e & 1], s[j][2 * e], s[j][2 * e + 1]);  // for the mean
+            for (int e = 0; e < V / 2; ++e) {
+              // for the mean, exact for any signs: one packed chain by the ordered Fast2Sum
+              // (a compare and two selects on the integer pipe), the other by TwoSum (on the
+              // FMA pipe), which keeps both pipes busy (LayerNorm variant bf16 16384 x 5120:
+              // 84.0 against 85.5 us with every pair ordered)
+              if (e & 1) dw2_add(accp[1], pk(s[j][2 * e], s[j][2 * e + 1]));
+              else dw2_add_ordered(accp[0], s[j][2 * e], s[j][2 * e + 1]);
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < V; ++e) smax = max_nan(smax, fabsf(s[j][e]));
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
       const float mean = __fdiv_rn(dw_value(tot), p.hidden_f);
       const uint64_t mean2 = pk(mean, mean);
       char* rrow = RES ? static_cast<char*>(p.res_out) + row * p.res_stride : nullptr;
-      DW2 accq[2] = {{0ull, 0ull}, {0ull, 0ull}};
+      float dmax = 0.f;  // the largest |d| of the thread's chunks (NaN-propagating)
 #pragma unroll
       for (int j = 0; j < NCH; ++j) {
         const Where w = where(j);
@@ -417,11 +424,29 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
             s[j][2 * e] = df.x;
             s[j][2 * e + 1] = df.y;
             // (a piece past the row holds zeros, not values of s: no deviation of it is summed)
-            if (!PIECE || e < V / 4 || w.vb) dw2_add_nonneg(accq[e & 1], mul_x2(dv, dv));  // fl32(d * d), through max / min
+            if (!PIECE || e < V / 4 || w.vb) dmax = max_nan(dmax, max_nan(fabsf(df.x), fabsf(df.y)));
           }
         }
       }
-      DW tot2 = dw_warp_allreduce(dw_combine(dw2_fold(accq[0]), dw2_fold(accq[1])));
+      // the squares fl32(d * d) (scalar mul.rn: never fused into the adds) in chains offset by
+      // the largest square, as RMSNorm's (fp16 65536 x 8192 variant: 415 against 426 us with
+      // chains ordered by a max / min pair)
+      const float Bq = pow2_floor(__fmul_rn(dmax, dmax));
+      DW2 accq[2] = {{pk(Bq, Bq), 0ull}, {pk(Bq, Bq), 0ull}};
+#pragma unroll
+      for (int j = 0; j < NCH; ++j) {
+        const Where w = where(j);
+        if (w.va) {
+#pragma unroll
+          for (int e = 0; e < V / 2; ++e)
+            if (!PIECE || e < V / 4 || w.vb)
+              dwb_add(accq[e & 1], pk(__fmul_rn(s[j][2 * e], s[j][2 * e]), __fmul_rn(s[j][2 * e + 1], s[j][2 * e + 1])));
+        }
+      }
+      DW q0, q1, q2, q3;
+      dwb_split(accq[0], Bq, q0, q1);
+      dwb_split(accq[1], Bq, q2, q3);
+      DW tot2 = dw_warp_allreduce(dw_combine(dw_combine(q0, q1), dw_combine(q2, q3)));
       if (G > 1 && !group_reduce(tot2, partials, bars, 2 * stages, g, NRED, 2 + (int)(it & 1u), G, G8, wg, lane,
                                  it, p, dw_combine))
         return;
