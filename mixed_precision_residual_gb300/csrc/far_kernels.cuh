@@ -398,7 +398,10 @@ __global__ void __launch_bounds__(max_threads(NCH, packed_rows(RES, ACT) && !LN)
 
     float rstd;
     if constexpr (LN) {
-      // LayerNorm: mean from the exact-per-addition signed sum; then d = s - mean in place,
+      // LayerNorm: mean from the exact-per-addition signed sum (each addition is exact, but the
+      // low parts are plain binary32 sums: where values of opposite sign cancel to a sum far
+      // below the row's partial sums, their rounding can leave the sum some ulps from the
+      // correctly rounded one; on rows without such cancellation it is that value); then d = s - mean in place,
       // residual_out stored from s on the way, and the sum of the squared deviations
       DW tot = dw_warp_allreduce_signed(dw_combine_signed(dw2_fold(accp[0]), dw2_fold(accp[1])));
       if (G > 1 && !group_reduce(tot, partials, bars, 2 * stages, g, NRED, (int)(it & 1u), G, G8, wg, lane, it, p,

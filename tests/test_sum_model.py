@@ -188,3 +188,129 @@ def test_chains_from_zero_lose_exactness():
             if Fraction(float(ss)) + Fraction(float(tt)) != Fraction(float(a)) + Fraction(float(b)):
                 inexact += 1
     assert inexact > 0
+
+
+# ---------------------------------------------------------------------------
+# LayerNorm's mean: a signed sum. Each thread's values go into two packed pairs of chains:
+# the pair of even pairs by the ordered Fast2Sum (the operand of larger magnitude first),
+# the pair of odd pairs by TwoSum; both are exact for any signs. The halves are folded with
+# TwoSum and the double words reduced across lanes and warps with TwoSum.
+# ---------------------------------------------------------------------------
+
+def _ordered_fast2sum(h, v):
+    with np.errstate(invalid="ignore"):
+        first = np.abs(h) >= np.abs(v)
+        big, small = np.where(first, h, v).astype(f32), np.where(first, v, h).astype(f32)
+        return _fast2sum(big, small)
+
+
+def model_signed_sum(rows, G, steps=None):
+    R, H = rows.shape
+    V = 8
+    C = (H + V - 1) // V
+    nch = (C + 32 * G - 1) // (32 * G)
+    pad = np.zeros((R, nch * G * 32 * V), f32)
+    pad[:, :H] = rows
+    x = pad.reshape(R, nch, G, 32, V)
+    with np.errstate(over="ignore", invalid="ignore"):
+        hi = [np.zeros((R, G, 32), f32) for _ in range(4)]  # chains: 2 * (pair parity) + half
+        lo = [np.zeros((R, G, 32), f32) for _ in range(4)]
+        for j in range(nch):
+            for e in range(V // 2):
+                for half in range(2):
+                    k = 2 * (e & 1) + half
+                    v = x[:, j, :, :, 2 * e + half]
+                    s, t = _two_sum(hi[k], v) if e & 1 else _ordered_fast2sum(hi[k], v)
+                    if steps is not None:
+                        steps.append((hi[k].copy(), v.copy(), s, t))
+                    hi[k], lo[k] = s, (lo[k] + t).astype(f32)
+        d = _combine_signed(_combine_signed((hi[0], lo[0]), (hi[1], lo[1])),
+                            _combine_signed((hi[2], lo[2]), (hi[3], lo[3])))
+        for off in (16, 8, 4, 2, 1):
+            perm = np.arange(32) ^ off
+            d = _combine_signed(d, (d[0][:, :, perm], d[1][:, :, perm]))
+        part = (d[0][:, :, 0], d[1][:, :, 0])
+        G8 = 1
+        while G8 < G:
+            G8 <<= 1
+        t = (np.zeros((R, G8), f32), np.zeros((R, G8), f32))
+        t[0][:, :G], t[1][:, :G] = part
+        off = G8 >> 1
+        while off:
+            perm = np.arange(G8) ^ off
+            t = _combine_signed(t, (t[0][:, perm], t[1][:, perm]))
+            off >>= 1
+        h, l = t[0][:, 0], t[1][:, 0]
+        return np.where(np.isfinite(h), (h + l).astype(f32), h).astype(f32)
+
+
+def _rn32(q):
+    """The binary32 value nearest the rational q, ties to even (q within the finite range)."""
+    c = np.float32(float(q))
+    best = None
+    for cand in (np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))):
+        dist = abs(Fraction(float(cand)) - q)
+        key = (dist, int(cand.view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, cand)
+    return best[1]
+
+
+def _signed_rows(kind, R, H, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "workload":
+        return far_gen.custom_inputs("f32", "f32", R, H, seed=seed)["x"].numpy()
+    if kind == "offset":  # a large mean over a small spread
+        return (1000.0 + rng.standard_normal((R, H))).astype(f32)
+    if kind == "cancelling":  # pairs of huge opposite values over small ones, in random lanes
+        x = rng.standard_normal((R, H)).astype(f32)
+        for r in range(R):
+            i, k = rng.choice(H, 2, replace=False)
+            big = f32(rng.uniform(1, 2) * 2.0 ** 40)
+            x[r, i], x[r, k] = big, -big
+        return x
+    if kind == "wide":
+        return (rng.choice([-1.0, 1.0], (R, H)) * np.exp2(rng.uniform(-100, 60, (R, H)))).astype(f32)
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["workload", "offset", "wide"])
+@pytest.mark.parametrize("H,G", [(8192, 4), (5120, 2), (1000, 1)])
+def test_mean_chains_give_the_correctly_rounded_sum(kind, H, G):
+    rows = _signed_rows(kind, 40, H, seed=H * 7 + G)
+    got = model_signed_sum(rows, G)
+    want = np.array([_rn32(sum((Fraction(float(v)) for v in r), Fraction(0))) for r in rows], f32)
+    assert _same(got, want), np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0][:10]
+
+
+@pytest.mark.parametrize("H,G", [(8192, 4), (5120, 2), (1000, 1)])
+def test_mean_under_cancellation_stays_within_its_bound(H, G):
+    """Where the row's partial sums dwarf its sum (two values of +-1.5 * 2^40 that cancel
+    among N(0, 1) ones), the chains are still exact at every step, but the low parts that
+    carry the small values are plain binary32 sums: their rounding errors, at most 2^-24 of
+    each partial low sum, add up to a few tens of ulps of the mean's sum. Checked: the
+    double word is within (chain length + 16) * 2^-24 * sum |t| of the exact sum, t the
+    steps' error terms, and some rows do round differently (the limitation is real)."""
+    rows = _signed_rows("cancelling", 40, H, seed=H * 7 + G)
+    steps = []
+    got = model_signed_sum(rows, G, steps=steps)
+    chain_len = len(steps) // 4
+    abs_t = sum(np.abs(t.astype(np.float64)).sum(axis=(1, 2)) for _, _, _, t in steps)  # per row
+    off = 0
+    for r in range(len(rows)):
+        exact = sum((Fraction(float(v)) for v in rows[r]), Fraction(0))
+        bound = Fraction((chain_len + 16) * abs_t[r]) * Fraction(1, 1 << 24) + abs(exact) * Fraction(1, 1 << 24)
+        assert abs(Fraction(float(got[r])) - exact) <= bound, r
+        off += got[r] != _rn32(exact)
+    assert off > 0
+
+
+def test_every_mean_step_is_exact():
+    """Each step of both kinds of chain: s + t equals hi + v exactly (rationals)."""
+    for kind in ("wide", "cancelling", "offset"):
+        rows = _signed_rows(kind, 3, 1024, seed=11)
+        steps = []
+        model_signed_sum(rows, 1, steps=steps)
+        for hi, v, s, t in steps:
+            for a, b, ss, tt in zip(hi.ravel()[::3], v.ravel()[::3], s.ravel()[::3], t.ravel()[::3]):
+                assert Fraction(float(ss)) + Fraction(float(tt)) == Fraction(float(a)) + Fraction(float(b))
