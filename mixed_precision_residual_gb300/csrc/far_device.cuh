@@ -242,7 +242,10 @@ template <int N> __device__ __forceinline__ void store_bytes(void* p, const uint
 // All terms are non-negative, so ordering the pair with max/min makes Dekker's
 // Fast2Sum exact (|a| >= |b|); the NaN-propagating max/min keep a NaN square
 // from being dropped.  Every add carries an explicit rounding intrinsic, so
-// nothing is contracted into an FMA.
+// nothing is contracted into an FMA.  (The generic kernel adds its squares this
+// way, one at a time; the staged kernel, which holds a thread's values in
+// registers, uses the packed chains offset by the largest square further below,
+// which need no ordering.)
 
 struct DW {
   float hi, lo;
